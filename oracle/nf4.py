@@ -1,0 +1,268 @@
+"""NF4 quantization with double quantization -- CPU oracle (test infrastructure only).
+
+What the pages fix:
+  * 4-bit NormalFloat (NF4) is a 4-bit data type that is information-
+    theoretically optimal for normally distributed weights and beats 4-bit
+    integers and 4-bit floats (arXiv 2305.14314 abstract page, innovation (a);
+    QLoRA news write-up, list of innovations, first item).
+  * Quantization is blockwise with one quantization constant per block, and
+    double quantization quantizes those constants, saving about 0.37 bit per
+    parameter, about 3 GB for a 65B model (news write-up, "Double
+    Quantization" item; Finnish summary, item (2)).
+
+Readings taken where the pages are silent (each is listed in the design doc):
+  R1 Codebook.  "Quantiles of N(0,1) normalised to [-1, 1] with an exact zero":
+     16 levels with both endpoints and an exact zero cannot be symmetric, so
+     the positive side gets 8 levels and the negative side 7.  The positive
+     levels are the standard-normal quantiles at 8 probabilities equally
+     spaced from DELTA down towards 1/2 (9 points, the 1/2 end dropped), the
+     negative levels are the negated quantiles at 7 probabilities equally
+     spaced from DELTA towards 1/2 (8 points, the 1/2 end dropped), zero is
+     added, and everything is divided by the quantile at DELTA so the
+     endpoints are exactly -1 and +1.  DELTA = 1 - (1/32 + 1/30)/2, the mean
+     of the outermost tail probabilities of symmetric 16- and 15-level
+     quantile grids.  The levels are built in fp64 and rounded once to fp32;
+     those 16 fp32 values are the codebook.
+  R2 Block size 64 over consecutive elements of a row-major matrix (every row
+     length is a multiple of 64, so blocks never straddle rows).
+  R3 The code of an element is the index of the nearest codebook level to
+     x = fl32(w / absmax); an exact tie goes to the lower index.  An all-zero
+     block (absmax 0) codes every element as the zero level (index 7).
+  R4 Nibble packing: element 2j goes to the high nibble of byte j.
+  R5 Double quantization: the second level is a symmetric linear int8 code of
+     the mean-subtracted block absmax values in groups of 256 consecutive
+     blocks: mu = fl32(S / n_b) with S the fp64 sum of all block absmax values
+     (exact for real weights, checked); c = fl32(absmax - mu);
+     step = fl32(max|c| / 127) per group; code = clamp(rne(fl32(c / step)),
+     -127, 127) (0 when step is 0).  Decode: fl32(fl32(code * step) + mu),
+     with no fused multiply-add.
+  R6 Dequantized weight: w_hat = bf16_rne(fl32(q[code] * absmax_hat)).
+
+Parity: the codebook, coding, packing, DQ and dequantization are pinned by
+tests against closed forms, brute force and error bounds; the exact codebook
+digits, R3's tie rule, R4's order and R5's int8-linear second level are
+conventions (no page prints them): parity unpinned for those choices as such,
+they are fixed by reading.
+"""
+import math
+
+import numpy as np
+from scipy.special import ndtri
+
+from .bf16 import bf16_bits_to_f32, f32_to_bf16_bits
+
+BLOCKSIZE = 64
+DQ_BLOCKSIZE = 256
+ZERO_CODE = 7
+
+# R1: outer probability of the asymmetric quantile grid.
+DELTA = 1.0 - 0.5 * (1.0 / 32.0 + 1.0 / 30.0)
+
+
+def normal_quantile(p):
+    """Standard normal quantile Phi^-1(p) in fp64 (scipy's ndtri)."""
+    return ndtri(np.asarray(p, dtype=np.float64))
+
+
+def nf4_probabilities():
+    """Probabilities whose quantiles give the positive and negative levels (R1)."""
+    pos = np.linspace(DELTA, 0.5, 9)[:-1]  # 8 values, DELTA first
+    neg = np.linspace(DELTA, 0.5, 8)[:-1]  # 7 values, DELTA first
+    return pos, neg
+
+
+def nf4_levels_f64():
+    """The 16 NF4 levels in fp64, ascending (R1)."""
+    pos_p, neg_p = nf4_probabilities()
+    z_max = normal_quantile(DELTA)
+    pos = normal_quantile(pos_p) / z_max
+    neg = -normal_quantile(neg_p) / z_max
+    levels = np.sort(np.concatenate([neg, [0.0], pos]))
+    return levels
+
+
+def nf4_levels():
+    """The NF4 codebook: the fp64 levels rounded once to fp32 (R1)."""
+    return nf4_levels_f64().astype(np.float32)
+
+
+def nf4_midpoints():
+    """Decision thresholds t_j = (q_j + q_{j+1}) / 2 of the fp32 codebook, exact in fp64."""
+    q = nf4_levels().astype(np.float64)
+    return (q[:-1] + q[1:]) / 2.0
+
+
+def nearest_code(x):
+    """Index of the nearest fp32 codebook level to each fp32 x (ties to the lower index, R3).
+
+    code = #{ j : x > t_j } over the 15 exact fp64 midpoints.
+    """
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    t = nf4_midpoints()
+    return (x[..., None] > t).sum(axis=-1).astype(np.uint8)
+
+
+def block_absmax(w_f32, blocksize=BLOCKSIZE):
+    """Per-block max |w| over consecutive groups of `blocksize` in each row (R2).
+
+    w_f32: (rows, cols) float32 with cols % blocksize == 0.
+    Returns float32 (rows, cols // blocksize).
+    """
+    rows, cols = w_f32.shape
+    assert cols % blocksize == 0
+    return np.abs(w_f32.reshape(rows, cols // blocksize, blocksize)).max(axis=2)
+
+
+def nf4_codes(w_f32, absmax, blocksize=BLOCKSIZE):
+    """NF4 code of every element, given its block's absmax (R3).
+
+    x = fl32(w / absmax) as an IEEE single division; all-zero blocks code to 7.
+    """
+    rows, cols = w_f32.shape
+    nb = cols // blocksize
+    w3 = w_f32.reshape(rows, nb, blocksize)
+    m = absmax.reshape(rows, nb, 1).astype(np.float32)
+    zero = m == 0
+    safe = np.where(zero, np.float32(1.0), m)
+    x = (w3 / safe).astype(np.float32)
+    codes = nearest_code(x)
+    codes = np.where(zero, np.uint8(ZERO_CODE), codes)
+    return codes.reshape(rows, cols)
+
+
+def pack_nibbles(codes):
+    """Pack codes two per byte, element 2j in the high nibble of byte j (R4)."""
+    c = np.asarray(codes, dtype=np.uint8).reshape(-1)
+    assert c.size % 2 == 0
+    return ((c[0::2] << 4) | c[1::2]).astype(np.uint8)
+
+
+def unpack_nibbles(packed):
+    """Inverse of pack_nibbles."""
+    p = np.asarray(packed, dtype=np.uint8).reshape(-1)
+    out = np.empty(p.size * 2, dtype=np.uint8)
+    out[0::2] = p >> 4
+    out[1::2] = p & 0x0F
+    return out
+
+
+def exact_sum_f64(values_f32):
+    """fp64 sum of non-negative fp32 values, and whether fp64 holds it exactly.
+
+    The sum is computed exactly in integer arithmetic (every fp32 value is an
+    integer multiple of 2**g for the smallest exponent g present) and then
+    rounded once to fp64.  When the exact sum fits in 53 bits, every order of
+    fp64 summation gives this same value.
+    """
+    v = np.asarray(values_f32, dtype=np.float32).reshape(-1)
+    nz = v[v != 0].astype(np.float64)
+    if nz.size == 0:
+        return 0.0, True
+    mant, expo = np.frexp(nz)  # nz = mant * 2**expo, 0.5 <= mant < 1
+    k = (mant * 2.0 ** 24).astype(np.int64)  # exact: fp32 has 24 significant bits
+    e = expo.astype(np.int64) - 24
+    g = int(e.min())
+    span = int(e.max()) - g
+    if span + 24 + math.ceil(math.log2(nz.size + 1)) <= 62:
+        total = int(np.sum(k << (e - g)))
+    else:
+        total = sum(int(ki) << int(ei - g) for ki, ei in zip(k, e))
+    tz = (total & -total).bit_length() - 1
+    exact = (total >> tz).bit_length() <= 53
+    return math.ldexp(float(total), g) if exact else float(
+        math.fsum(nz.tolist())), exact
+
+
+def double_quantize(absmax, dq_blocksize=DQ_BLOCKSIZE):
+    """Second-level int8 code of the mean-subtracted block absmax values (R5).
+
+    absmax: float32 vector of n_b block absmax values in block order
+    (row-major over (row, block-in-row)).
+    Returns (code int8[n_b], step float32[n_2], mean float32, mean_exact bool).
+    """
+    a = np.asarray(absmax, dtype=np.float32).reshape(-1)
+    n_b = a.size
+    S, exact = exact_sum_f64(a)
+    mean = np.float32(S / float(n_b))
+    c = (a - mean).astype(np.float32)
+    n_2 = (n_b + dq_blocksize - 1) // dq_blocksize
+    code = np.zeros(n_b, dtype=np.int8)
+    step = np.zeros(n_2, dtype=np.float32)
+    for g in range(n_2):
+        cg = c[g * dq_blocksize:(g + 1) * dq_blocksize]
+        a2 = np.float32(np.abs(cg).max())
+        st = np.float32(a2 / np.float32(127.0))
+        step[g] = st
+        if st == 0:
+            continue
+        r = np.rint((cg / st).astype(np.float32))
+        code[g * dq_blocksize:(g + 1) * dq_blocksize] = np.clip(r, -127, 127).astype(np.int8)
+    return code, step, mean, exact
+
+
+def double_dequantize(code, step, mean, dq_blocksize=DQ_BLOCKSIZE):
+    """absmax_hat = fl32(fl32(code * step) + mean), no FMA (R5)."""
+    code = np.asarray(code, dtype=np.int8).reshape(-1)
+    st = np.repeat(np.asarray(step, dtype=np.float32), dq_blocksize)[:code.size]
+    prod = (code.astype(np.float32) * st).astype(np.float32)
+    return (prod + np.float32(mean)).astype(np.float32)
+
+
+def dequantize_codes(codes, absmax_hat, blocksize=BLOCKSIZE):
+    """w_hat = bf16_rne(fl32(q[code] * absmax_hat)) (R6); returns bf16 bits, same shape as codes."""
+    rows, cols = codes.shape
+    q = nf4_levels()
+    vals = q[codes.astype(np.int64)].reshape(rows, cols // blocksize, blocksize)
+    prod = (vals * absmax_hat.reshape(rows, cols // blocksize, 1).astype(np.float32)).astype(np.float32)
+    return f32_to_bf16_bits(prod.reshape(rows, cols))
+
+
+def quantize(w_bits, blocksize=BLOCKSIZE, dq_blocksize=DQ_BLOCKSIZE):
+    """Quantize a bf16 (rows, cols) weight matrix given as uint16 bit patterns.
+
+    Returns a dict with: rows, cols, blocksize, dq_blocksize, packed (uint8,
+    rows*cols/2), absmax (float32, n_b), and, when dq_blocksize > 0, code
+    (int8, n_b), step (float32, n_2), mean (float32), mean_exact (bool).
+    """
+    w_bits = np.asarray(w_bits, dtype=np.uint16)
+    rows, cols = w_bits.shape
+    w = bf16_bits_to_f32(w_bits)
+    absmax = block_absmax(w, blocksize)
+    codes = nf4_codes(w, absmax, blocksize)
+    out = dict(rows=rows, cols=cols, blocksize=blocksize, dq_blocksize=dq_blocksize,
+               packed=pack_nibbles(codes), absmax=absmax.reshape(-1))
+    if dq_blocksize:
+        code, step, mean, exact = double_quantize(absmax.reshape(-1), dq_blocksize)
+        out.update(code=code, step=step, mean=mean, mean_exact=exact)
+    return out
+
+
+def absmax_hat(qt):
+    """The block constants the dequantizer uses: decoded DQ values, or the fp32 absmax."""
+    if qt["dq_blocksize"]:
+        return double_dequantize(qt["code"], qt["step"], qt["mean"], qt["dq_blocksize"])
+    return np.asarray(qt["absmax"], dtype=np.float32)
+
+
+def dequantize(qt, rows=None):
+    """Dequantize a quantized tensor to bf16 bits (rows x cols), optionally only some rows."""
+    R, C, bs = qt["rows"], qt["cols"], qt["blocksize"]
+    codes = unpack_nibbles(qt["packed"]).reshape(R, C)
+    mh = absmax_hat(qt).reshape(R, C // bs)
+    if rows is not None:
+        codes, mh = codes[rows], mh[rows]
+    return dequantize_codes(codes, mh, bs)
+
+
+def constant_bits_per_param(rows, cols, blocksize=BLOCKSIZE, dq_blocksize=DQ_BLOCKSIZE):
+    """Bits of quantization constants per parameter, counted from the stored arrays.
+
+    Without DQ: one fp32 absmax per block.  With DQ: one int8 code per block,
+    one fp32 step per group of dq_blocksize blocks, one fp32 mean per tensor.
+    """
+    n = rows * cols
+    n_b = n // blocksize
+    if not dq_blocksize:
+        return 32.0 * n_b / n
+    n_2 = (n_b + dq_blocksize - 1) // dq_blocksize
+    return (8.0 * n_b + 32.0 * n_2 + 32.0) / n
