@@ -1,0 +1,157 @@
+// C entry points of libqlora: argument checks, workspace layout, dispatch.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+#include "linear.cuh"
+
+namespace ql {
+
+namespace {
+thread_local char g_msg[512] = "";
+__device__ int g_status;
+}  // namespace
+
+int set_error(int code, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int check_cuda(cudaError_t e, const char *what) {
+  if (e == cudaSuccess) return QL_OK;
+  return set_error(QL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int *device_status_ptr() {
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+  return static_cast<int *>(p);
+}
+
+namespace {
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int check_tensor(const ql_nf4_tensor *q, const char *fn, bool need_absmax_dq_off) {
+  if (!q) return set_error(QL_ERR_INVALID, "%s: null nf4 tensor", fn);
+  if (q->rows <= 0 || q->cols <= 0)
+    return set_error(QL_ERR_INVALID, "%s: non-positive weight shape %lld x %lld", fn,
+                     (long long)q->rows, (long long)q->cols);
+  if (q->blocksize != 64) return set_error(QL_ERR_UNSUPPORTED, "%s: blocksize %d (only 64)", fn, q->blocksize);
+  if (q->dq_blocksize != 0 && q->dq_blocksize != 256)
+    return set_error(QL_ERR_UNSUPPORTED, "%s: dq_blocksize %d (only 0 or 256)", fn, q->dq_blocksize);
+  if (q->cols % 64) return set_error(QL_ERR_UNSUPPORTED, "%s: cols %lld not a multiple of 64", fn, (long long)q->cols);
+  if (!q->packed) return set_error(QL_ERR_INVALID, "%s: null packed", fn);
+  if (!aligned(q->packed, 16)) return set_error(QL_ERR_MISALIGNED, "%s: packed not 16-byte aligned", fn);
+  if (q->dq_blocksize) {
+    if (!q->absmax_code || !q->dq_step || !q->dq_mean)
+      return set_error(QL_ERR_INVALID, "%s: null double-quant array", fn);
+    if (!aligned(q->absmax_code, 16) || !aligned(q->dq_step, 16) || !aligned(q->dq_mean, 4))
+      return set_error(QL_ERR_MISALIGNED, "%s: double-quant array misaligned", fn);
+  } else if (need_absmax_dq_off) {
+    if (!q->absmax) return set_error(QL_ERR_INVALID, "%s: null absmax", fn);
+    if (!aligned(q->absmax, 16)) return set_error(QL_ERR_MISALIGNED, "%s: absmax not 16-byte aligned", fn);
+  }
+  return QL_OK;
+}
+
+// quantize workspace: [fp64 sum | pad to 256][fp32 absmax n_b (double quant only)]
+size_t quantize_ws(int64_t N, int64_t K) { return 256 + round_up((size_t)(N * K / 64) * 4, 256); }
+
+}  // namespace
+}  // namespace ql
+
+using namespace ql;
+
+extern "C" size_t ql_workspace_size(int op, int64_t M, int64_t N, int64_t K, int32_t r) {
+  switch (op) {
+    case QL_OP_QUANTIZE: return quantize_ws(N, K);
+    case QL_OP_DEQUANTIZE: return 0;
+    case QL_OP_LINEAR_FWD: return linear_fwd_ws(M, N, K, r);
+    case QL_OP_LINEAR_BWD: return linear_bwd_ws(M, N, K, r);
+    default: return (size_t)-1;
+  }
+}
+
+extern "C" const char *ql_last_error(void) { return g_msg; }
+
+extern "C" int ql_get_device_status(ql_stream_t stream) {
+  int rc = check_cuda(cudaStreamSynchronize(stream), "ql_get_device_status: synchronize");
+  if (rc) return rc;
+  int v = 0;
+  rc = check_cuda(cudaMemcpyFromSymbol(&v, g_status, sizeof(int)), "ql_get_device_status: read");
+  if (rc) return rc;
+  if (v != kStatusOk) {
+    int z = 0;
+    cudaMemcpyToSymbol(g_status, &z, sizeof(int));
+    return set_error(QL_ERR_TIMEOUT, "a kernel gave up waiting (status %d)", v);
+  }
+  return QL_OK;
+}
+
+extern "C" int nf4_quantize(const uint16_t *W, const ql_nf4_tensor *q, void *ws, size_t ws_bytes,
+                            ql_stream_t stream) {
+  g_msg[0] = 0;
+  int rc = check_tensor(q, "nf4_quantize", true);
+  if (rc) return rc;
+  if (!W) return set_error(QL_ERR_INVALID, "nf4_quantize: null W");
+  if (!aligned(W, 16)) return set_error(QL_ERR_MISALIGNED, "nf4_quantize: W not 16-byte aligned");
+  if (!ws) return set_error(QL_ERR_INVALID, "nf4_quantize: null workspace");
+  if (!aligned(ws, 256)) return set_error(QL_ERR_MISALIGNED, "nf4_quantize: workspace not 256-byte aligned");
+  if (ws_bytes < quantize_ws(q->rows, q->cols))
+    return set_error(QL_ERR_UNSUPPORTED, "nf4_quantize: workspace %zu < %zu bytes", ws_bytes,
+                     quantize_ws(q->rows, q->cols));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  double *sum = static_cast<double *>(ws);
+  float *absmax = q->dq_blocksize ? reinterpret_cast<float *>(static_cast<char *>(ws) + 256) : q->absmax;
+  const int64_t n_b = q->rows * q->cols / 64;
+  rc = check_cuda(cudaMemsetAsync(sum, 0, sizeof(double), st), "nf4_quantize: clear sum");
+  if (rc) return rc;
+  rc = check_cuda(launch_quantize(W, q->rows, q->cols, q->packed, absmax, sum, st), "nf4_quantize: launch");
+  if (rc || !q->dq_blocksize) return rc;
+  return check_cuda(launch_double_quant(absmax, n_b, q->dq_blocksize, sum, q->absmax_code, q->dq_step,
+                                        q->dq_mean, st),
+                    "nf4_quantize: double-quant launch");
+}
+
+extern "C" int nf4_dequantize(const ql_nf4_tensor *q, uint16_t *W_out, ql_stream_t stream) {
+  g_msg[0] = 0;
+  int rc = check_tensor(q, "nf4_dequantize", true);
+  if (rc) return rc;
+  if (!W_out) return set_error(QL_ERR_INVALID, "nf4_dequantize: null output");
+  if (!aligned(W_out, 16)) return set_error(QL_ERR_MISALIGNED, "nf4_dequantize: output not 16-byte aligned");
+  return check_cuda(launch_dequantize(*q, W_out, reinterpret_cast<cudaStream_t>(stream)),
+                    "nf4_dequantize: launch");
+}
+
+extern "C" int qlora_linear_fwd(const uint16_t *X, int64_t M, const ql_nf4_tensor *W, const uint16_t *A,
+                                const uint16_t *B, int32_t r, float scale, uint16_t *Y, uint16_t *XA_out,
+                                void *ws, size_t ws_bytes, ql_stream_t stream) {
+  g_msg[0] = 0;
+  int rc = check_tensor(W, "qlora_linear_fwd", true);
+  if (rc) return rc;
+  LinearArgs a{};
+  a.X = X; a.M = M; a.W = *W; a.A = A; a.B = B; a.r = r; a.scale = scale;
+  a.Y = Y; a.XA = XA_out; a.ws = ws; a.ws_bytes = ws_bytes;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  return linear_fwd(a);
+}
+
+extern "C" int qlora_linear_bwd(const uint16_t *dY, const uint16_t *X, const uint16_t *XA, int64_t M,
+                                const ql_nf4_tensor *W, const uint16_t *A, const uint16_t *B, int32_t r,
+                                float scale, uint16_t *dX, float *dA, float *dB, void *ws, size_t ws_bytes,
+                                ql_stream_t stream) {
+  g_msg[0] = 0;
+  int rc = check_tensor(W, "qlora_linear_bwd", true);
+  if (rc) return rc;
+  LinearArgs a{};
+  a.dY = dY; a.X = X; a.XA_in = XA; a.M = M; a.W = *W; a.A = A; a.B = B; a.r = r; a.scale = scale;
+  a.dX = dX; a.dA = dA; a.dB = dB; a.ws = ws; a.ws_bytes = ws_bytes;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  return linear_bwd(a);
+}

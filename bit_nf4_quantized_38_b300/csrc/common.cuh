@@ -1,0 +1,66 @@
+// Shared declarations of libqlora's CUDA sources (internal; the public ABI is
+// include/qlora.h).
+#pragma once
+
+#include <cstdint>
+#include <cstddef>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "../../include/qlora.h"
+
+namespace ql {
+
+// ---------------------------------------------------------------------------
+// NF4 codebook, built on the host at load time from its definition (standard
+// normal quantiles normalised to [-1, 1] with an exact zero) and handed to the
+// kernels by value.
+
+constexpr int kCells = 65;  // coding cells of width 1/32 over [-1, 1]
+
+struct Codebook {
+  float q[16];        // levels, ascending, fp32
+  // Coding cells: an fp32 x in [-1, 1] falls in cell c = rne(32 x + 32).
+  // Every cell holds at most one decision threshold; for x in cell c,
+  // code(x) = cell_lo[c] + (x >= cell_u[c]).
+  float cell_u[kCells];  // smallest fp32 above the cell's threshold (or +inf)
+  int32_t cell_lo[kCells];
+};
+
+// Host: the codebook (built once, thread-safe).
+const Codebook &codebook();
+
+// ---------------------------------------------------------------------------
+// errors
+
+int set_error(int code, const char *fmt, ...);
+int check_cuda(cudaError_t e, const char *what);
+
+// Device status word set by bounded waits that give up (one per device).
+enum : int { kStatusOk = 0, kStatusTimeout = 1 };
+int *device_status_ptr();  // device address of the current device's word
+
+// ---------------------------------------------------------------------------
+// small device helpers
+
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// Two fp32 -> packed bf16x2 with IEEE round-to-nearest-even; `lo` lands in the
+// low 16 bits.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// launchers (quant.cu)
+
+cudaError_t launch_quantize(const uint16_t *W, int64_t rows, int64_t cols, uint8_t *packed,
+                            float *absmax, double *sum_acc, cudaStream_t st);
+cudaError_t launch_double_quant(const float *absmax, int64_t n_b, int dq_bs, const double *sum,
+                                int8_t *code, float *step, float *mean, cudaStream_t st);
+cudaError_t launch_dequantize(const ql_nf4_tensor &q, uint16_t *W_out, cudaStream_t st);
+
+}  // namespace ql

@@ -1,0 +1,249 @@
+// NF4 quantization, double quantization of the block constants, and
+// dequantization (QLoRA abstract, innovations (a) and (b); news write-up,
+// "4-bit NormalFloat" and "Double Quantization" items).
+//
+// All three kernels are HBM-bound streams over the weight:
+//   quantize   reads 2 B/param (bf16), writes 0.5 B/param + 4 B/block absmax
+//   double q.  reads 4 B/block, writes 1 B/block + 4 B per 256 blocks
+//   dequantize reads 0.5 B/param + 1 B/block, writes 2 B/param
+// A warp covers 4 consecutive 64-element blocks per step (8 lanes per block,
+// 16 B of bf16 or 4 B of nibbles per lane), so every load and store is a
+// contiguous, fully used 128-512 B run.
+#include "common.cuh"
+
+namespace ql {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;  // warp steps in flight per thread
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// x = fl32(w / m) for |w| <= m, without a division per element: with
+// r = RN(1/m) and x0 = RN(w r), the residual w - x0 m is exact under FMA and
+// RN(x0 + residual * r) is the correctly rounded quotient (Markstein's
+// correction step for division).  Checked exhaustively over every pair of
+// bf16 values with |w| <= m and m in [2^-60, 2^60]: it equals the IEEE
+// quotient whenever |x| >= 2^-12; smaller quotients (only with subnormal w)
+// may differ in the last bit, but every quotient that small codes to the zero
+// level either way.  Blocks with m outside that range take the IEEE division.
+__device__ __forceinline__ float quotient(float w, float m, float r) {
+  float x0 = __fmul_rn(w, r);
+  float res = __fmaf_rn(-x0, m, w);
+  return __fmaf_rn(res, r, x0);
+}
+
+__device__ __forceinline__ uint32_t cell_of(float x) {
+  // rne(32 x + 32) through the 1.5 * 2^23 rounding constant
+  return min(__float_as_uint(__fmaf_rn(x, 32.0f, 12582944.0f)) & 0x7Fu, (uint32_t)(kCells - 1));
+}
+
+__global__ void __launch_bounds__(kThreads)
+k_quantize(const uint4 *__restrict__ W, int64_t n_blocks, Codebook cb, uint32_t *__restrict__ packed,
+           float *__restrict__ absmax, double *__restrict__ sum_acc) {
+  // Coding table, one copy per lane so lookups never conflict on a bank.
+  __shared__ uint2 table[kCells * 32];
+  __shared__ double red[kThreads / 32];
+  for (int i = threadIdx.x; i < kCells * 32; i += kThreads) {
+    int c = i >> 5;
+    table[i] = make_uint2(__float_as_uint(cb.cell_u[c]), (uint32_t)cb.cell_lo[c]);
+  }
+  __syncthreads();
+
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 7;
+  const uint2 *tab = table + lane;
+  const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  double local = 0.0;
+
+  for (int64_t base = warp * 4 * kUnroll; base < n_blocks; base += nwarps * 4 * kUnroll) {
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      int64_t b = base + u * 4 + (lane >> 3);
+      v[u] = b < n_blocks ? ld_stream(W + b * 8 + sub) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      int64_t b = base + u * 4 + (lane >> 3);
+      float w[8];
+      uint32_t words[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        w[2 * i] = bf16lo_to_f32(words[i]);
+        w[2 * i + 1] = bf16hi_to_f32(words[i]);
+      }
+      float m = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(w[e]));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+      if (b >= n_blocks) continue;
+      if (sub == 0) {
+        absmax[b] = m;
+        local += (double)m;
+      }
+      uint32_t out = 0x77777777u;  // all-zero block: the zero level everywhere
+      if (m > 0.0f) {
+        out = 0;
+        const bool fast = m >= 0x1p-60f && m <= 0x1p60f;
+        const float r = __frcp_rn(m);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float x = fast ? quotient(w[e], m, r) : __fdiv_rn(w[e], m);
+          uint2 t = tab[cell_of(x) << 5];
+          uint32_t code = t.y + (x >= __uint_as_float(t.x) ? 1u : 0u);
+          // element 2j -> high nibble of byte j
+          out |= code << (8 * (e >> 1) + ((e & 1) ? 0 : 4));
+        }
+      }
+      packed[b * 8 + sub] = out;
+    }
+  }
+
+  // fp64 sum of this CTA's block absmax values (exact for real weights, so the
+  // order of the atomics does not change the total)
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
+  if (lane == 0) red[threadIdx.x >> 5] = local;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double s = 0.0;
+    for (int i = 0; i < kThreads / 32; ++i) s += red[i];
+    if (s != 0.0) atomicAdd(sum_acc, s);
+  }
+}
+
+__global__ void __launch_bounds__(256)
+k_double_quant(const float *__restrict__ absmax, int64_t n_b, const double *__restrict__ sum,
+               int8_t *__restrict__ code, float *__restrict__ step, float *__restrict__ mean) {
+  __shared__ float red[8];
+  const float mu = __double2float_rn(__ddiv_rn(*sum, (double)n_b));
+  const int64_t g = blockIdx.x;
+  const int64_t i = g * 256 + threadIdx.x;
+  const bool valid = i < n_b;
+  const float c = valid ? __fsub_rn(absmax[i], mu) : 0.0f;
+  float a = fabsf(c);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __syncthreads();
+  float a2 = red[0];
+#pragma unroll
+  for (int k = 1; k < 8; ++k) a2 = fmaxf(a2, red[k]);
+  const float st = __fdiv_rn(a2, 127.0f);
+  if (valid) {
+    int k = 0;
+    if (st != 0.0f) {
+      float t = rintf(__fdiv_rn(c, st));
+      t = fminf(fmaxf(t, -127.0f), 127.0f);
+      k = (int)t;
+    }
+    code[i] = (int8_t)k;
+  }
+  if (threadIdx.x == 0) {
+    step[g] = st;
+    if (g == 0) *mean = mu;
+  }
+}
+
+template <bool kDQ>
+__global__ void __launch_bounds__(kThreads)
+k_dequantize(const uint32_t *__restrict__ packed, int64_t n_blocks, const int8_t *__restrict__ code,
+             const float *__restrict__ step, const float *__restrict__ mean,
+             const float *__restrict__ absmax, Codebook cb, uint4 *__restrict__ out) {
+  __shared__ float qtab[16 * 32];  // one copy of the levels per lane
+  for (int i = threadIdx.x; i < 16 * 32; i += kThreads) qtab[i] = cb.q[i >> 5];
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 7;
+  const float *q = qtab + lane;
+  const float mu = kDQ ? *mean : 0.0f;
+  const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  for (int64_t base = warp * 4 * kUnroll; base < n_blocks; base += nwarps * 4 * kUnroll) {
+    uint32_t wd[kUnroll];
+    float mh[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      int64_t b = base + u * 4 + (lane >> 3);
+      wd[u] = 0;
+      mh[u] = 0.0f;
+      if (b < n_blocks) {
+        wd[u] = __ldg(packed + b * 8 + sub);
+        if (kDQ) mh[u] = __fadd_rn(__fmul_rn((float)__ldg(code + b), __ldg(step + (b >> 8))), mu);
+        else mh[u] = __ldg(absmax + b);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      int64_t b = base + u * 4 + (lane >> 3);
+      if (b >= n_blocks) continue;
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // byte j holds elements 2j (high) and 2j+1 (low)
+        uint32_t byte = (wd[u] >> (8 * j)) & 0xFFu;
+        float v0 = __fmul_rn(q[(byte >> 4) << 5], mh[u]);
+        float v1 = __fmul_rn(q[(byte & 15u) << 5], mh[u]);
+        o[j] = pack_bf16x2(v0, v1);
+      }
+      out[b * 8 + sub] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+int grid_for(int64_t n_blocks, int ctas_per_sm) {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  int64_t need = (n_blocks + 4 * kUnroll * (kThreads / 32) - 1) / (4 * kUnroll * (kThreads / 32));
+  int64_t g = (int64_t)sms * ctas_per_sm;
+  if (need < g) g = need;
+  return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const uint16_t *W, int64_t rows, int64_t cols, uint8_t *packed,
+                            float *absmax, double *sum_acc, cudaStream_t st) {
+  const int64_t n_blocks = rows * cols / 64;
+  k_quantize<<<grid_for(n_blocks, 8), kThreads, 0, st>>>(
+      reinterpret_cast<const uint4 *>(W), n_blocks, codebook(), reinterpret_cast<uint32_t *>(packed),
+      absmax, sum_acc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_double_quant(const float *absmax, int64_t n_b, int dq_bs, const double *sum,
+                                int8_t *code, float *step, float *mean, cudaStream_t st) {
+  (void)dq_bs;  // 256, checked by the caller
+  const int64_t n_2 = (n_b + 255) / 256;
+  k_double_quant<<<(unsigned)n_2, 256, 0, st>>>(absmax, n_b, sum, code, step, mean);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize(const ql_nf4_tensor &q, uint16_t *W_out, cudaStream_t st) {
+  const int64_t n_blocks = q.rows * q.cols / 64;
+  const int g = grid_for(n_blocks, 8);
+  const uint32_t *p = reinterpret_cast<const uint32_t *>(q.packed);
+  uint4 *o = reinterpret_cast<uint4 *>(W_out);
+  if (q.dq_blocksize)
+    k_dequantize<true><<<g, kThreads, 0, st>>>(p, n_blocks, q.absmax_code, q.dq_step, q.dq_mean,
+                                               nullptr, codebook(), o);
+  else
+    k_dequantize<false><<<g, kThreads, 0, st>>>(p, n_blocks, nullptr, nullptr, nullptr, q.absmax,
+                                                codebook(), o);
+  return cudaGetLastError();
+}
+
+}  // namespace ql

@@ -1,0 +1,214 @@
+"""Python binding of libqlora (the C ABI declared in include/qlora.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  PyTorch provides device memory and the current stream.  Importing
+this module raises ImportError when the library has not been built; there is
+no other code path.
+"""
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libqlora.so")
+
+QL_OK, QL_ERR_INVALID, QL_ERR_UNSUPPORTED, QL_ERR_MISALIGNED, QL_ERR_CUDA, QL_ERR_TIMEOUT = range(6)
+OP_QUANTIZE, OP_DEQUANTIZE, OP_LINEAR_FWD, OP_LINEAR_BWD = range(4)
+
+_c_i64, _c_i32, _c_f32, _c_p, _c_sz = (ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
+                                       ctypes.c_void_p, ctypes.c_size_t)
+
+
+class NF4Struct(ctypes.Structure):
+    _fields_ = [("rows", _c_i64), ("cols", _c_i64), ("blocksize", _c_i32), ("dq_blocksize", _c_i32),
+                ("packed", _c_p), ("absmax", _c_p), ("absmax_code", _c_p), ("dq_step", _c_p),
+                ("dq_mean", _c_p)]
+
+
+_SIGNATURES = {
+    "ql_workspace_size": (_c_sz, [ctypes.c_int, _c_i64, _c_i64, _c_i64, _c_i32]),
+    "ql_nf4_codebook": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float)]),
+    "nf4_quantize": (ctypes.c_int, [_c_p, ctypes.POINTER(NF4Struct), _c_p, _c_sz, _c_p]),
+    "nf4_dequantize": (ctypes.c_int, [ctypes.POINTER(NF4Struct), _c_p, _c_p]),
+    "qlora_linear_fwd": (ctypes.c_int, [_c_p, _c_i64, ctypes.POINTER(NF4Struct), _c_p, _c_p, _c_i32,
+                                        _c_f32, _c_p, _c_p, _c_p, _c_sz, _c_p]),
+    "qlora_linear_bwd": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, ctypes.POINTER(NF4Struct), _c_p,
+                                        _c_p, _c_i32, _c_f32, _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p]),
+    "ql_get_device_status": (ctypes.c_int, [_c_p]),
+    "ql_last_error": (ctypes.c_char_p, []),
+}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -m bit_nf4_quantized_38_b300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+class QLError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"libqlora error {code}: {msg}")
+        self.code = code
+
+
+def _check(rc):
+    if rc != QL_OK:
+        raise QLError(rc, lib.ql_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, name, shape=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def workspace_size(op, M=0, N=0, K=0, r=0):
+    return int(lib.ql_workspace_size(op, M, N, K, r))
+
+
+def nf4_codebook():
+    buf = (ctypes.c_float * 16)()
+    _check(lib.ql_nf4_codebook(buf))
+    return [float(v) for v in buf]
+
+
+def device_status(stream=None):
+    """QL_OK, or raises QLError(QL_ERR_TIMEOUT) if a kernel gave up waiting."""
+    _check(lib.ql_get_device_status(_stream(stream)))
+
+
+def _workspace(nbytes, device, ws):
+    if nbytes == 0:
+        return None, 0
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return ws, ws.numel()
+
+
+@dataclass
+class NF4Tensor:
+    """Device storage of an NF4 weight (layout as ql_nf4_tensor in include/qlora.h)."""
+    rows: int
+    cols: int
+    packed: torch.Tensor
+    absmax: torch.Tensor = None
+    absmax_code: torch.Tensor = None
+    dq_step: torch.Tensor = None
+    dq_mean: torch.Tensor = None
+    blocksize: int = 64
+    dq_blocksize: int = 256
+
+    @classmethod
+    def empty(cls, rows, cols, device, dq_blocksize=256, blocksize=64):
+        n_b = rows * cols // blocksize
+        t = cls(rows, cols, torch.empty(rows * cols // 2, dtype=torch.uint8, device=device),
+                blocksize=blocksize, dq_blocksize=dq_blocksize)
+        if dq_blocksize:
+            t.absmax_code = torch.empty(n_b, dtype=torch.int8, device=device)
+            t.dq_step = torch.empty((n_b + dq_blocksize - 1) // dq_blocksize, dtype=torch.float32,
+                                    device=device)
+            t.dq_mean = torch.empty(1, dtype=torch.float32, device=device)
+        else:
+            t.absmax = torch.empty(n_b, dtype=torch.float32, device=device)
+        return t
+
+    def struct(self):
+        return NF4Struct(self.rows, self.cols, self.blocksize, self.dq_blocksize,
+                         _ptr(self.packed), _ptr(self.absmax), _ptr(self.absmax_code),
+                         _ptr(self.dq_step), _ptr(self.dq_mean))
+
+    def nbytes(self):
+        return sum(t.numel() * t.element_size() for t in
+                   (self.packed, self.absmax, self.absmax_code, self.dq_step, self.dq_mean)
+                   if t is not None)
+
+
+def nf4_quantize(W, dq_blocksize=256, blocksize=64, out=None, ws=None, stream=None):
+    """Quantize a bf16 (rows x cols) CUDA tensor to NF4 (+ double quant)."""
+    _need(W, torch.bfloat16, "W")
+    rows, cols = W.shape
+    q = out if out is not None else NF4Tensor.empty(rows, cols, W.device, dq_blocksize, blocksize)
+    ws, nbytes = _workspace(workspace_size(OP_QUANTIZE, 0, rows, cols, 0), W.device, ws)
+    s = q.struct()
+    _check(lib.nf4_quantize(_ptr(W), ctypes.byref(s), _ptr(ws), nbytes, _stream(stream)))
+    return q
+
+
+def nf4_dequantize(q, out=None, stream=None):
+    if out is None:
+        out = torch.empty(q.rows, q.cols, dtype=torch.bfloat16, device=q.packed.device)
+    _need(out, torch.bfloat16, "out", (q.rows, q.cols))
+    s = q.struct()
+    _check(lib.nf4_dequantize(ctypes.byref(s), _ptr(out), _stream(stream)))
+    return out
+
+
+def qlora_linear_fwd(X, q, A, B, scale, Y=None, XA=None, ws=None, stream=None, want_xa=True):
+    """Y = X W_hat^T + scale (X A) B; returns (Y, XA or None)."""
+    M, K = X.shape
+    r = A.shape[1]
+    _need(X, torch.bfloat16, "X", (M, q.cols))
+    _need(A, torch.bfloat16, "A", (q.cols, r))
+    _need(B, torch.bfloat16, "B", (r, q.rows))
+    if Y is None:
+        Y = torch.empty(M, q.rows, dtype=torch.bfloat16, device=X.device)
+    _need(Y, torch.bfloat16, "Y", (M, q.rows))
+    if XA is None and want_xa:
+        XA = torch.empty(M, r, dtype=torch.bfloat16, device=X.device)
+    if XA is not None:
+        _need(XA, torch.bfloat16, "XA", (M, r))
+    ws, nbytes = _workspace(workspace_size(OP_LINEAR_FWD, M, q.rows, q.cols, r), X.device, ws)
+    s = q.struct()
+    _check(lib.qlora_linear_fwd(_ptr(X), M, ctypes.byref(s), _ptr(A), _ptr(B), r, float(scale),
+                                _ptr(Y), _ptr(XA), _ptr(ws), nbytes, _stream(stream)))
+    return Y, XA
+
+
+def qlora_linear_bwd(dY, X, XA, q, A, B, scale, dX=None, dA=None, dB=None, ws=None, stream=None):
+    """Returns (dX bf16, dA fp32, dB fp32)."""
+    M = X.shape[0]
+    r = A.shape[1]
+    _need(dY, torch.bfloat16, "dY", (M, q.rows))
+    _need(X, torch.bfloat16, "X", (M, q.cols))
+    _need(A, torch.bfloat16, "A", (q.cols, r))
+    _need(B, torch.bfloat16, "B", (r, q.rows))
+    if XA is not None:
+        _need(XA, torch.bfloat16, "XA", (M, r))
+    dev = X.device
+    dX = torch.empty(M, q.cols, dtype=torch.bfloat16, device=dev) if dX is None else dX
+    dA = torch.empty(q.cols, r, dtype=torch.float32, device=dev) if dA is None else dA
+    dB = torch.empty(r, q.rows, dtype=torch.float32, device=dev) if dB is None else dB
+    _need(dX, torch.bfloat16, "dX", (M, q.cols))
+    _need(dA, torch.float32, "dA", (q.cols, r))
+    _need(dB, torch.float32, "dB", (r, q.rows))
+    ws, nbytes = _workspace(workspace_size(OP_LINEAR_BWD, M, q.rows, q.cols, r), dev, ws)
+    s = q.struct()
+    _check(lib.qlora_linear_bwd(_ptr(dY), _ptr(X), _ptr(XA), M, ctypes.byref(s), _ptr(A), _ptr(B), r,
+                                float(scale), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(ws), nbytes,
+                                _stream(stream)))
+    return dX, dA, dB

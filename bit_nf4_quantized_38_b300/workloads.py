@@ -128,17 +128,22 @@ def normal_with_outliers_bf16(shape, std, p, factor, seed, device="cpu"):
     return w.to(torch.bfloat16)
 
 
-def student_t4_bf16(shape, std, seed, device="cpu"):
+def student_t4_bf16(shape, std, seed, device="cpu", rows_per_chunk=1024):
     """Student-t with 4 degrees of freedom scaled to standard deviation `std`; bf16.
 
     t = z0 / sqrt((z1^2 + z2^2 + z3^2 + z4^2) / 4) has variance 4 / (4 - 2) = 2,
-    so it is multiplied by std / sqrt(2).
+    so it is multiplied by std / sqrt(2).  Rows are drawn in chunks of
+    `rows_per_chunk` (five normal planes per chunk, in order) to bound memory.
     """
     g = _gen(seed, device)
-    z = torch.randn((5,) + tuple(shape), generator=g, device=device, dtype=torch.float32)
-    chi = (z[1:] ** 2).sum(0) / 4.0
-    t = z[0] / torch.sqrt(chi)
-    return (t * (std / math.sqrt(2.0))).to(torch.bfloat16)
+    rows, cols = shape
+    out = torch.empty((rows, cols), dtype=torch.bfloat16, device=device)
+    for r0 in range(0, rows, rows_per_chunk):
+        r1 = min(rows, r0 + rows_per_chunk)
+        z = torch.randn((5, r1 - r0, cols), generator=g, device=device, dtype=torch.float32)
+        chi = (z[1:] ** 2).sum(0) / 4.0
+        out[r0:r1] = (z[0] / torch.sqrt(chi) * (std / math.sqrt(2.0))).to(torch.bfloat16)
+    return out
 
 
 def case_weight(case, device="cpu"):

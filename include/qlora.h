@@ -1,0 +1,182 @@
+/*
+ * qlora.h -- C ABI of libqlora: the frozen-NF4 linear layer with a LoRA adapter
+ * (QLoRA), hand-written CUDA for B300 (sm_103a).
+ *
+ * The method (arXiv 2305.14314, "QLoRA: Efficient Finetuning of Quantized
+ * LLMs", abstract; the Chinese QLoRA news write-up, list of innovations):
+ * weights are stored as 4-bit NormalFloat (NF4) codes with one constant per
+ * block, the block constants are themselves quantized ("double
+ * quantization"), and gradients flow through the frozen dequantized weights
+ * into low-rank adapters (LoRA tutorial, Lit-LLaMA translation: h = Wx + dWx,
+ * dW = W_A W_B, scale alpha).
+ *
+ * Conventions for every call:
+ *  - Row-major matrices.  bf16 values are passed as their 16-bit patterns
+ *    (uint16_t).  X is M x K (tokens x in), the weight W is N x K (out x in),
+ *    Y is M x N, A is K x r, B is r x N, s = alpha / r.
+ *  - All pointers are DEVICE pointers of the current CUDA device unless
+ *    stated otherwise, 16-byte aligned, and owned by the caller.  The library
+ *    allocates nothing and never synchronises (except ql_get_device_status).
+ *  - Calls are asynchronous and ordered on `stream` (NULL = legacy default).
+ *  - Return codes: QL_OK, or an error code with a message available from
+ *    ql_last_error() (thread-local).  Argument errors are detected on the host
+ *    before any launch.  Inputs must be finite; NaN/Inf behaviour is
+ *    unspecified.
+ *  - Workspace `ws` is caller-owned device scratch of at least
+ *    ql_workspace_size(op, ...) bytes, 256-byte aligned; it may be reused
+ *    between calls that are ordered on the same stream.
+ */
+#ifndef QLORA_H
+#define QLORA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define QL_API __attribute__((visibility("default")))
+#else
+#define QL_API
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *ql_stream_t;
+
+enum ql_status {
+  QL_OK = 0,
+  QL_ERR_INVALID = 1,     /* null pointer, non-positive or inconsistent size */
+  QL_ERR_UNSUPPORTED = 2, /* blocksize != 64, dq_blocksize not 0/256, K % 64,
+                             r not in {8,16,32,64,128}, too small workspace */
+  QL_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned (ws: 256) */
+  QL_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  QL_ERR_TIMEOUT = 5      /* a kernel gave up waiting (see ql_get_device_status) */
+};
+
+enum ql_op {
+  QL_OP_QUANTIZE = 0,
+  QL_OP_DEQUANTIZE = 1,
+  QL_OP_LINEAR_FWD = 2,
+  QL_OP_LINEAR_BWD = 3
+};
+
+/*
+ * A quantized weight (the NF4 storage of QLoRA; BitsAndBytes-style knobs of the
+ * QLoRA project page's configuration example: 4-bit NF4, double quant on/off).
+ *   rows x cols    : N x K of the bf16 weight it came from; cols % 64 == 0.
+ *   blocksize      : 64 elements per first-level block (consecutive in a row).
+ *   dq_blocksize   : 256 first-level blocks per second-level group, or 0 for
+ *                    no double quantization.
+ *   packed         : rows*cols/2 bytes; element 2j of the row-major matrix is
+ *                    the HIGH nibble of byte j, element 2j+1 the low nibble.
+ *   absmax         : n_b = rows*cols/64 floats, the block absmax values.
+ *                    Required when dq_blocksize == 0; ignored otherwise.
+ *   absmax_code    : n_b int8 second-level codes   (dq_blocksize != 0)
+ *   dq_step        : n_2 = ceil(n_b/256) floats     (dq_blocksize != 0)
+ *   dq_mean        : 1 float                         (dq_blocksize != 0)
+ * Block b = row*(cols/64) + j covers row `row`, columns [64j, 64j+64).
+ * Decoded block constant: dq off: absmax[b];
+ *   dq on: fl32(fl32(absmax_code[b] * dq_step[b/256]) + dq_mean[0]).
+ * Dequantized weight: bf16_rne(fl32(q[code] * constant)), q = NF4 codebook.
+ */
+typedef struct {
+  int64_t rows;
+  int64_t cols;
+  int32_t blocksize;
+  int32_t dq_blocksize;
+  uint8_t *packed;
+  float *absmax;
+  int8_t *absmax_code;
+  float *dq_step;
+  float *dq_mean;
+} ql_nf4_tensor;
+
+/*
+ * Bytes of workspace the op needs for the given sizes (M tokens, N out, K in,
+ * r rank; unused sizes may be 0).  Returns 0 when the op needs none, and
+ * (size_t)-1 for an unknown op.
+ */
+QL_API size_t ql_workspace_size(int op, int64_t M, int64_t N, int64_t K, int32_t r);
+
+/*
+ * The 16 NF4 levels (ascending, fp32) the kernels use, written to host
+ * memory `out16`.  Built at library load from the definition: standard-normal
+ * quantiles normalised to [-1, 1] with an exact zero (8 positive levels,
+ * 7 negative).  Returns QL_OK.
+ */
+QL_API int ql_nf4_codebook(float *out16);
+
+/*
+ * NF4 quantization with optional double quantization (QLoRA abstract,
+ * innovations (a) and (b); news write-up: "Double Quantization" saves about
+ * 0.37 bit per parameter).
+ *   W  : rows x cols bf16 (device), finite.
+ *   q  : host struct describing the device outputs (all written).
+ *   ws : ql_workspace_size(QL_OP_QUANTIZE, 0, rows, cols, 0) bytes.
+ * Block absmax m = max|w| over 64 elements; code = index of the nearest NF4
+ * level to fl32(w / m) (ties to the lower index; all-zero block -> code 7).
+ * Double quant: mu = fl32(S / n_b) with S the fp64 sum of all m (exact when
+ * the exponents of the block absmax values span fewer than
+ * 45 - log2(n_b) binades, which holds for real weights); per 256 blocks
+ * step = fl32(max|fl32(m - mu)| / 127), code = clamp(rne(fl32((m-mu)/step)),
+ * -127, 127) (0 when step == 0).  Results are deterministic.
+ */
+QL_API int nf4_quantize(const uint16_t *W, const ql_nf4_tensor *q, void *ws,
+                 size_t ws_bytes, ql_stream_t stream);
+
+/*
+ * Dequantize to bf16 (the weight the linear layer computes with).
+ *   q     : host struct of device inputs; W_out : rows x cols bf16 (device).
+ */
+QL_API int nf4_dequantize(const ql_nf4_tensor *q, uint16_t *W_out, ql_stream_t stream);
+
+/*
+ * Forward of the frozen-NF4 linear with LoRA (LoRA tutorial: h = Wx + dWx;
+ * QLoRA abstract: frozen 4-bit weights):
+ *   Y = X W_hat^T + s (X A) B        (fp32 accumulation, bf16 output)
+ *   X  : M x K bf16, A : K x r bf16, B : r x N bf16,  W : N x K NF4 (q).
+ *   Y  : M x N bf16 (output).
+ *   XA_out : M x r bf16 (output, may be NULL): X A rounded to bf16, for the
+ *            backward pass.
+ *   scale  : s = alpha / r.
+ *   ws     : ql_workspace_size(QL_OP_LINEAR_FWD, M, N, K, r) bytes.
+ * M >= 1.  M <= 16 takes the decode (GEMV) path, larger M the tensor-core path.
+ */
+QL_API int qlora_linear_fwd(const uint16_t *X, int64_t M, const ql_nf4_tensor *W,
+                     const uint16_t *A, const uint16_t *B, int32_t r,
+                     float scale, uint16_t *Y, uint16_t *XA_out, void *ws,
+                     size_t ws_bytes, ql_stream_t stream);
+
+/*
+ * Backward of the same layer (QLoRA abstract: gradients back-propagate through
+ * the frozen 4-bit weights into the adapters; the weights get none):
+ *   G  = dY B^T                       (M x r, internal)
+ *   dX = dY W_hat + s G A^T           (M x K bf16 output)
+ *   dA = s X^T G                      (K x r fp32 output, overwritten)
+ *   dB = s (X A)^T dY                 (r x N fp32 output, overwritten)
+ *   XA : M x r bf16 from the forward, or NULL to recompute it from X and A.
+ *   ws : ql_workspace_size(QL_OP_LINEAR_BWD, M, N, K, r) bytes.
+ */
+QL_API int qlora_linear_bwd(const uint16_t *dY, const uint16_t *X, const uint16_t *XA,
+                     int64_t M, const ql_nf4_tensor *W, const uint16_t *A,
+                     const uint16_t *B, int32_t r, float scale, uint16_t *dX,
+                     float *dA, float *dB, void *ws, size_t ws_bytes,
+                     ql_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word, which kernels set when a bounded wait gives up.  Returns QL_OK,
+ * QL_ERR_TIMEOUT, or QL_ERR_CUDA if the synchronisation itself failed.
+ */
+QL_API int ql_get_device_status(ql_stream_t stream);
+
+/* Message for the last error returned on this host thread ("" if none). */
+QL_API const char *ql_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QLORA_H */

@@ -113,21 +113,26 @@ def block_absmax(w_f32, blocksize=BLOCKSIZE):
     return np.abs(w_f32.reshape(rows, cols // blocksize, blocksize)).max(axis=2)
 
 
-def nf4_codes(w_f32, absmax, blocksize=BLOCKSIZE):
+def nf4_codes(w_f32, absmax, blocksize=BLOCKSIZE, rows_per_chunk=512):
     """NF4 code of every element, given its block's absmax (R3).
 
     x = fl32(w / absmax) as an IEEE single division; all-zero blocks code to 7.
+    Rows are processed in chunks only to bound memory.
     """
     rows, cols = w_f32.shape
     nb = cols // blocksize
-    w3 = w_f32.reshape(rows, nb, blocksize)
-    m = absmax.reshape(rows, nb, 1).astype(np.float32)
-    zero = m == 0
-    safe = np.where(zero, np.float32(1.0), m)
-    x = (w3 / safe).astype(np.float32)
-    codes = nearest_code(x)
-    codes = np.where(zero, np.uint8(ZERO_CODE), codes)
-    return codes.reshape(rows, cols)
+    out = np.empty((rows, cols), dtype=np.uint8)
+    for r0 in range(0, rows, rows_per_chunk):
+        r1 = min(rows, r0 + rows_per_chunk)
+        w3 = w_f32[r0:r1].reshape(r1 - r0, nb, blocksize)
+        m = absmax[r0:r1].reshape(r1 - r0, nb, 1).astype(np.float32)
+        zero = m == 0
+        safe = np.where(zero, np.float32(1.0), m)
+        x = (w3 / safe).astype(np.float32)
+        codes = nearest_code(x)
+        codes = np.where(zero, np.uint8(ZERO_CODE), codes)
+        out[r0:r1] = codes.reshape(r1 - r0, cols)
+    return out
 
 
 def pack_nibbles(codes):
