@@ -1,0 +1,382 @@
+// Dequant-in-the-mainloop tensor-core GEMM for the QLoRA linear (sm_103a).
+//
+//   forward  : Y  = [X  | XA] . [W_hat | s B^T]^T      (B tile rows = W rows)
+//   backward : dX = [dY | sG] . [W_hat ; A^T]           (B tile = W_hat^T)
+//
+// The frozen weight W_hat is never materialised: converter warps expand the
+// packed NF4 nibbles of each 64-element block through a 16-entry bf16 table
+// (the block's 16 possible values q[c] * absmax_hat, rounded once) straight
+// into the 128-byte-swizzled shared-memory tile the tensor core reads.  The
+// LoRA branch rides along as extra K-steps whose operands TMA loads directly.
+//
+// One CTA computes a 128 x 256 output tile with tcgen05.mma (M=128, N=256,
+// K=16 per instruction) into a TMEM accumulator of 256 columns:
+//   warp 0      TMA producer (X / dY tiles; LoRA tiles)
+//   warp 1      TMEM allocation and the single MMA-issuing thread
+//   warps 2-5   converters during the main loop, then the epilogue
+// A 4-stage ring of {A 16 KB, B 32 KB} tiles is handed between the roles with
+// mbarriers (full: TMA bytes + 128 converter arrivals; empty: MMA commit).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "tc_gemm.cuh"
+
+namespace ql {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr int CONV_THREADS = 128;
+constexpr int TMEM_COLS = 256;
+constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+
+struct GemmArgs {
+  int M;            // output rows
+  int Nout;         // output columns
+  int ksteps_main;  // 64-wide reduction steps through the NF4 weight
+  int ksteps_lora;  // 64-wide reduction steps through the LoRA operands
+  NF4View w;
+  uint16_t *out;
+  int64_t ldo;
+  int *status;
+  float q[16];
+};
+
+// 8 bf16 values of one 16-byte smem chunk from 8 packed nibbles, through the
+// 16-entry table held as low-byte (TL) and high-byte (TH) planes.  Byte j of
+// `w` holds element 2j in its high nibble and element 2j+1 in its low nibble.
+__device__ __forceinline__ void lookup8(uint32_t w, const uint32_t (&TL)[4], const uint32_t (&TH)[4],
+                                        uint32_t &o0, uint32_t &o1, uint32_t &o2, uint32_t &o3) {
+  using ptx::prmt;
+  // selector: the low 3 bits of every nibble pick a byte among 8 entries
+  const uint32_t s = w & 0x77777777u;
+  // second-level selector: byte i from the first (entries 0-7) or second
+  // (entries 8-15) half, by bit 3 of nibble i
+  const uint32_t s2 = ((w >> 1) & 0x44444444u) | 0x32103210u;
+  {
+    uint32_t L = prmt(prmt(TL[0], TL[1], s), prmt(TL[2], TL[3], s), s2);
+    uint32_t H = prmt(prmt(TH[0], TH[1], s), prmt(TH[2], TH[3], s), s2);
+    // L, H bytes hold elements (1, 0, 3, 2); interleave to bf16 pairs (0,1), (2,3)
+    o0 = prmt(L, H, 0x4051u);
+    o1 = prmt(L, H, 0x6273u);
+  }
+  {
+    const uint32_t sh = s >> 16, s2h = s2 >> 16;
+    uint32_t L = prmt(prmt(TL[0], TL[1], sh), prmt(TL[2], TL[3], sh), s2h);
+    uint32_t H = prmt(prmt(TH[0], TH[1], sh), prmt(TH[2], TH[3], sh), s2h);
+    o2 = prmt(L, H, 0x4051u);
+    o3 = prmt(L, H, 0x6273u);
+  }
+}
+
+// One 64-element row-block: 32 packed bytes and the block constant -> one
+// 128-byte row of a 128B-swizzled tile at `dst` (chunk j stored at j ^ swz).
+__device__ __forceinline__ void convert_rowblock(const uint4 &p0, const uint4 &p1, float mhat,
+                                                 const float (&q)[16], uint32_t dst, uint32_t swz) {
+  uint32_t P[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) P[k] = pack_bf16x2(__fmul_rn(q[2 * k], mhat), __fmul_rn(q[2 * k + 1], mhat));
+  uint32_t TL[4], TH[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    TL[i] = ptx::prmt(P[2 * i], P[2 * i + 1], 0x6420u);
+    TH[i] = ptx::prmt(P[2 * i], P[2 * i + 1], 0x7531u);
+  }
+  const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t o0, o1, o2, o3;
+    lookup8(words[j], TL, TH, o0, o1, o2, o3);
+    ptx::sts128(dst + (((uint32_t)j ^ swz) << 4), o0, o1, o2, o3);
+  }
+}
+
+__device__ __forceinline__ void zero_row(uint32_t dst) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) ptx::sts128(dst + (j << 4), 0, 0, 0, 0);
+}
+
+struct RowBlockSrc {
+  uint4 p0, p1;
+  float mhat;
+  bool valid;
+};
+
+__device__ __forceinline__ RowBlockSrc load_rowblock(const NF4View &w, int64_t n, int64_t kb) {
+  RowBlockSrc r;
+  r.valid = n < w.rows && kb < w.cols / 64;
+  if (r.valid) {
+    const uint8_t *src = w.packed + n * (w.cols >> 1) + kb * 32;
+    r.p0 = ptx::ldg_nc_v4(src);
+    r.p1 = ptx::ldg_nc_v4(src + 16);
+    const int64_t b = n * (w.cols >> 6) + kb;
+    if (w.dq)
+      r.mhat = __fadd_rn(__fmul_rn((float)__ldg(w.code + b), __ldg(w.step + (b >> 8))), __ldg(w.mean));
+    else
+      r.mhat = __ldg(w.absmax + b);
+  } else {
+    r.p0 = r.p1 = make_uint4(0, 0, 0, 0);
+    r.mhat = 0.0f;
+  }
+  return r;
+}
+
+template <bool kTrans>
+__global__ void __launch_bounds__(THREADS, 1)
+k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+           const __grid_constant__ CUtensorMap tmB2, const GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 1);
+  volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  auto full = [&](int s) { return ptx::smem_u32(&bars[s]); };
+  auto empty = [&](int s) { return ptx::smem_u32(&bars[STAGES + s]); };
+  const uint32_t accf = ptx::smem_u32(&bars[2 * STAGES]);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int nsteps = p.ksteps_main + p.ksteps_lora;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(full(s), 1 + CONV_THREADS);
+      ptx::mbar_init(empty(s), 1);
+    }
+    ptx::mbar_init(accf, 1);
+    *abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmA2);
+    ptx::prefetch_tmap(&tmB2);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      for (int ks = 0; ks < nsteps; ++ks) {
+        const int s = ks % STAGES;
+        const uint32_t ph = (ks / STAGES) & 1;
+        if (!ptx::mbar_wait(empty(s), ph ^ 1, abort, p.status)) break;
+        const uint32_t a_dst = sbase + s * STAGE_BYTES;
+        if (ks < p.ksteps_main) {
+          ptx::mbar_arrive_expect_tx(full(s), A_BYTES);
+          ptx::tma_load_2d(a_dst, &tmA, full(s), ks * BK, m0);
+        } else {
+          const int kl = ks - p.ksteps_main;
+          ptx::mbar_arrive_expect_tx(full(s), A_BYTES + B_BYTES);
+          ptx::tma_load_2d(a_dst, &tmA2, full(s), kl * BK, m0);
+          ptx::tma_load_2d(a_dst + A_BYTES, &tmB2, full(s), kl * BK, n0);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc_main = ptx::idesc_bf16(BM, BN, kTrans);
+      constexpr uint32_t idesc_kmaj = ptx::idesc_bf16(BM, BN, false);
+      bool ok = true;
+      for (int ks = 0; ks < nsteps; ++ks) {
+        const int s = ks % STAGES;
+        const uint32_t ph = (ks / STAGES) & 1;
+        if (!ptx::mbar_wait(full(s), ph, abort, p.status)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t a_addr = sbase + s * STAGE_BYTES;
+        const uint32_t b_addr = a_addr + A_BYTES;
+        const bool lora = ks >= p.ksteps_main;
+        const uint64_t a_desc = ptx::desc_sw128(a_addr, 16, 1024);
+        // K-major B: rows of 128 B, 8-row atoms 1024 B apart.  MN-major B
+        // (W_hat^T for dX): atoms of 64 output columns x 8 reduction rows;
+        // 8 K-atoms (1024 B apart) per 8 KB MN-atom column.
+        const bool bmn = kTrans && !lora;
+        const uint64_t b_desc = bmn ? ptx::desc_sw128(b_addr, 8192, 1024) : ptx::desc_sw128(b_addr, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          // K advance of 16 elements: +32 B inside the swizzled row (K-major)
+          // or two 8-row K-atoms = +2048 B (MN-major)
+          const uint64_t ad = a_desc + (uint64_t)(kk * 2);
+          const uint64_t bd = b_desc + (uint64_t)(bmn ? kk * 128 : kk * 2);
+          ptx::mma_bf16(tmem, ad, bd, bmn ? idesc_main : idesc_kmaj, (ks > 0 || kk > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(empty(s));
+      }
+      if (ok) ptx::mma_commit(accf);
+    }
+  } else {
+    // ---------------------------------------------------------------- converters
+    const int ct = threadIdx.x - 64;  // 0..127
+    float q[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) q[i] = p.q[i];
+    // the two row-blocks this thread expands in every stage
+    int64_t rb_n[2], rb_kb0[2];
+    uint32_t rb_dst[2], rb_swz[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = ct + h * 128;
+      if (!kTrans) {
+        rb_n[h] = n0 + i;  // weight row = output column
+        rb_kb0[h] = 0;     // + ks
+        rb_dst[h] = (uint32_t)i * 128u;
+        rb_swz[h] = (uint32_t)(i & 7);
+      } else {
+        const int nl = i & 63, kbl = i >> 6;
+        rb_n[h] = nl;                  // + 64 ks: weight row = reduction index
+        rb_kb0[h] = (n0 >> 6) + kbl;   // weight column block = output columns / 64
+        rb_dst[h] = (uint32_t)((kbl * 8 + (nl >> 3)) * 1024 + (nl & 7) * 128);
+        rb_swz[h] = (uint32_t)(nl & 7);
+      }
+    }
+    auto fetch = [&](int ks, RowBlockSrc (&r)[2]) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (!kTrans) r[h] = load_rowblock(p.w, rb_n[h], rb_kb0[h] + ks);
+        else r[h] = load_rowblock(p.w, rb_n[h] + (int64_t)ks * 64, rb_kb0[h]);
+      }
+    };
+    RowBlockSrc cur[2], nxt[2];
+    if (p.ksteps_main > 0) fetch(0, cur);
+    for (int ks = 0; ks < nsteps; ++ks) {
+      const int s = ks % STAGES;
+      const uint32_t ph = (ks / STAGES) & 1;
+      const bool main_step = ks < p.ksteps_main;
+      if (ks + 1 < p.ksteps_main) fetch(ks + 1, nxt);
+      if (!ptx::mbar_wait(empty(s), ph ^ 1, abort, p.status)) break;
+      if (main_step) {
+        const uint32_t b_addr = sbase + s * STAGE_BYTES + A_BYTES;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (cur[h].valid) convert_rowblock(cur[h].p0, cur[h].p1, cur[h].mhat, q, b_addr + rb_dst[h], rb_swz[h]);
+          else zero_row(b_addr + rb_dst[h]);
+        }
+        ptx::fence_proxy_async_smem();
+      }
+      ptx::mbar_arrive(full(s));
+      if (ks + 1 < p.ksteps_main) {
+        cur[0] = nxt[0];
+        cur[1] = nxt[1];
+      }
+    }
+    // ---------------------------------------------------------------- epilogue
+    if (!*abort && ptx::mbar_wait(accf, 0, abort, p.status)) {
+      ptx::tc_fence_after();
+      const int qd = warp & 3;  // TMEM lane quarter this warp may access
+      const int row = m0 + qd * 32 + lane;
+      uint16_t *orow = p.out + (int64_t)row * p.ldo;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(c * 32), r);
+        ptx::tmem_wait_ld();
+        if (row < p.M) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int col = n0 + c * 32 + j * 8;
+            if (col + 8 <= p.Nout) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
+              v.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
+              v.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
+              v.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
+              *reinterpret_cast<uint4 *>(orow + col) = v;
+            }
+          }
+        }
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) ptx::tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------- host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor [outer][inner] (inner contiguous), box [box_outer][64],
+// 128-byte swizzle, zero fill outside the tensor.
+int make_tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return set_error(QL_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(QL_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return QL_OK;
+}
+
+template <bool kTrans>
+int launch(const GemmProblem &g, cudaStream_t st) {
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    int rc = check_cuda(cudaFuncSetAttribute(k_nf4_gemm<kTrans>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)SMEM_BYTES),
+                        "tensor-core GEMM: shared-memory attribute");
+    if (rc) return rc;
+    attr_done[dev] = true;
+  }
+  CUtensorMap tA, tA2, tB2;
+  int rc = make_tmap(&tA, g.A, (uint64_t)g.Kred, (uint64_t)g.M, BM);
+  if (!rc) rc = make_tmap(&tA2, g.A2, (uint64_t)g.rp, (uint64_t)g.M, BM);
+  if (!rc) rc = make_tmap(&tB2, g.B2, (uint64_t)g.rp, (uint64_t)g.Nout, BN);
+  if (rc) return rc;
+  GemmArgs a{};
+  a.M = (int)g.M;
+  a.Nout = (int)g.Nout;
+  a.ksteps_main = (int)((g.Kred + BK - 1) / BK);
+  a.ksteps_lora = g.rp / BK;
+  a.w = g.w;
+  a.out = g.out;
+  a.ldo = g.Nout;
+  a.status = device_status_ptr();
+  const Codebook &cb = codebook();
+  for (int i = 0; i < 16; ++i) a.q[i] = cb.q[i];
+  dim3 grid((unsigned)((g.Nout + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM));
+  k_nf4_gemm<kTrans><<<grid, THREADS, SMEM_BYTES, st>>>(tA, tA2, tB2, a);
+  return check_cuda(cudaGetLastError(), "tensor-core GEMM launch");
+}
+
+}  // namespace
+
+int launch_nf4_gemm(const GemmProblem &g, cudaStream_t st) {
+  return g.trans ? launch<true>(g, st) : launch<false>(g, st);
+}
+
+}  // namespace ql

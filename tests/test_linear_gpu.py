@@ -1,0 +1,184 @@
+"""GPU parity of the QLoRA linear forward and backward against the fp64 oracle.
+
+Tolerance (fp32 accumulation vs fp64 on the same dequantized weights):
+relative Frobenius error <= 5e-3 and |err| <= 1e-2 (|ref| + rms(ref)) per
+element.  The in-GEMM dequantization is checked bit-exactly with one-hot
+inputs."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import linear, nf4
+
+pytestmark = pytest.mark.gpu
+
+REL_FRO = 5e-3
+ELEM = 1e-2
+
+
+@pytest.fixture(scope="module")
+def ql():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_nf4_quantized_38_b300 import qlora
+    return qlora
+
+
+def bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def f64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def assert_close(name, got, want):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    assert got.shape == want.shape, name
+    diff = got - want
+    rel = np.linalg.norm(diff) / max(np.linalg.norm(want), 1e-300)
+    rms = np.sqrt(np.mean(want ** 2))
+    bound = ELEM * (np.abs(want) + rms)
+    worst = np.max(np.abs(diff) / bound)
+    assert rel <= REL_FRO, f"{name}: relative Frobenius error {rel:.3e}"
+    assert worst <= 1.0, f"{name}: element error {worst:.3f} of the bound"
+
+
+def make_case(N, K, M, r, seed, alpha=16.0, dq=256, B_zero=False):
+    from bit_nf4_quantized_38_b300.workloads import normal_bf16, normal_with_outliers_bf16
+    W = normal_with_outliers_bf16((N, K), 0.02, 0.001, 20.0, seed)
+    X = normal_bf16((M, K), 1.0, seed + 1)
+    A = normal_bf16((K, r), 1.0 / np.sqrt(r), seed + 2)
+    B = torch.zeros((r, N), dtype=torch.bfloat16) if B_zero else normal_bf16((r, N), 0.01, seed + 3)
+    dY = normal_bf16((M, N), 1.0, seed + 4)
+    return W, X, A, B, dY, alpha / r
+
+
+def run_gpu(ql, W, X, A, B, dY, s, dq=256, xa_from_fwd=True):
+    dev = torch.device("cuda")
+    q = ql.nf4_quantize(W.to(dev), dq_blocksize=dq)
+    Xd, Ad, Bd, dYd = X.to(dev), A.to(dev), B.to(dev), dY.to(dev)
+    Y, XA = ql.qlora_linear_fwd(Xd, q, Ad, Bd, s)
+    dX, dA, dB = ql.qlora_linear_bwd(dYd, Xd, XA if xa_from_fwd else None, q, Ad, Bd, s)
+    torch.cuda.synchronize()
+    ql.device_status()
+    return q, Y, XA, dX, dA, dB
+
+
+def oracle_all(W, X, A, B, dY, s, dq=256):
+    ref = nf4.quantize(bits(W), dq_blocksize=dq)
+    Wh = nf4.dequantize(ref)
+    Y, XA = linear.lora_forward(bits(X), Wh, bits(A), bits(B), s)
+    dX, dA, dB, _ = linear.lora_backward(bits(dY), bits(X), Wh, bits(A), bits(B), s)
+    return Y, XA, dX, dA, dB
+
+
+SHAPES = [
+    # N, K, M, r
+    (1024, 1024, 16, 8),    # the single 1024x1024 linear, 16 tokens
+    (1024, 1024, 256, 64),  # two M tiles, four N tiles
+    (328, 320, 200, 16),    # ragged in every dimension
+    (512, 4160, 130, 32),   # long reduction, M just over one tile
+    (264, 192, 129, 128),   # rank 128: two LoRA K-steps
+]
+
+
+@pytest.mark.parametrize("N,K,M,r", SHAPES)
+def test_forward_backward_within_tolerance(ql, N, K, M, r):
+    W, X, A, B, dY, s = make_case(N, K, M, r, seed=N + K + M + r)
+    _, Y, XA, dX, dA, dB = run_gpu(ql, W, X, A, B, dY, s)
+    Yr, XAr, dXr, dAr, dBr = oracle_all(W, X, A, B, dY, s)
+    assert_close("Y", f64(Y), Yr)
+    assert_close("XA", f64(XA), XAr)
+    assert_close("dX", f64(dX), dXr)
+    assert_close("dA", f64(dA), dAr)
+    assert_close("dB", f64(dB), dBr)
+
+
+def test_double_quant_off(ql):
+    W, X, A, B, dY, s = make_case(512, 512, 64, 16, seed=5)
+    _, Y, XA, dX, dA, dB = run_gpu(ql, W, X, A, B, dY, s, dq=0)
+    Yr, _, dXr, dAr, dBr = oracle_all(W, X, A, B, dY, s, dq=0)
+    assert_close("Y", f64(Y), Yr)
+    assert_close("dX", f64(dX), dXr)
+    assert_close("dA", f64(dA), dAr)
+    assert_close("dB", f64(dB), dBr)
+
+
+@pytest.mark.parametrize("N,K", [(512, 384), (296, 320)])
+def test_in_gemm_dequant_is_bit_exact(ql, N, K):
+    """With B = 0 and one-hot tokens, Y[m, n] = W_hat[n, k_m] exactly (one
+    fp32 product by 1.0, rounded to bf16 once); with one-hot dY,
+    dX[m, k] = W_hat[n_m, k] exactly.  Both must equal the oracle's W_hat."""
+    from bit_nf4_quantized_38_b300.workloads import normal_with_outliers_bf16
+    W = normal_with_outliers_bf16((N, K), 0.02, 0.001, 20.0, seed=7)
+    ref = nf4.quantize(bits(W))
+    Wh = nf4.dequantize(ref)
+    dev = torch.device("cuda")
+    q = ql.nf4_quantize(W.to(dev))
+    r = 8
+    A = torch.randn(K, r).to(torch.bfloat16).to(dev)
+    Bz = torch.zeros(r, N, dtype=torch.bfloat16, device=dev)
+    ks = np.arange(K)
+    X = torch.zeros(K, K, dtype=torch.bfloat16)
+    X[torch.arange(K), torch.from_numpy(ks)] = 1.0
+    Y, _ = ql.qlora_linear_fwd(X.to(dev), q, A, Bz, 2.0)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(Y), Wh.T[ks])
+    dY = torch.zeros(N, N, dtype=torch.bfloat16)
+    dY[torch.arange(N), torch.arange(N)] = 1.0
+    X2 = torch.zeros(N, K, dtype=torch.bfloat16, device=dev)
+    dX, dA, dB = ql.qlora_linear_bwd(dY.to(dev), X2, None, q, A, Bz, 2.0)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(dX), Wh)
+    assert torch.count_nonzero(dA) == 0
+
+
+def test_recomputed_xa_matches_forward_xa_bitwise(ql):
+    W, X, A, B, dY, s = make_case(768, 640, 192, 64, seed=9)
+    _, _, _, dX1, dA1, dB1 = run_gpu(ql, W, X, A, B, dY, s, xa_from_fwd=True)
+    _, _, _, dX2, dA2, dB2 = run_gpu(ql, W, X, A, B, dY, s, xa_from_fwd=False)
+    assert torch.equal(dX1, dX2) and torch.equal(dA1, dA2) and torch.equal(dB1, dB2)
+
+
+def test_results_are_deterministic(ql):
+    W, X, A, B, dY, s = make_case(1024, 1024, 300, 64, seed=10)
+    a = run_gpu(ql, W, X, A, B, dY, s)
+    b = run_gpu(ql, W, X, A, B, dY, s)
+    for x, y in zip(a[1:], b[1:]):
+        assert torch.equal(x, y)
+
+
+def test_zero_B_gives_zero_dA(ql):
+    W, X, A, B, dY, s = make_case(256, 256, 64, 8, seed=11, B_zero=True)
+    _, Y, XA, dX, dA, dB = run_gpu(ql, W, X, A, B, dY, s)
+    assert torch.count_nonzero(dA) == 0
+    Yr, _, dXr, _, dBr = oracle_all(W, X, A, B, dY, s)
+    assert_close("Y", f64(Y), Yr)
+    assert_close("dB", f64(dB), dBr)
+
+
+@pytest.mark.parametrize("idx", [0, 4, 6])
+def test_llama7b_linear_full_size_sampled(ql, idx):
+    """LLaMA-7B linears at M = 4096 tokens, r = 64: Y and dX checked on 64
+    sampled rows, XA, dA and dB in full."""
+    from bit_nf4_quantized_38_b300.workloads import case_inputs, case_weight, llama7b_linears
+    case = llama7b_linears().cases[idx]
+    W = case_weight(case)
+    X, A, B, dY = case_inputs(case)
+    s = case.scale
+    _, Y, XA, dX, dA, dB = run_gpu(ql, W, X, A, B, dY, s)
+    ref = nf4.quantize(bits(W))
+    Wh = nf4.dequantize(ref)
+    rows = np.sort(np.random.default_rng(idx).choice(case.M, 64, replace=False))
+    Yr, _ = linear.lora_forward(bits(X)[rows], Wh, bits(A), bits(B), s)
+    assert_close("Y rows", f64(Y)[rows], Yr)
+    dXr, _, _, _ = linear.lora_backward(bits(dY)[rows], bits(X)[rows], Wh, bits(A), bits(B), s)
+    assert_close("dX rows", f64(dX)[rows], dXr)
+    Xf, Af, Bf, dYf = (linear.as_f64(bits(t)) for t in (X, A, B, dY))
+    XAr = Xf @ Af
+    assert_close("XA", f64(XA), XAr)
+    G = dYf @ Bf.T
+    assert_close("dA", f64(dA), s * (Xf.T @ G))
+    assert_close("dB", f64(dB), s * (XAr.T @ dYf))
