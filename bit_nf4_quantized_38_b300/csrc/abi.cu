@@ -1,4 +1,5 @@
 // C entry points of libqlora: argument checks, workspace layout, dispatch.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -10,6 +11,7 @@ namespace ql {
 
 namespace {
 thread_local char g_msg[512] = "";
+std::atomic<uint64_t> g_launches{0};
 __device__ int g_status;
 }  // namespace
 
@@ -25,6 +27,8 @@ int check_cuda(cudaError_t e, const char *what) {
   if (e == cudaSuccess) return QL_OK;
   return set_error(QL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
+
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
 int *device_status_ptr() {
   void *p = nullptr;
@@ -79,6 +83,8 @@ extern "C" size_t ql_workspace_size(int op, int64_t M, int64_t N, int64_t K, int
 }
 
 extern "C" const char *ql_last_error(void) { return g_msg; }
+
+extern "C" uint64_t ql_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 extern "C" int ql_get_device_status(ql_stream_t stream) {
   int rc = check_cuda(cudaStreamSynchronize(stream), "ql_get_device_status: synchronize");

@@ -39,6 +39,7 @@ int check_cuda(cudaError_t e, const char *what);
 // Device status word set by bounded waits that give up (one per device).
 enum : int { kStatusOk = 0, kStatusTimeout = 1 };
 int *device_status_ptr();  // device address of the current device's word
+void count_launch(int n = 1);  // kernels launched (process-wide counter)
 
 // ---------------------------------------------------------------------------
 // small device helpers

@@ -115,7 +115,7 @@ int linear_fwd(const LinearArgs &a) {
   GemmProblem g{};
   g.trans = false;
   g.A = a.X; g.M = M; g.Kred = K;
-  g.A2 = xa_pad; g.B2 = bt_pad; g.rp = rp;
+  g.A2 = xa_pad; g.B2 = bt_pad; g.r = r; g.rp = rp;
   g.w = nf4_view(a.W);
   g.out = a.Y; g.Nout = N;
   return launch_nf4_gemm(g, st);
@@ -154,7 +154,7 @@ int linear_bwd(const LinearArgs &a) {
   GemmProblem g{};
   g.trans = true;
   g.A = a.dY; g.M = M; g.Kred = N;
-  g.A2 = gs_pad; g.B2 = a_pad; g.rp = rp;
+  g.A2 = gs_pad; g.B2 = a_pad; g.r = r; g.rp = rp;
   g.w = nf4_view(a.W);
   g.out = a.dX; g.Nout = K;
   QL_TRY(launch_nf4_gemm(g, st));

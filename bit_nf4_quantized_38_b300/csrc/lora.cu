@@ -261,18 +261,21 @@ int launch_skinny(const SkinnyProblem &s, cudaStream_t st) {
     k_skinny<true, false><<<grid, SKINNY_THREADS, 0, st>>>(s.L, s.ldl, s.R, s.ldr, s.P, s.Q, s.T, tps, s.part);
   else
     k_skinny<true, true><<<grid, SKINNY_THREADS, 0, st>>>(s.L, s.ldl, s.R, s.ldr, s.P, s.Q, s.T, tps, s.part);
+  count_launch();
   return check_cuda(cudaGetLastError(), "LoRA side GEMM launch");
 }
 
 int launch_finalize_bf16(const float *part, int splits, int64_t P, int64_t Q, float scale, uint16_t *out_pad,
                          int qp, uint16_t *out, cudaStream_t st) {
   k_finalize_bf16<<<blocks_for(P * qp, 256), 256, 0, st>>>(part, splits, P, Q, scale, out_pad, qp, out);
+  count_launch();
   return check_cuda(cudaGetLastError(), "LoRA finalize launch");
 }
 
 int launch_finalize_f32(const float *part, int splits, int64_t P, int64_t Q, float scale, float *out,
                         cudaStream_t st) {
   k_finalize_f32<<<blocks_for(P * Q, 256), 256, 0, st>>>(part, splits, P * Q, scale, out);
+  count_launch();
   return check_cuda(cudaGetLastError(), "LoRA finalize launch");
 }
 
@@ -280,11 +283,13 @@ int launch_pack_transpose(const uint16_t *B, int r, int64_t N, float scale, uint
                           cudaStream_t st) {
   dim3 grid((unsigned)((N + 31) / 32), (unsigned)((rp + 31) / 32));
   k_pack_transpose<<<grid, dim3(32, 8), 0, st>>>(B, r, N, scale, Bt, rp);
+  count_launch();
   return check_cuda(cudaGetLastError(), "LoRA pack launch");
 }
 
 int launch_pack_pad(const uint16_t *A, int64_t K, int r, uint16_t *Ap, int rp, cudaStream_t st) {
   k_pack_pad<<<blocks_for(K * rp, 256), 256, 0, st>>>(A, K, r, Ap, rp);
+  count_launch();
   return check_cuda(cudaGetLastError(), "LoRA pack launch");
 }
 

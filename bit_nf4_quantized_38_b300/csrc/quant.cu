@@ -221,6 +221,7 @@ cudaError_t launch_quantize(const uint16_t *W, int64_t rows, int64_t cols, uint8
   k_quantize<<<grid_for(n_blocks, 8), kThreads, 0, st>>>(
       reinterpret_cast<const uint4 *>(W), n_blocks, codebook(), reinterpret_cast<uint32_t *>(packed),
       absmax, sum_acc);
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -229,6 +230,7 @@ cudaError_t launch_double_quant(const float *absmax, int64_t n_b, int dq_bs, con
   (void)dq_bs;  // 256, checked by the caller
   const int64_t n_2 = (n_b + 255) / 256;
   k_double_quant<<<(unsigned)n_2, 256, 0, st>>>(absmax, n_b, sum, code, step, mean);
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -243,6 +245,7 @@ cudaError_t launch_dequantize(const ql_nf4_tensor &q, uint16_t *W_out, cudaStrea
   else
     k_dequantize<false><<<g, kThreads, 0, st>>>(p, n_blocks, nullptr, nullptr, nullptr, q.absmax,
                                                 codebook(), o);
+  count_launch();
   return cudaGetLastError();
 }
 

@@ -20,6 +20,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -308,6 +309,213 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
   if (warp == 1) ptx::tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------- CTA-pair kernel
+//
+// A cluster of two CTAs on two SMs computes a (NACC x 256) x 256 output tile
+// with pair MMAs (tcgen05.mma.cta_group::2, M = 256, N = 256, K = 16): the
+// even CTA issues them; each CTA holds 128 A rows per accumulator and HALF of
+// the 256 B rows, and the tensor cores of the pair exchange the B halves.  So
+// every dequantized weight element is converted once and consumed by
+// NACC x 256 token rows, and each SM reads only its own A and B halves from
+// shared memory.  With NACC = 2 each CTA keeps two accumulators (2 x 256 TMEM
+// columns).
+//   warp 0     TMA producer: this CTA's A tiles (and LoRA B half); completion
+//              is counted on the even CTA's `full` barrier
+//   warp 1     TMEM allocation; in the even CTA, the MMA-issuing thread
+//   warps 2-9  two converter groups of 4 warps taking alternate stages (each
+//              has two MMA steps of time to load and expand its row-blocks),
+//              then the epilogue (group g drains accumulator g)
+namespace pairk {
+constexpr int BMH = 128;  // A rows per CTA per accumulator
+constexpr int BNH = 128;  // B rows per CTA (half of N = 256)
+constexpr int BK = 64, STAGES = 4, THREADS = 320, GROUP_WARPS = 4;
+template <int NACC>
+struct Geo {
+  static constexpr int A_ONE = BMH * BK * 2;  // 16 KB
+  static constexpr int A_BYTES = NACC * A_ONE;
+  static constexpr int B_BYTES = BNH * BK * 2;  // 16 KB
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = NACC * 256;
+  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256;
+};
+}  // namespace pairk
+
+template <bool kTrans, int NACC>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pairk::THREADS, 1)
+k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                const __grid_constant__ CUtensorMap tmB2, const GemmArgs p) {
+  using G = pairk::Geo<NACC>;
+  constexpr int PSTAGES = pairk::STAGES, PBK = pairk::BK, BMH = pairk::BMH, BNH = pairk::BNH,
+                GROUP_WARPS = pairk::GROUP_WARPS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + PSTAGES * G::STAGE_BYTES);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * PSTAGES + 1);
+  volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  auto full = [&](int s) { return ptx::smem_u32(&bars[s]); };
+  auto empty = [&](int s) { return ptx::smem_u32(&bars[PSTAGES + s]); };
+  const uint32_t accf = ptx::smem_u32(&bars[2 * PSTAGES]);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = ptx::cluster_ctarank();
+  const int n0 = (blockIdx.x >> 1) * 256;          // pair's first output column
+  const int mrow0 = blockIdx.y * (NACC * 256);     // pair's first output row
+  const int nsteps = p.ksteps_main + p.ksteps_lora;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PSTAGES; ++s) {
+      ptx::mbar_init(full(s), 2 + 2 * GROUP_WARPS);  // 2 producers + one group's warps in each CTA
+      ptx::mbar_init(empty(s), 1);
+    }
+    ptx::mbar_init(accf, 1);
+    *abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmA2);
+    ptx::prefetch_tmap(&tmB2);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), G::TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      for (int ks = 0; ks < nsteps; ++ks) {
+        const int s = ks % PSTAGES;
+        const uint32_t ph = (ks / PSTAGES) & 1;
+        if (!ptx::mbar_wait_cluster(empty(s), ph ^ 1, abort, p.status)) break;
+        const uint32_t a_dst = sbase + s * G::STAGE_BYTES;
+        const uint32_t lead_full = ptx::mapa(full(s), 0);
+        const bool lora = ks >= p.ksteps_main;
+        ptx::mbar_arrive_expect_tx_cluster(lead_full, G::A_BYTES + (lora ? G::B_BYTES : 0));
+        const int x = (lora ? ks - p.ksteps_main : ks) * PBK;
+#pragma unroll
+        for (int a = 0; a < NACC; ++a)
+          ptx::tma_load_2d_pair(a_dst + a * G::A_ONE, lora ? &tmA2 : &tmA, lead_full, x,
+                                mrow0 + a * 256 + (int)crank * BMH);
+        if (lora)
+          ptx::tma_load_2d_pair(a_dst + G::A_BYTES, &tmB2, lead_full, x, n0 + (int)crank * BNH);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA (even CTA)
+    if (lane == 0 && crank == 0) {
+      constexpr uint32_t idesc_main = ptx::idesc_bf16(256, 256, kTrans);
+      constexpr uint32_t idesc_kmaj = ptx::idesc_bf16(256, 256, false);
+      bool ok = true;
+      for (int ks = 0; ks < nsteps; ++ks) {
+        const int s = ks % PSTAGES;
+        const uint32_t ph = (ks / PSTAGES) & 1;
+        if (!ptx::mbar_wait_cluster(full(s), ph, abort, p.status)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t a_addr = sbase + s * G::STAGE_BYTES;
+        const uint32_t b_addr = a_addr + G::A_BYTES;
+        const bool bmn = kTrans && ks < p.ksteps_main;
+        // K-major B half: 128 rows of 128 B.  MN-major B half (W_hat^T):
+        // 2 MN-atoms of 64 output columns, 8 KB apart, each 8 K-atoms of
+        // 8 reduction rows, 1 KB apart.
+        const uint64_t b_desc = bmn ? ptx::desc_sw128(b_addr, 8192, 1024) : ptx::desc_sw128(b_addr, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < PBK / 16; ++kk) {
+          const uint64_t bd = b_desc + (uint64_t)(bmn ? kk * 128 : kk * 2);
+#pragma unroll
+          for (int a = 0; a < NACC; ++a) {
+            const uint64_t ad = ptx::desc_sw128(a_addr + a * G::A_ONE, 16, 1024) + (uint64_t)(kk * 2);
+            ptx::mma_bf16_pair(tmem + a * 256, ad, bd, bmn ? idesc_main : idesc_kmaj,
+                               (ks > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        ptx::mma_commit_pair(empty(s));
+      }
+      if (ok) ptx::mma_commit_pair(accf);
+    }
+  } else {
+    // ---------------------------------------------------------------- converters
+    const int grp = (warp - 2) / GROUP_WARPS;              // stages ks = grp, grp + 2, ...
+    const int ct = ((warp - 2) % GROUP_WARPS) * 32 + lane;  // this thread's row-block, 0..127
+    float q[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) q[i] = p.q[i];
+    int64_t rb_n, rb_kb0;
+    uint32_t rb_dst, rb_swz;
+    if (!kTrans) {
+      rb_n = n0 + (int)crank * BNH + ct;  // weight row = output column
+      rb_kb0 = 0;                         // + ks
+      rb_dst = (uint32_t)ct * 128u;
+      rb_swz = (uint32_t)(ct & 7);
+    } else {
+      const int nl = ct & 63, kbl = ct >> 6;
+      rb_n = nl;                                          // + 64 ks
+      rb_kb0 = ((n0 + (int)crank * BNH) >> 6) + kbl;      // output columns / 64
+      rb_dst = (uint32_t)((kbl * 8 + (nl >> 3)) * 1024 + (nl & 7) * 128);
+      rb_swz = (uint32_t)(nl & 7);
+    }
+    auto fetch = [&](int ks) {
+      return kTrans ? load_rowblock(p.w, rb_n + (int64_t)ks * 64, rb_kb0) : load_rowblock(p.w, rb_n, rb_kb0 + ks);
+    };
+    RowBlockSrc cur, nxt;
+    if (grp < p.ksteps_main) cur = fetch(grp);
+    for (int ks = grp; ks < nsteps; ks += 2) {
+      const int s = ks % PSTAGES;
+      const uint32_t ph = (ks / PSTAGES) & 1;
+      if (ks + 2 < p.ksteps_main) nxt = fetch(ks + 2);
+      if (!ptx::mbar_wait_cluster(empty(s), ph ^ 1, abort, p.status)) break;
+      if (ks < p.ksteps_main) {
+        const uint32_t b_addr = sbase + s * G::STAGE_BYTES + G::A_BYTES;
+        if (cur.valid) convert_rowblock(cur.p0, cur.p1, cur.mhat, q, b_addr + rb_dst, rb_swz);
+        else zero_row(b_addr + rb_dst);
+        ptx::fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(full(s), 0));
+      if (ks + 2 < p.ksteps_main) cur = nxt;
+    }
+    // ---------------------------------------------------------------- epilogue
+    if (!*abort && ptx::mbar_wait_cluster(accf, 0, abort, p.status)) {
+      ptx::tc_fence_after();
+      const int qd = warp & 3;  // TMEM lane quarter this warp may access
+      const int acc = NACC == 2 ? grp : 0;
+      const int c_begin = NACC == 2 ? 0 : grp * 4, c_end = NACC == 2 ? 8 : grp * 4 + 4;
+      const int row = mrow0 + acc * 256 + (int)crank * BMH + qd * 32 + lane;
+      uint16_t *orow = p.out + (int64_t)row * p.ldo;
+#pragma unroll 1
+      for (int c = c_begin; c < c_end; ++c) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(acc * 256 + c * 32), r);
+        ptx::tmem_wait_ld();
+        if (row < p.M) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int col = n0 + c * 32 + j * 8;
+            if (col + 8 <= p.Nout) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
+              v.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
+              v.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
+              v.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
+              *reinterpret_cast<uint4 *>(orow + col) = v;
+            }
+          }
+        }
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();
+  if (warp == 1) ptx::tmem_dealloc_pair(tmem, G::TMEM_COLS);
+}
+
 // ---------------------------------------------------------------------------- host
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -340,6 +548,41 @@ int make_tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer, 
   return QL_OK;
 }
 
+template <bool kTrans, int NACC>
+int launch_pair(const GemmProblem &g, cudaStream_t st) {
+  using Gm = pairk::Geo<NACC>;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    int rc = check_cuda(cudaFuncSetAttribute(k_nf4_gemm_pair<kTrans, NACC>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Gm::SMEM),
+                        "tensor-core pair GEMM: shared-memory attribute");
+    if (rc) return rc;
+    attr_done[dev] = true;
+  }
+  CUtensorMap tA, tA2, tB2;
+  int rc = make_tmap(&tA, g.A, (uint64_t)g.Kred, (uint64_t)g.M, pairk::BMH);
+  if (!rc) rc = make_tmap(&tA2, g.A2, (uint64_t)g.rp, (uint64_t)g.M, pairk::BMH);
+  if (!rc) rc = make_tmap(&tB2, g.B2, (uint64_t)g.rp, (uint64_t)g.Nout, pairk::BNH);
+  if (rc) return rc;
+  GemmArgs a{};
+  a.M = (int)g.M;
+  a.Nout = (int)g.Nout;
+  a.ksteps_main = (int)((g.Kred + BK - 1) / BK);
+  a.ksteps_lora = g.rp / BK;
+  a.w = g.w;
+  a.out = g.out;
+  a.ldo = g.Nout;
+  a.status = device_status_ptr();
+  const Codebook &cb = codebook();
+  for (int i = 0; i < 16; ++i) a.q[i] = cb.q[i];
+  dim3 grid((unsigned)(2 * ((g.Nout + 255) / 256)), (unsigned)((g.M + NACC * 256 - 1) / (NACC * 256)));
+  k_nf4_gemm_pair<kTrans, NACC><<<grid, pairk::THREADS, Gm::SMEM, st>>>(tA, tA2, tB2, a);
+  count_launch();
+  return check_cuda(cudaGetLastError(), "tensor-core pair GEMM launch");
+}
+
 template <bool kTrans>
 int launch(const GemmProblem &g, cudaStream_t st) {
   static bool attr_done[64] = {};
@@ -370,13 +613,74 @@ int launch(const GemmProblem &g, cudaStream_t st) {
   for (int i = 0; i < 16; ++i) a.q[i] = cb.q[i];
   dim3 grid((unsigned)((g.Nout + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM));
   k_nf4_gemm<kTrans><<<grid, THREADS, SMEM_BYTES, st>>>(tA, tA2, tB2, a);
+  count_launch();
   return check_cuda(cudaGetLastError(), "tensor-core GEMM launch");
 }
+
+struct Timing {
+  bool on = false;
+  int capacity = 0, used = 0;
+  std::vector<cudaEvent_t> ev;
+  std::vector<double> flops;
+};
+thread_local Timing g_timing;
 
 }  // namespace
 
 int launch_nf4_gemm(const GemmProblem &g, cudaStream_t st) {
-  return g.trans ? launch<true>(g, st) : launch<false>(g, st);
+  Timing &t = g_timing;
+  const bool timed = t.on && t.used < t.capacity;
+  if (timed) cudaEventRecord(t.ev[2 * t.used], st);
+  int rc;
+  if (g.M <= 128) rc = g.trans ? launch<true>(g, st) : launch<false>(g, st);
+  else if (g.M <= 256) rc = g.trans ? launch_pair<true, 1>(g, st) : launch_pair<false, 1>(g, st);
+  else rc = g.trans ? launch_pair<true, 2>(g, st) : launch_pair<false, 2>(g, st);
+  if (timed && rc == QL_OK) {
+    cudaEventRecord(t.ev[2 * t.used + 1], st);
+    t.flops[t.used] = 2.0 * (double)g.M * (double)g.Nout * (double)(g.Kred + g.r);
+    ++t.used;
+  }
+  return rc;
 }
 
 }  // namespace ql
+
+extern "C" int ql_timing_start(int capacity) {
+  using namespace ql;
+  Timing &t = g_timing;
+  if (t.on) return set_error(QL_ERR_INVALID, "ql_timing_start: timing already on");
+  if (capacity <= 0) return set_error(QL_ERR_INVALID, "ql_timing_start: capacity %d", capacity);
+  t.ev.assign(2 * (size_t)capacity, nullptr);
+  t.flops.assign((size_t)capacity, 0.0);
+  for (auto &e : t.ev) {
+    int rc = check_cuda(cudaEventCreate(&e), "ql_timing_start: event");
+    if (rc) return rc;
+  }
+  t.capacity = capacity;
+  t.used = 0;
+  t.on = true;
+  return QL_OK;
+}
+
+extern "C" int ql_timing_stop(float *total_ms, int *launches, double *flops) {
+  using namespace ql;
+  Timing &t = g_timing;
+  if (!t.on) return set_error(QL_ERR_INVALID, "ql_timing_stop: timing is off");
+  int rc = QL_OK;
+  float sum = 0.0f;
+  double fl = 0.0;
+  for (int i = 0; i < t.used && !rc; ++i) {
+    float ms = 0.0f;
+    rc = check_cuda(cudaEventSynchronize(t.ev[2 * i + 1]), "ql_timing_stop: synchronize");
+    if (!rc) rc = check_cuda(cudaEventElapsedTime(&ms, t.ev[2 * i], t.ev[2 * i + 1]), "ql_timing_stop: elapsed");
+    sum += ms;
+    fl += t.flops[i];
+  }
+  for (auto &e : t.ev)
+    if (e) cudaEventDestroy(e);
+  if (total_ms) *total_ms = sum;
+  if (launches) *launches = t.used;
+  if (flops) *flops = fl;
+  t = Timing{};
+  return rc;
+}

@@ -29,7 +29,8 @@ struct GemmProblem {
   int64_t M, Kred;
   const uint16_t *A2;
   const uint16_t *B2;
-  int rp;
+  int r;   // LoRA rank
+  int rp;  // r padded to a multiple of 64
   NF4View w;
   uint16_t *out;
   int64_t Nout;

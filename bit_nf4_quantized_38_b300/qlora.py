@@ -37,6 +37,10 @@ _SIGNATURES = {
                                         _c_p, _c_i32, _c_f32, _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p]),
     "ql_get_device_status": (ctypes.c_int, [_c_p]),
     "ql_last_error": (ctypes.c_char_p, []),
+    "ql_launch_count": (ctypes.c_uint64, []),
+    "ql_timing_start": (ctypes.c_int, [ctypes.c_int]),
+    "ql_timing_stop": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int),
+                                      ctypes.POINTER(ctypes.c_double)]),
 }
 
 
@@ -100,6 +104,23 @@ def nf4_codebook():
 def device_status(stream=None):
     """QL_OK, or raises QLError(QL_ERR_TIMEOUT) if a kernel gave up waiting."""
     _check(lib.ql_get_device_status(_stream(stream)))
+
+
+def launch_count():
+    """Kernels the library has launched in this process."""
+    return int(lib.ql_launch_count())
+
+
+def timing_start(capacity):
+    """Bracket the next `capacity` tensor-core GEMM launches with CUDA events."""
+    _check(lib.ql_timing_start(int(capacity)))
+
+
+def timing_stop():
+    """Returns (summed GEMM milliseconds, launches, summed algorithmic flops)."""
+    ms, n, fl = ctypes.c_float(), ctypes.c_int(), ctypes.c_double()
+    _check(lib.ql_timing_stop(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(fl)))
+    return float(ms.value), int(n.value), float(fl.value)
 
 
 def _workspace(nbytes, device, ws):

@@ -172,6 +172,23 @@ QL_API int qlora_linear_bwd(const uint16_t *dY, const uint16_t *X, const uint16_
  */
 QL_API int ql_get_device_status(ql_stream_t stream);
 
+/*
+ * Optional timing of the tensor-core GEMM launches, off by default.
+ * ql_timing_start(capacity): from now on every tensor-core GEMM that this host
+ *   thread launches is bracketed by a CUDA event pair recorded on its stream
+ *   (up to `capacity` launches; later ones are not timed).  Creates the events.
+ * ql_timing_stop(total_ms, launches, flops): waits for the recorded events,
+ *   writes the summed launch durations (ms), the number of timed launches and
+ *   their summed algorithmic flops (2 M N_out (K_red + r) each) to host
+ *   memory, destroys the events and turns timing off.
+ * Device work is unchanged; only event records are added to the stream.
+ */
+QL_API int ql_timing_start(int capacity);
+QL_API int ql_timing_stop(float *total_ms, int *launches, double *flops);
+
+/* Number of CUDA kernels the library has launched in this process. */
+QL_API uint64_t ql_launch_count(void);
+
 /* Message for the last error returned on this host thread ("" if none). */
 QL_API const char *ql_last_error(void);
 

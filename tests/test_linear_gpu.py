@@ -81,6 +81,8 @@ SHAPES = [
     (328, 320, 200, 16),    # ragged in every dimension
     (512, 4160, 130, 32),   # long reduction, M just over one tile
     (264, 192, 129, 128),   # rank 128: two LoRA K-steps
+    (328, 320, 600, 16),    # CTA-pair tiles, ragged
+    (1032, 576, 1100, 32),  # CTA-pair tiles, partial pair in N and M
 ]
 
 
