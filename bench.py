@@ -53,6 +53,11 @@ def parse_args():
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-extras", action="store_true", help="skip the decode and quantizer sub-results")
     p.add_argument("--linears", default="", help="comma-separated subset of the 7 linears (profiling runs)")
+    p.add_argument("--only", choices=["all", "decode", "quantize"], default="all",
+                   help="run only one sub-benchmark (profiling runs)")
+    p.add_argument("--decode-m", default="1,4,16", help="decode token counts")
+    p.add_argument("--decode-shapes", default="0,1,2", help="indices of the LLaMA-13B decode shapes")
+    p.add_argument("--decode-calls", type=int, default=240)
     return p.parse_args()
 
 
@@ -227,6 +232,119 @@ def run_reference(args):
     }), flush=True)
 
 
+# ----------------------------------------------------------------------------- sub-benchmarks
+
+def clone_nf4(ql, q):
+    import torch
+    t = ql.NF4Tensor(q.rows, q.cols, q.packed.clone(), blocksize=q.blocksize, dq_blocksize=q.dq_blocksize)
+    for f in ("absmax", "absmax_code", "dq_step", "dq_mean"):
+        v = getattr(q, f)
+        setattr(t, f, None if v is None else v.clone())
+    return t
+
+
+def bench_decode(ql, dev, hbm_gbs, calls=240, Ms=(1, 4, 16), shapes=(0, 1, 2)):
+    """LLaMA-13B decode shapes, M in {1, 4, 16}, r = 64: a CUDA graph of `calls`
+    forward calls cycling over weight copies that together exceed 3x L2."""
+    import torch
+    from bit_nf4_quantized_38_b300.workloads import case_inputs, case_weight, llama13b_decode
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    out = []
+    for M in Ms:
+        for c in [llama13b_decode(M=M).cases[i] for i in shapes]:
+            W = case_weight(c, device=dev)
+            q0 = ql.nf4_quantize(W)
+            del W
+            copies = max(2, math.ceil(3 * l2 / q0.nbytes()))
+            qs = [q0] + [clone_nf4(ql, q0) for _ in range(copies - 1)]
+            X, A, B, _ = (t.to(dev) for t in case_inputs(c))
+            Y = torch.empty(M, c.N, dtype=torch.bfloat16, device=dev)
+            XA = torch.empty(M, c.r, dtype=torch.bfloat16, device=dev)
+            ws = torch.empty(ql.workspace_size(ql.OP_LINEAR_FWD, M, c.N, c.K, c.r), dtype=torch.uint8, device=dev)
+            for q in qs:
+                ql.qlora_linear_fwd(X, q, A, B, c.scale, Y=Y, XA=XA, ws=ws)
+            torch.cuda.synchronize()
+            n = copies * max(1, calls // copies)
+            g = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    for i in range(n):
+                        ql.qlora_linear_fwd(X, qs[i % copies], A, B, c.scale, Y=Y, XA=XA, ws=ws)
+            g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 5
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (reps * n)
+            n_b = c.N * c.K // 64
+            alg = c.N * c.K // 2 + n_b + 4 * ((n_b + 255) // 256) + 4 + 2 * c.r * (c.K + c.N) + 2 * M * (c.K + c.N)
+            gbs = alg / (us * 1e-6) / 1e9
+            out.append({"shape": f"{c.N}x{c.K}", "M": M, "us_per_call": us, "bytes": alg, "GB/s": gbs,
+                        "frac_hbm": gbs / hbm_gbs, "weight_copies": copies})
+            del qs, q0
+            torch.cuda.empty_cache()
+    return out
+
+
+def bench_quantize(ql, dev, hbm_gbs, reps=5):
+    """NF4 + double quant of the 7 weights of one LLaMA-65B layer (Student-t(4)
+    values with std 0.015, drawn on the device), and the dequantize round trip."""
+    import torch
+    from bit_nf4_quantized_38_b300.workloads import case_weight, llama65b_layer_quant
+    cases = llama65b_layer_quant().cases
+    Ws = [case_weight(c, device=dev) for c in cases]
+    qs = [ql.nf4_quantize(W) for W in Ws]
+    outs = [torch.empty_like(W) for W in Ws]
+    wss = [torch.empty(ql.workspace_size(ql.OP_QUANTIZE, 0, c.N, c.K, 0), dtype=torch.uint8, device=dev)
+           for c in cases]
+    params = sum(c.N * c.K for c in cases)
+    n_b = sum(c.N * c.K // 64 for c in cases)
+    n_2 = sum((c.N * c.K // 64 + 255) // 256 for c in cases)
+    alg = 2 * params + params // 2 + n_b + 4 * n_2 + 4 * len(cases)
+    res = {}
+    for name, fn in (("quantize", lambda i: ql.nf4_quantize(Ws[i], out=qs[i], ws=wss[i])),
+                     ("dequantize", lambda i: ql.nf4_dequantize(qs[i], out=outs[i]))):
+        for i in range(len(cases)):
+            fn(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            for i in range(len(cases)):
+                fn(i)
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        gbs = alg / (us * 1e-6) / 1e9
+        res[name] = {"us_per_layer": us, "bytes": alg, "GB/s": gbs, "frac_hbm": gbs / hbm_gbs}
+    res["params"] = params
+    res["workload"] = "llama65b_layer_7_weights_student_t4"
+    del Ws, qs, outs
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_only(args):
+    """One sub-benchmark alone, printed as a JSON line (for profiling)."""
+    import torch
+    from bit_nf4_quantized_38_b300 import qlora as ql
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, _ = load_peaks()
+    if args.only == "decode":
+        res = bench_decode(ql, dev, peaks["hbm_gbs"], args.decode_calls,
+                           tuple(int(m) for m in args.decode_m.split(",")),
+                           tuple(int(i) for i in args.decode_shapes.split(",")))
+    else:
+        res = bench_quantize(ql, dev, peaks["hbm_gbs"])
+    print(json.dumps({"only": args.only, "results": res}), flush=True)
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 def main():
@@ -237,6 +355,9 @@ def main():
 
     import torch
     import torch.distributed as dist
+
+    if args.only != "all":
+        return run_only(args)
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -391,6 +512,16 @@ def main():
     }
     if e2e:
         out["e2e"] = e2e
+    if not args.no_extras and world == 1:
+        del layers, ws
+        torch.cuda.empty_cache()
+        out["decode"] = {"workload": "llama13b decode shapes, M in {1,4,16}, r=64, fwd, CUDA graph over "
+                                     "weight copies > 3x L2",
+                         "peak_hbm_gbs": peaks["hbm_gbs"],
+                         "results": bench_decode(ql, dev, peaks["hbm_gbs"], args.decode_calls,
+                                                 tuple(int(m) for m in args.decode_m.split(",")),
+                                                 tuple(int(i) for i in args.decode_shapes.split(",")))}
+        out["quantize"] = bench_quantize(ql, dev, peaks["hbm_gbs"])
     if rank == 0 and world == 1 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline()
     if rank == 0:

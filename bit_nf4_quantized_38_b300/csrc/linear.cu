@@ -14,6 +14,7 @@
 //   6. dB = s XA^T dY                 side GEMM + finalize
 #include <algorithm>
 
+#include "decode.cuh"
 #include "linear.cuh"
 #include "tc_gemm.cuh"
 
@@ -84,8 +85,11 @@ int check_common(const LinearArgs &a, const char *fn, size_t need) {
 
 }  // namespace
 
+constexpr int64_t kDecodeMaxM = 16;  // M at or below this takes the decode path
+
 size_t linear_fwd_ws(int64_t M, int64_t N, int64_t K, int32_t r) {
   if (M <= 0 || N <= 0 || K <= 0 || !rank_ok(r)) return 0;
+  if (M <= kDecodeMaxM) return decode_ws(N, K, r);
   return fwd_layout(M, N, K, r).total;
 }
 
@@ -101,6 +105,13 @@ int linear_fwd(const LinearArgs &a) {
     return set_error(QL_ERR_MISALIGNED, "%s: operand not 16-byte aligned", fn);
   const int64_t M = a.M, N = a.W.rows, K = a.W.cols;
   const int r = a.r, rp = padded_rank(r);
+  if (M >= 1 && M <= kDecodeMaxM) {
+    QL_TRY(check_common(a, fn, decode_ws(N, K, r)));
+    DecodeProblem d{};
+    d.X = a.X; d.M = M; d.K = K; d.N = N; d.w = nf4_view(a.W); d.A = a.A; d.B = a.B; d.r = r;
+    d.scale = a.scale; d.Y = a.Y; d.XA_out = a.XA; d.ws = a.ws;
+    return launch_decode(d, a.stream);
+  }
   const FwdLayout L = fwd_layout(M, N, K, r);
   QL_TRY(check_common(a, fn, L.total));
   char *ws = static_cast<char *>(a.ws);

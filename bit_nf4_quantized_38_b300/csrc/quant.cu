@@ -91,16 +91,24 @@ k_quantize(const uint4 *__restrict__ W, int64_t n_blocks, Codebook cb, uint32_t 
         local += (double)m;
       }
       uint32_t out = 0x77777777u;  // all-zero block: the zero level everywhere
-      if (m > 0.0f) {
+      if (m >= 0x1p-60f && m <= 0x1p60f) {
         out = 0;
-        const bool fast = m >= 0x1p-60f && m <= 0x1p60f;
         const float r = __frcp_rn(m);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          float x = fast ? quotient(w[e], m, r) : __fdiv_rn(w[e], m);
-          uint2 t = tab[cell_of(x) << 5];
-          uint32_t code = t.y + (x >= __uint_as_float(t.x) ? 1u : 0u);
+          const float x = quotient(w[e], m, r);
+          const uint2 t = tab[cell_of(x) << 5];
+          const uint32_t code = t.y + (x >= __uint_as_float(t.x) ? 1u : 0u);
           // element 2j -> high nibble of byte j
+          out |= code << (8 * (e >> 1) + ((e & 1) ? 0 : 4));
+        }
+      } else if (m > 0.0f) {
+        out = 0;
+#pragma unroll 1
+        for (int e = 0; e < 8; ++e) {
+          const float x = __fdiv_rn(w[e], m);
+          const uint2 t = tab[cell_of(x) << 5];
+          const uint32_t code = t.y + (x >= __uint_as_float(t.x) ? 1u : 0u);
           out |= code << (8 * (e >> 1) + ((e & 1) ? 0 : 4));
         }
       }

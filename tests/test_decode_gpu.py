@@ -1,0 +1,106 @@
+"""GPU parity of the decode-sized forward (M <= 16 tokens) against the fp64
+oracle.  The decode path applies each block constant to fp32 partial sums of
+x * bf16(q[code]) instead of using bf16(q[code] * constant) per weight; the
+difference is one bf16 rounding per weight and stays inside the tolerance
+(relative Frobenius error <= 5e-3, |err| <= 1e-2 (|ref| + rms(ref)))."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import linear, nf4
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ql():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_nf4_quantized_38_b300 import qlora
+    return qlora
+
+
+def bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def assert_close(name, got, want, rel_fro=5e-3, elem=1e-2):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    diff = got - want
+    rel = np.linalg.norm(diff) / max(np.linalg.norm(want), 1e-300)
+    rms = np.sqrt(np.mean(want ** 2))
+    worst = np.max(np.abs(diff) / (elem * (np.abs(want) + rms)))
+    assert rel <= rel_fro, f"{name}: relative Frobenius error {rel:.3e}"
+    assert worst <= 1.0, f"{name}: element error {worst:.3f} of the bound"
+    return rel
+
+
+def run(ql, W, X, A, B, s, dq=256):
+    dev = torch.device("cuda")
+    q = ql.nf4_quantize(W.to(dev), dq_blocksize=dq)
+    Y, XA = ql.qlora_linear_fwd(X.to(dev), q, A.to(dev), B.to(dev), s)
+    torch.cuda.synchronize()
+    ql.device_status()
+    return q, Y, XA
+
+
+def reference(W, X, A, B, s, dq=256):
+    Wh = nf4.dequantize(nf4.quantize(bits(W), dq_blocksize=dq))
+    return linear.lora_forward(bits(X), Wh, bits(A), bits(B), s)
+
+
+@pytest.mark.parametrize("N,K,M,r", [
+    (1024, 1024, 1, 8), (1032, 576, 3, 8), (1032, 576, 9, 128), (520, 4160, 16, 32), (64, 64, 16, 16),
+    (4096, 128, 7, 64), (256, 8192, 12, 64),
+])
+def test_decode_ragged_shapes(ql, N, K, M, r):
+    from bit_nf4_quantized_38_b300.workloads import normal_bf16, normal_with_outliers_bf16
+    seed = N + K + M
+    W = normal_with_outliers_bf16((N, K), 0.02, 0.001, 20.0, seed)
+    X = normal_bf16((M, K), 1.0, seed + 1)
+    A = normal_bf16((K, r), 1.0 / np.sqrt(r), seed + 2)
+    B = normal_bf16((r, N), 0.01, seed + 3)
+    s = 16.0 / r
+    _, Y, XA = run(ql, W, X, A, B, s)
+    Yr, XAr = reference(W, X, A, B, s)
+    assert_close("Y", Y.float().cpu().numpy(), Yr)
+    assert_close("XA", XA.float().cpu().numpy(), XAr)
+
+
+def test_decode_double_quant_off(ql):
+    from bit_nf4_quantized_38_b300.workloads import normal_bf16
+    W = normal_bf16((512, 1024), 0.02, 1)
+    X = normal_bf16((4, 1024), 1.0, 2)
+    A = normal_bf16((1024, 16), 0.25, 3)
+    B = normal_bf16((16, 512), 0.01, 4)
+    _, Y, _ = run(ql, W, X, A, B, 1.0, dq=0)
+    Yr, _ = reference(W, X, A, B, 1.0, dq=0)
+    assert_close("Y", Y.float().cpu().numpy(), Yr)
+
+
+@pytest.mark.parametrize("M", [1, 4, 16])
+@pytest.mark.parametrize("idx", [0, 1, 2])
+def test_decode_llama13b_full_size(ql, idx, M):
+    """LLaMA-13B shapes (5120x5120, 13824x5120, 5120x13824), r = 64: every output checked."""
+    from bit_nf4_quantized_38_b300.workloads import case_inputs, case_weight, llama13b_decode
+    case = llama13b_decode(M=M).cases[idx]
+    W = case_weight(case)
+    X, A, B, _ = case_inputs(case)
+    _, Y, XA = run(ql, W, X, A, B, case.scale)
+    Yr, XAr = reference(W, X, A, B, case.scale)
+    assert_close("Y", Y.float().cpu().numpy(), Yr)
+    assert_close("XA", XA.float().cpu().numpy(), XAr)
+
+
+def test_decode_is_deterministic_and_repeatable(ql):
+    from bit_nf4_quantized_38_b300.workloads import normal_bf16
+    dev = torch.device("cuda")
+    W = normal_bf16((5120, 5120), 0.02, 5).to(dev)
+    q = ql.nf4_quantize(W)
+    X = normal_bf16((16, 5120), 1.0, 6).to(dev)
+    A = normal_bf16((5120, 64), 0.125, 7).to(dev)
+    B = normal_bf16((64, 5120), 0.01, 8).to(dev)
+    outs = [ql.qlora_linear_fwd(X, q, A, B, 0.25)[0] for _ in range(3)]
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
