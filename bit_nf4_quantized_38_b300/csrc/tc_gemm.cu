@@ -463,6 +463,7 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     auto fetch = [&](int ks) {
       return kTrans ? load_rowblock(p.w, rb_n + (int64_t)ks * 64, rb_kb0) : load_rowblock(p.w, rb_n, rb_kb0 + ks);
     };
+    // The row-blocks of stage ks + 2 are loaded while stage ks is converted.
     RowBlockSrc cur, nxt;
     if (grp < p.ksteps_main) cur = fetch(grp);
     for (int ks = grp; ks < nsteps; ks += 2) {
