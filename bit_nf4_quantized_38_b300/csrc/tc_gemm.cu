@@ -185,14 +185,20 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           const int kl = ks - p.ksteps_main;
           ptx::mbar_arrive_expect_tx(full(s), A_BYTES + B_BYTES);
           ptx::tma_load_2d(a_dst, &tmA2, full(s), kl * BK, m0);
-          ptx::tma_load_2d(a_dst + A_BYTES, &tmB2, full(s), kl * BK, n0);
+          if (kTrans) {  // LoRA A stored [k][j]: K-major rows of the output columns
+            ptx::tma_load_2d(a_dst + A_BYTES, &tmB2, full(s), kl * BK, n0);
+          } else {       // LoRA B stored [j][n]: MN-major, four 64-column atoms
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i)
+              ptx::tma_load_2d(a_dst + A_BYTES + 8192 * i, &tmB2, full(s), n0 + 64 * i, kl * BK);
+          }
         }
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t idesc_main = ptx::idesc_bf16(BM, BN, kTrans);
+      constexpr uint32_t idesc_mn = ptx::idesc_bf16(BM, BN, true);
       constexpr uint32_t idesc_kmaj = ptx::idesc_bf16(BM, BN, false);
       bool ok = true;
       for (int ks = 0; ks < nsteps; ++ks) {
@@ -205,9 +211,10 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         const bool lora = ks >= p.ksteps_main;
         const uint64_t a_desc = ptx::desc_sw128(a_addr, 16, 1024);
         // K-major B: rows of 128 B, 8-row atoms 1024 B apart.  MN-major B
-        // (W_hat^T for dX): atoms of 64 output columns x 8 reduction rows;
-        // 8 K-atoms (1024 B apart) per 8 KB MN-atom column.
-        const bool bmn = kTrans && !lora;
+        // (W_hat^T for dX, the LoRA B for the forward): atoms of 64 output
+        // columns x 8 reduction rows; 8 K-atoms (1024 B apart) per 8 KB
+        // MN-atom column.
+        const bool bmn = kTrans != lora;
         const uint64_t b_desc = bmn ? ptx::desc_sw128(b_addr, 8192, 1024) : ptx::desc_sw128(b_addr, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
@@ -215,7 +222,7 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           // or two 8-row K-atoms = +2048 B (MN-major)
           const uint64_t ad = a_desc + (uint64_t)(kk * 2);
           const uint64_t bd = b_desc + (uint64_t)(bmn ? kk * 128 : kk * 2);
-          ptx::mma_bf16(tmem, ad, bd, bmn ? idesc_main : idesc_kmaj, (ks > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_bf16(tmem, ad, bd, bmn ? idesc_mn : idesc_kmaj, (ks > 0 || kk > 0) ? 1u : 0u);
         }
         ptx::mma_commit(empty(s));
       }
@@ -403,14 +410,20 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         for (int a = 0; a < NACC; ++a)
           ptx::tma_load_2d_pair(a_dst + a * G::A_ONE, lora ? &tmA2 : &tmA, lead_full, x,
                                 mrow0 + a * 256 + (int)crank * BMH);
-        if (lora)
-          ptx::tma_load_2d_pair(a_dst + G::A_BYTES, &tmB2, lead_full, x, n0 + (int)crank * BNH);
+        if (lora) {
+          if (kTrans) {  // LoRA A stored [k][j]: K-major rows of this CTA's output columns
+            ptx::tma_load_2d_pair(a_dst + G::A_BYTES, &tmB2, lead_full, x, n0 + (int)crank * BNH);
+          } else {       // LoRA B stored [j][n]: MN-major, two 64-column atoms
+            ptx::tma_load_2d_pair(a_dst + G::A_BYTES, &tmB2, lead_full, n0 + (int)crank * BNH, x);
+            ptx::tma_load_2d_pair(a_dst + G::A_BYTES + 8192, &tmB2, lead_full, n0 + (int)crank * BNH + 64, x);
+          }
+        }
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA (even CTA)
     if (lane == 0 && crank == 0) {
-      constexpr uint32_t idesc_main = ptx::idesc_bf16(256, 256, kTrans);
+      constexpr uint32_t idesc_mn = ptx::idesc_bf16(256, 256, true);
       constexpr uint32_t idesc_kmaj = ptx::idesc_bf16(256, 256, false);
       bool ok = true;
       for (int ks = 0; ks < nsteps; ++ks) {
@@ -420,10 +433,10 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         ptx::tc_fence_after();
         const uint32_t a_addr = sbase + s * G::STAGE_BYTES;
         const uint32_t b_addr = a_addr + G::A_BYTES;
-        const bool bmn = kTrans && ks < p.ksteps_main;
-        // K-major B half: 128 rows of 128 B.  MN-major B half (W_hat^T):
-        // 2 MN-atoms of 64 output columns, 8 KB apart, each 8 K-atoms of
-        // 8 reduction rows, 1 KB apart.
+        const bool bmn = kTrans != (ks >= p.ksteps_main);
+        // K-major B half: 128 rows of 128 B.  MN-major B half (W_hat^T, or
+        // the LoRA B in the forward): 2 MN-atoms of 64 output columns, 8 KB
+        // apart, each 8 K-atoms of 8 reduction rows, 1 KB apart.
         const uint64_t b_desc = bmn ? ptx::desc_sw128(b_addr, 8192, 1024) : ptx::desc_sw128(b_addr, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < PBK / 16; ++kk) {
@@ -431,7 +444,7 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
           for (int a = 0; a < NACC; ++a) {
             const uint64_t ad = ptx::desc_sw128(a_addr + a * G::A_ONE, 16, 1024) + (uint64_t)(kk * 2);
-            ptx::mma_bf16_pair(tmem + a * 256, ad, bd, bmn ? idesc_main : idesc_kmaj,
+            ptx::mma_bf16_pair(tmem + a * 256, ad, bd, bmn ? idesc_mn : idesc_kmaj,
                                (ks > 0 || kk > 0) ? 1u : 0u);
           }
         }
@@ -533,8 +546,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor [outer][inner] (inner contiguous), box [box_outer][64],
-// 128-byte swizzle, zero fill outside the tensor.
+}  // namespace
+
 int make_tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
   auto fn = encode_fn();
   if (!fn) return set_error(QL_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
@@ -548,6 +561,8 @@ int make_tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer, 
   if (r != CUDA_SUCCESS) return set_error(QL_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return QL_OK;
 }
+
+namespace {
 
 template <bool kTrans, int NACC>
 int launch_pair(const GemmProblem &g, cudaStream_t st) {
@@ -564,14 +579,16 @@ int launch_pair(const GemmProblem &g, cudaStream_t st) {
   }
   CUtensorMap tA, tA2, tB2;
   int rc = make_tmap(&tA, g.A, (uint64_t)g.Kred, (uint64_t)g.M, pairk::BMH);
-  if (!rc) rc = make_tmap(&tA2, g.A2, (uint64_t)g.rp, (uint64_t)g.M, pairk::BMH);
-  if (!rc) rc = make_tmap(&tB2, g.B2, (uint64_t)g.rp, (uint64_t)g.Nout, pairk::BNH);
+  if (!rc) rc = make_tmap(&tA2, g.A2, (uint64_t)g.r, (uint64_t)g.M, pairk::BMH);
+  if (!rc)
+    rc = kTrans ? make_tmap(&tB2, g.B2, (uint64_t)g.r, (uint64_t)g.Nout, pairk::BNH)
+                : make_tmap(&tB2, g.B2, (uint64_t)g.Nout, (uint64_t)g.r, 64);
   if (rc) return rc;
   GemmArgs a{};
   a.M = (int)g.M;
   a.Nout = (int)g.Nout;
   a.ksteps_main = (int)((g.Kred + BK - 1) / BK);
-  a.ksteps_lora = g.rp / BK;
+  a.ksteps_lora = (g.r + BK - 1) / BK;
   a.w = g.w;
   a.out = g.out;
   a.ldo = g.Nout;
@@ -598,14 +615,16 @@ int launch(const GemmProblem &g, cudaStream_t st) {
   }
   CUtensorMap tA, tA2, tB2;
   int rc = make_tmap(&tA, g.A, (uint64_t)g.Kred, (uint64_t)g.M, BM);
-  if (!rc) rc = make_tmap(&tA2, g.A2, (uint64_t)g.rp, (uint64_t)g.M, BM);
-  if (!rc) rc = make_tmap(&tB2, g.B2, (uint64_t)g.rp, (uint64_t)g.Nout, BN);
+  if (!rc) rc = make_tmap(&tA2, g.A2, (uint64_t)g.r, (uint64_t)g.M, BM);
+  if (!rc)
+    rc = kTrans ? make_tmap(&tB2, g.B2, (uint64_t)g.r, (uint64_t)g.Nout, BN)
+                : make_tmap(&tB2, g.B2, (uint64_t)g.Nout, (uint64_t)g.r, 64);
   if (rc) return rc;
   GemmArgs a{};
   a.M = (int)g.M;
   a.Nout = (int)g.Nout;
   a.ksteps_main = (int)((g.Kred + BK - 1) / BK);
-  a.ksteps_lora = g.rp / BK;
+  a.ksteps_lora = (g.r + BK - 1) / BK;
   a.w = g.w;
   a.out = g.out;
   a.ldo = g.Nout;
