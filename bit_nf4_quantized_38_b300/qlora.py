@@ -30,6 +30,7 @@ _SIGNATURES = {
     "ql_workspace_size": (_c_sz, [ctypes.c_int, _c_i64, _c_i64, _c_i64, _c_i32]),
     "ql_nf4_codebook": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float)]),
     "nf4_quantize": (ctypes.c_int, [_c_p, ctypes.POINTER(NF4Struct), _c_p, _c_sz, _c_p]),
+    "nf4_quantize_noalloc": (ctypes.c_int, [_c_p, ctypes.POINTER(NF4Struct), _c_p]),
     "nf4_dequantize": (ctypes.c_int, [ctypes.POINTER(NF4Struct), _c_p, _c_p]),
     "qlora_linear_fwd": (ctypes.c_int, [_c_p, _c_i64, ctypes.POINTER(NF4Struct), _c_p, _c_p, _c_i32,
                                         _c_f32, _c_p, _c_p, _c_p, _c_sz, _c_p]),
@@ -177,6 +178,17 @@ def nf4_quantize(W, dq_blocksize=256, blocksize=64, out=None, ws=None, stream=No
     ws, nbytes = _workspace(workspace_size(OP_QUANTIZE, 0, rows, cols, 0), W.device, ws)
     s = q.struct()
     _check(lib.nf4_quantize(_ptr(W), ctypes.byref(s), _ptr(ws), nbytes, _stream(stream)))
+    return q
+
+
+def nf4_quantize_noalloc(W, dq_blocksize=256, blocksize=64, out=None, stream=None):
+    """nf4_quantize without a workspace: the scratch is the library's built-in
+    array (for callers that cannot allocate per call; see include/qlora.h)."""
+    _need(W, torch.bfloat16, "W")
+    rows, cols = W.shape
+    q = out if out is not None else NF4Tensor.empty(rows, cols, W.device, dq_blocksize, blocksize)
+    s = q.struct()
+    _check(lib.nf4_quantize_noalloc(_ptr(W), ctypes.byref(s), _stream(stream)))
     return q
 
 

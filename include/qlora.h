@@ -127,6 +127,26 @@ QL_API int nf4_quantize(const uint16_t *W, const ql_nf4_tensor *q, void *ws,
                  size_t ws_bytes, ql_stream_t stream);
 
 /*
+ * nf4_quantize for callers that cannot pass a workspace (no counterpart in the
+ * paper: an interface convenience of this library).  Callers inside a region
+ * being captured into a CUDA graph, callers whose memory was all planned up
+ * front, and callers that must not trigger cudaMalloc's implicit device
+ * synchronisation cannot allocate scratch per call; this entry point uses a
+ * fixed scratch array built into the library instead (about 16 MB per GPU that
+ * loads the library, held until the process exits).  It allocates nothing.
+ *   W, q, stream : as for nf4_quantize.
+ * Limit: rows * cols / 64 <= 4,194,304 blocks (256 Mi parameters); larger
+ * weights return QL_ERR_UNSUPPORTED with a message.
+ * The first call on a device looks the array's device address up once, with
+ * that device current; make that first call before any stream capture.  All
+ * calls share the one array (its contents are those of the last call; the
+ * part that must start at zero is cleared by every call), so calls that
+ * overlap on the GPU -- on different streams, or from different host threads
+ * -- race and must be ordered by the caller.
+ */
+QL_API int nf4_quantize_noalloc(const uint16_t *W, const ql_nf4_tensor *q, ql_stream_t stream);
+
+/*
  * Dequantize to bf16 (the weight the linear layer computes with).
  *   q     : host struct of device inputs; W_out : rows x cols bf16 (device).
  */
