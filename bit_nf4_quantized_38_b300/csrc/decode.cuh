@@ -17,7 +17,6 @@ struct DecodeProblem {
   void *ws;
 };
 
-int decode_splits(int64_t N, int64_t K);
 size_t decode_ws(int64_t N, int64_t K, int r);
 int launch_decode(const DecodeProblem &p, cudaStream_t st);
 
