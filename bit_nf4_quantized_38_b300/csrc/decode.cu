@@ -32,7 +32,8 @@
 //                    group it stores its partial tile to the group's slot for
 //                    that CTA.
 //   k_decode_finish  one warp per 16 rows: adds the row group's slots in CTA
-//                    order, adds s XA B (warp MMAs) and writes Y.
+//                    order and s (XA B)^T (warp MMAs, B loaded before the
+//                    weight stream ends), and writes Y.
 //
 // Numerics: the block constant multiplies fp32 partial sums of x * bf16(q[c]),
 // so the weight used is q[c] (rounded once to bf16) times the fp32 constant,
@@ -272,7 +273,7 @@ k_decode_xa(const XaArgs a) {
 }
 
 // XA = the clusters' tiles added in cluster order (one CTA, a programmatic
-// dependent of k_decode_xa).
+// dependent of k_decode_xa), fp32 and, if asked for, bf16.
 constexpr int XF_THREADS = 256;
 __global__ void __launch_bounds__(XF_THREADS)
 k_decode_xa_final(const XaArgs a, int R, int ncl) {
@@ -535,45 +536,78 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
 
 // ---------------------------------------------------------------------------- finish
 struct FinArgs {
-  int M, N, r;
+  int M, N;
   int nbox, W, G;       // the weight stream's unit split
   const float *slots;   // its partial tiles
-  const float *XA;      // [M][r] fp32
-  const uint16_t *B;    // [r][N]
+  const float *XA;      // [M][R] fp32
+  const uint16_t *B;    // [R][N]
   float scale;
   uint16_t *Y;
 };
 constexpr int FIN_WARPS = 4;
 
-// Y = bf16(main term + s (XA B)^T), one warp per 16-row tile.  The main term
-// adds the row group's partial tiles in CTA order.  The LoRA product runs on
-// MMAs with weight rows as M, tokens as N and the rank as k: B supplies the
-// bf16 A fragments; XA (fp32) is split into bf16 high and low parts, two
-// MMAs, so XA keeps about 16 bits.  All loads of a 32-wide rank chunk are
-// issued before its first MMA.
-template <int MT>
+__device__ __forceinline__ uint32_t movtrans(uint32_t v) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(v));
+  return r;
+}
+
+// Y = bf16(main term + s (XA B)^T), one warp per 16-row tile.  Before waiting
+// for the weight stream the warp loads its B[:, rows] fragments (B is an
+// input): 8 x 8 blocks read row-wise, 4 bytes per lane, and transposed in
+// registers, which gives MMA A fragments with weight rows as M and the rank
+// as k.  After the wait it adds the row group's partial tiles in CTA order
+// and runs the LoRA MMAs with XA (fp32, split into bf16 high and low parts, so
+// XA keeps about 16 bits) as the B fragments, tokens as N.
+template <int MT, int R>
 __global__ void __launch_bounds__(FIN_WARPS * 32)
 k_decode_finish(const FinArgs a) {
-  griddep_wait();  // the weight stream, and through it the XA kernels, completed
+  constexpr int KS = (R + 15) / 16;
+  constexpr int ZB = MT == 1 ? 8 : 4;  // partial tiles loaded per batch
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int tile = blockIdx.x * FIN_WARPS + warp;
-  // N is a multiple of 8, so a tile's rows g (all lanes) are valid together
-  if (tile * 16 >= a.N) return;
+  const bool live = tile * 16 < a.N;  // N % 8 == 0: rows g of a live tile are valid
+  const int row0 = tile * 16;
+  uint32_t af[KS][4];
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+    for (int f = 0; f < 4; ++f) {  // a0: (rows 0-7, k 0-7), a1: rows 8-15, a2: k 8-15, a3: both
+      const int k = ks * 16 + 8 * (f >> 1) + g, n = row0 + 8 * (f & 1) + 2 * t;
+      af[ks][f] = (live && k < R && n < a.N) ? __ldg(reinterpret_cast<const uint32_t *>(a.B + (int64_t)k * a.N + n))
+                                             : 0u;
+    }
+  griddep_wait();  // the weight stream, and through it the XA kernels, completed
+  if (!live) return;
   const int rg = tile >> 4, rl = (tile & 15) * 16 + g;
-  const int rowg = tile * 16 + g, rowg8 = rowg + 8;
+  const int rowg = row0 + g, rowg8 = rowg + 8;
   const bool vg8 = rowg8 < a.N;
   // CTAs of the stream that worked on row group rg: cta(u) = floor(((u+1) G - 1) / W)
   const int cf = (int)((((int64_t)rg * a.nbox + 1) * a.G - 1) / a.W);
   const int cl = (int)((((int64_t)(rg + 1) * a.nbox) * a.G - 1) / a.W);
   const float *base = a.slots + (int64_t)(rg + cf) * SLOT_FLOATS;
+  // XA fragments: token 8 mt + g, k pairs (16 ks + 2t, +1) and (+8, +9).
+  // Every warp reads the same few lines: through L1 (read-only from here on),
+  // so that each SM asks L2 for them once instead of every warp.
+  float2 xf[KS][MT][2];
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const int k = ks * 16 + 2 * t;
+      const bool tv = mt * 8 + g < a.M;
+      const float *xa = a.XA + (mt * 8 + g) * R;
+      xf[ks][mt][0] = tv && k < R ? __ldg(reinterpret_cast<const float2 *>(xa + k)) : make_float2(0.0f, 0.0f);
+      xf[ks][mt][1] = tv && k + 8 < R ? __ldg(reinterpret_cast<const float2 *>(xa + k + 8)) : make_float2(0.0f, 0.0f);
+    }
   float2 sm[MT][2];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) sm[mt][0] = sm[mt][1] = make_float2(0.0f, 0.0f);
 #pragma unroll 1
-  for (int z0 = 0; z0 <= cl - cf; z0 += 4) {
-    float2 v[4][MT][2];
+  for (int z0 = 0; z0 <= cl - cf; z0 += ZB) {
+    float2 v[ZB][MT][2];
 #pragma unroll
-    for (int dz = 0; dz < 4; ++dz)
+    for (int dz = 0; dz < ZB; ++dz)
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         const bool in = z0 + dz <= cl - cf;
@@ -582,7 +616,7 @@ k_decode_finish(const FinArgs a) {
         v[dz][mt][1] = in ? __ldcg(reinterpret_cast<const float2 *>(pz + (rl + 8) * 16)) : make_float2(0.0f, 0.0f);
       }
 #pragma unroll
-    for (int dz = 0; dz < 4; ++dz)
+    for (int dz = 0; dz < ZB; ++dz)
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -596,41 +630,19 @@ k_decode_finish(const FinArgs a) {
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) L[mt][e] = 0.0f;
-#pragma unroll 1
-  for (int kk0 = 0; kk0 < a.r; kk0 += 32) {
-    uint32_t bf[2][4];
-    float2 xf[2][MT][2];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int k = kk0 + 16 * q + 2 * t;
+  for (int ks = 0; ks < KS; ++ks) {
+    const uint32_t a0 = movtrans(af[ks][0]), a1 = movtrans(af[ks][1]);
+    const uint32_t a2 = movtrans(af[ks][2]), a3 = movtrans(af[ks][3]);
 #pragma unroll
-      for (int f = 0; f < 4; ++f) {  // a0: (g, k), a1: (g + 8, k), a2: (g, k + 8), a3: (g + 8, k + 8)
-        const int kr = k + 8 * (f >> 1), row = (f & 1) ? rowg8 : rowg;
-        const bool v = kr < a.r && ((f & 1) ? vg8 : true);
-        bf[q][f] = v ? ((uint32_t)__ldg(a.B + (int64_t)kr * a.N + row) |
-                        ((uint32_t)__ldg(a.B + (int64_t)(kr + 1) * a.N + row) << 16))
-                     : 0u;
-      }
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        const bool tv = mt * 8 + g < a.M;
-        const float *xa = a.XA + (mt * 8 + g) * a.r;
-        xf[q][mt][0] = tv && k < a.r ? __ldcg(reinterpret_cast<const float2 *>(xa + k)) : make_float2(0.0f, 0.0f);
-        xf[q][mt][1] =
-            tv && k + 8 < a.r ? __ldcg(reinterpret_cast<const float2 *>(xa + k + 8)) : make_float2(0.0f, 0.0f);
-      }
+    for (int mt = 0; mt < MT; ++mt) {
+      const float2 x0 = xf[ks][mt][0], x1 = xf[ks][mt][1];
+      const uint32_t h0 = pack_bf16x2(x0.x, x0.y), h1 = pack_bf16x2(x1.x, x1.y);
+      const uint32_t l0 = pack_bf16x2(x0.x - bf16lo_to_f32(h0), x0.y - bf16hi_to_f32(h0));
+      const uint32_t l1 = pack_bf16x2(x1.x - bf16lo_to_f32(h1), x1.y - bf16hi_to_f32(h1));
+      mma16816(L[mt], a0, a1, a2, a3, h0, h1);
+      mma16816(L[mt], a0, a1, a2, a3, l0, l1);
     }
-#pragma unroll
-    for (int q = 0; q < 2; ++q)
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        const float2 x0 = xf[q][mt][0], x1 = xf[q][mt][1];
-        const uint32_t h0 = pack_bf16x2(x0.x, x0.y), h1 = pack_bf16x2(x1.x, x1.y);
-        const uint32_t l0 = pack_bf16x2(x0.x - bf16lo_to_f32(h0), x0.y - bf16hi_to_f32(h0));
-        const uint32_t l1 = pack_bf16x2(x1.x - bf16lo_to_f32(h1), x1.y - bf16hi_to_f32(h1));
-        mma16816(L[mt], bf[q][0], bf[q][1], bf[q][2], bf[q][3], h0, h1);
-        mma16816(L[mt], bf[q][0], bf[q][1], bf[q][2], bf[q][3], l0, l1);
-      }
   }
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
@@ -704,12 +716,21 @@ constexpr size_t WS_XA = 0;
 constexpr size_t WS_XAP = up256(16 * 128 * 4);
 constexpr size_t WS_SLOTS = WS_XAP + up256((size_t)XA_MAX_CLUSTERS * 16 * 128 * 4);
 
+template <typename F>
+int max_carveout(F *fn) {
+  return check_cuda(cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared),
+                    "decode: shared-memory carveout");
+}
+
 template <int NT>
 int launch_xa(const DecodeProblem &p, char *ws, int sms, DevInfo &di, int ti, cudaStream_t st) {
+  const int64_t groups = (p.N + UNIT_ROWS - 1) / UNIT_ROWS;
+  (void)groups;
   constexpr int R = NT * 8;
   // chunk rows: A chunk (kcc x R) + X chunk (16 x (kcc + 8)) within XA_STAGE_MAX
   const int GX = XA_MAX_CLUSTERS * XA_CLUSTER;  // 128 CTAs: one cluster per GPC
-  (void)sms;
+
   const int64_t steps_max = (p.K / 16 + GX - 1) / GX;
   const int64_t kcc = std::max<int64_t>(
       16, std::min<int64_t>(steps_max * 16, (XA_STAGE_MAX - 256) / (2 * R + 32) / 16 * 16));
@@ -721,6 +742,12 @@ int launch_xa(const DecodeProblem &p, char *ws, int sms, DevInfo &di, int ti, cu
       rc = check_cuda(cudaFuncSetAttribute(k_decode_xa<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            16 * 128 * 4 + XA_STAGE_MAX + 1024),
                       "decode XA: shared-memory attribute");
+    // Every decode kernel asks for the largest shared-memory carveout: an SM
+    // configured for a small one could not take a weight-stream CTA beside it.
+    if (!rc) rc = max_carveout(k_decode_xa<NT>);
+    if (!rc) rc = max_carveout(k_decode_xa_final);
+    if (!rc) rc = max_carveout(k_decode_finish<1, R>);
+    if (!rc) rc = max_carveout(k_decode_finish<2, R>);
     if (rc) return rc;
     di.xa_attr[ti] = true;
   }
@@ -807,6 +834,11 @@ int launch_decode(const DecodeProblem &p, cudaStream_t st) {
       rc = check_cuda(cudaFuncSetAttribute(k_decode_stream<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)stream_smem<2>()),
                       "decode stream: shared-memory attribute");
+    if (!rc) rc = max_carveout(k_decode_stream<1, true>);
+    if (!rc) rc = max_carveout(k_decode_stream<1, false>);
+    if (!rc) rc = max_carveout(k_decode_stream<2, true>);
+    if (!rc) rc = max_carveout(k_decode_stream<2, false>);
+
     if (rc) return rc;
     di.st_attr = true;
   }
@@ -850,7 +882,7 @@ int launch_decode(const DecodeProblem &p, cudaStream_t st) {
   if (rc) return rc;
 
   FinArgs f{};
-  f.M = (int)p.M; f.N = (int)p.N; f.r = p.r;
+  f.M = (int)p.M; f.N = (int)p.N;
   f.nbox = a.nbox; f.W = a.W; f.G = G;
   f.slots = slots;
   f.XA = reinterpret_cast<const float *>(ws + WS_XA);
@@ -861,7 +893,14 @@ int launch_decode(const DecodeProblem &p, cudaStream_t st) {
   ff.stream = st;
   ff.attrs = attr;
   ff.numAttrs = 1;
-  e = mt2 ? cudaLaunchKernelEx(&ff, k_decode_finish<2>, f) : cudaLaunchKernelEx(&ff, k_decode_finish<1>, f);
+  switch (p.r * 4 + (mt2 ? 2 : 1)) {
+#define QL_FIN(R_)                                                   \
+  case R_ * 4 + 1: e = cudaLaunchKernelEx(&ff, k_decode_finish<1, R_>, f); break; \
+  case R_ * 4 + 2: e = cudaLaunchKernelEx(&ff, k_decode_finish<2, R_>, f); break;
+    QL_FIN(8) QL_FIN(16) QL_FIN(32) QL_FIN(64) QL_FIN(128)
+#undef QL_FIN
+    default: return set_error(QL_ERR_UNSUPPORTED, "decode: rank %d", p.r);
+  }
   count_launch();
   return check_cuda(e, "decode finish launch");
 }
