@@ -38,81 +38,110 @@ __device__ __forceinline__ float quotient(float w, float m, float r) {
   return __fmaf_rn(res, r, x0);
 }
 
-__device__ __forceinline__ uint32_t cell_of(float x) {
-  // rne(32 x + 32) through the 1.5 * 2^23 rounding constant
-  return min(__float_as_uint(__fmaf_rn(x, 32.0f, 12582944.0f)) & 0x7Fu, (uint32_t)(kCells - 1));
+// Quantizer layout: 4 lanes per 64-element block, 16 consecutive elements
+// (32 bytes of bf16) each, so one warp step covers 8 consecutive blocks
+// (1 KB of W) and writes 8 bytes of nibbles per lane.
+constexpr int kQLanes = 4;
+constexpr int kQBlocksPerStep = 32 / kQLanes;
+constexpr int kQUnroll = 2;  // warp steps in flight per thread
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
 }
 
 __global__ void __launch_bounds__(kThreads)
-k_quantize(const uint4 *__restrict__ W, int64_t n_blocks, Codebook cb, uint32_t *__restrict__ packed,
+k_quantize(const uint4 *__restrict__ W, int64_t n_blocks, Codebook cb, uint2 *__restrict__ packed,
            float *__restrict__ absmax, double *__restrict__ sum_acc) {
-  // Coding table, one copy per lane so lookups never conflict on a bank.
-  __shared__ uint2 table[kCells * 32];
+  // Coding table, one copy per lane so lookups never conflict on a bank: cell
+  // c, lane l at byte c * 256 + l * 8 (threshold bits, lower code).  The
+  // lookup address comes from one byte permute of the cell index (the low
+  // byte of the rounding-constant sum below) and l * 8.
+  __shared__ __align__(16) uint2 table[kCells * 32];
   __shared__ double red[kThreads / 32];
   for (int i = threadIdx.x; i < kCells * 32; i += kThreads) {
-    int c = i >> 5;
+    const int c = i >> 5;
     table[i] = make_uint2(__float_as_uint(cb.cell_u[c]), (uint32_t)cb.cell_lo[c]);
   }
   __syncthreads();
 
   const int lane = threadIdx.x & 31;
-  const int sub = lane & 7;
-  const uint2 *tab = table + lane;
+  const int sub = lane & (kQLanes - 1);
+  const uint32_t tbase = (uint32_t)__cvta_generic_to_shared(table);
+  const uint32_t lane8 = (uint32_t)lane * 8u;
   const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
   double local = 0.0;
 
-  for (int64_t base = warp * 4 * kUnroll; base < n_blocks; base += nwarps * 4 * kUnroll) {
-    uint4 v[kUnroll];
+  for (int64_t base = warp * kQBlocksPerStep * kQUnroll; base < n_blocks;
+       base += nwarps * kQBlocksPerStep * kQUnroll) {
+    uint4 v[kQUnroll][2];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      int64_t b = base + u * 4 + (lane >> 3);
-      v[u] = b < n_blocks ? ld_stream(W + b * 8 + sub) : make_uint4(0, 0, 0, 0);
+    for (int u = 0; u < kQUnroll; ++u) {
+      const int64_t b = base + u * kQBlocksPerStep + lane / kQLanes;
+      const bool in = b < n_blocks;
+      v[u][0] = in ? ld_stream(W + b * 8 + sub * 2) : make_uint4(0, 0, 0, 0);
+      v[u][1] = in ? ld_stream(W + b * 8 + sub * 2 + 1) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      int64_t b = base + u * 4 + (lane >> 3);
-      float w[8];
-      uint32_t words[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+    for (int u = 0; u < kQUnroll; ++u) {
+      const int64_t b = base + u * kQBlocksPerStep + lane / kQLanes;
+      float w[16];
+      const uint32_t words[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w,
+                                 v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 8; ++i) {
         w[2 * i] = bf16lo_to_f32(words[i]);
         w[2 * i + 1] = bf16hi_to_f32(words[i]);
       }
       float m = 0.0f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(w[e]));
+      for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(w[e]));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
       if (b >= n_blocks) continue;
       if (sub == 0) {
         absmax[b] = m;
         local += (double)m;
       }
-      uint32_t out = 0x77777777u;  // all-zero block: the zero level everywhere
+      uint32_t out[2] = {0x77777777u, 0x77777777u};  // all-zero block: the zero level everywhere
       if (m >= 0x1p-60f && m <= 0x1p60f) {
-        out = 0;
         const float r = __frcp_rn(m);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float x = quotient(w[e], m, r);
-          const uint2 t = tab[cell_of(x) << 5];
-          const uint32_t code = t.y + (x >= __uint_as_float(t.x) ? 1u : 0u);
-          // element 2j -> high nibble of byte j
-          out |= code << (8 * (e >> 1) + ((e & 1) ? 0 : 4));
+        for (int h = 0; h < 2; ++h) {
+          uint32_t o = 0;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float x = quotient(w[8 * h + e], m, r);
+            // rne(32 x + 32) in the low byte, through the 1.5 * 2^23 rounding constant
+            const uint32_t cu = __float_as_uint(__fmaf_rn(x, 32.0f, 12582944.0f));
+            uint2 t;
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                         : "=r"(t.x), "=r"(t.y)
+                         : "r"(tbase + prmt(cu, lane8, 0x5504u)));
+            const uint32_t code = t.y + (x >= __uint_as_float(t.x) ? 1u : 0u);
+            // element 2j -> high nibble of byte j
+            o |= code << (8 * (e >> 1) + ((e & 1) ? 0 : 4));
+          }
+          out[h] = o;
         }
-      } else if (m > 0.0f) {
-        out = 0;
-#pragma unroll 1
-        for (int e = 0; e < 8; ++e) {
-          const float x = __fdiv_rn(w[e], m);
-          const uint2 t = tab[cell_of(x) << 5];
-          const uint32_t code = t.y + (x >= __uint_as_float(t.x) ? 1u : 0u);
-          out |= code << (8 * (e >> 1) + ((e & 1) ? 0 : 4));
+      } else if (m > 0.0f) {  // constants outside [2^-60, 2^60]: IEEE division
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t o = 0;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float x = __fdiv_rn(w[8 * h + e], m);
+            const uint32_t cu = __float_as_uint(__fmaf_rn(x, 32.0f, 12582944.0f));
+            const uint2 t = table[((cu & 0x7Fu) << 5) + lane];
+            const uint32_t code = t.y + (x >= __uint_as_float(t.x) ? 1u : 0u);
+            o |= code << (8 * (e >> 1) + ((e & 1) ? 0 : 4));
+          }
+          out[h] = o;
         }
       }
-      packed[b * 8 + sub] = out;
+      packed[b * kQLanes + sub] = make_uint2(out[0], out[1]);
     }
   }
 
@@ -207,6 +236,21 @@ k_dequantize(const uint32_t *__restrict__ packed, int64_t n_blocks, const int8_t
   }
 }
 
+int grid_for_q(int64_t n_blocks, int ctas_per_sm) {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  const int64_t per_cta = (int64_t)kQBlocksPerStep * kQUnroll * (kThreads / 32);
+  int64_t need = (n_blocks + per_cta - 1) / per_cta;
+  int64_t g = (int64_t)sms * ctas_per_sm;
+  if (need < g) g = need;
+  return (int)(g < 1 ? 1 : g);
+}
+
 int grid_for(int64_t n_blocks, int ctas_per_sm) {
   static int sms = 0;
   if (!sms) {
@@ -226,8 +270,8 @@ int grid_for(int64_t n_blocks, int ctas_per_sm) {
 cudaError_t launch_quantize(const uint16_t *W, int64_t rows, int64_t cols, uint8_t *packed,
                             float *absmax, double *sum_acc, cudaStream_t st) {
   const int64_t n_blocks = rows * cols / 64;
-  k_quantize<<<grid_for(n_blocks, 8), kThreads, 0, st>>>(
-      reinterpret_cast<const uint4 *>(W), n_blocks, codebook(), reinterpret_cast<uint32_t *>(packed),
+  k_quantize<<<grid_for_q(n_blocks, 8), kThreads, 0, st>>>(
+      reinterpret_cast<const uint4 *>(W), n_blocks, codebook(), reinterpret_cast<uint2 *>(packed),
       absmax, sum_acc);
   count_launch();
   return cudaGetLastError();
