@@ -178,11 +178,16 @@ k_lora_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
       c4 = idx % chunks;
     }
     const uint32_t off = (uint32_t)((rr * G::TILE_LD + 4 * c4) * 4);
+    float4 v[8];  // every CTA's partial loaded before adding (cluster size <= 8)
+#pragma unroll
+    for (uint32_t cc = 0; cc < 8; ++cc)
+      v[cc] = cc < csize ? ptx::ld_shared_cluster_v4(ptx::mapa(tile_addr + off, cc)) : make_float4(0.f, 0.f, 0.f, 0.f);
     float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (uint32_t cc = 0; cc < csize; ++cc) {
-      const float4 v = ptx::ld_shared_cluster_v4(ptx::mapa(tile_addr + off, cc));
-      sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
-    }
+#pragma unroll
+    for (uint32_t cc = 0; cc < 8; ++cc)
+      if (cc < csize) {
+        sum.x += v[cc].x; sum.y += v[cc].y; sum.z += v[cc].z; sum.w += v[cc].w;
+      }
     const int64_t p = p0 + rr;
     if (p >= a.P) continue;
     const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
@@ -259,8 +264,10 @@ int launch_ab(const LoraProblem &L, cudaStream_t st) {
 }  // namespace
 
 int lora_splits(int64_t P, int64_t T) {
+  // As many splits as keep every CTA in one wave (two CTAs per SM on 148
+  // SMs), at most 8 (the portable cluster size).
   const int64_t tiles = (P + LBP - 1) / LBP, nT = (T + LBT - 1) / LBT;
-  int64_t S = (2 * 148 + tiles - 1) / tiles;
+  int64_t S = (2 * 148) / tiles;
   S = std::min<int64_t>(S, 8);
   S = std::min<int64_t>(S, std::max<int64_t>(1, nT));
   return (int)std::max<int64_t>(S, 1);

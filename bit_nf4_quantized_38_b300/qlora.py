@@ -37,6 +37,7 @@ _SIGNATURES = {
     "qlora_linear_bwd": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, ctypes.POINTER(NF4Struct), _c_p,
                                         _c_p, _c_i32, _c_f32, _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p]),
     "ql_get_device_status": (ctypes.c_int, [_c_p]),
+    "ql_selftest_wait": (ctypes.c_int, [ctypes.c_int64, _c_p]),
     "ql_last_error": (ctypes.c_char_p, []),
     "ql_launch_count": (ctypes.c_uint64, []),
     "ql_timing_start": (ctypes.c_int, [ctypes.c_int]),
@@ -105,6 +106,12 @@ def nf4_codebook():
 def device_status(stream=None):
     """QL_OK, or raises QLError(QL_ERR_TIMEOUT) if a kernel gave up waiting."""
     _check(lib.ql_get_device_status(_stream(stream)))
+
+
+def selftest_wait(limit_ns, stream=None):
+    """Launch the failure-path self-test: a kernel whose bounded wait runs out
+    after `limit_ns`; device_status() afterwards raises QL_ERR_TIMEOUT."""
+    _check(lib.ql_selftest_wait(int(limit_ns), _stream(stream)))
 
 
 def launch_count():

@@ -206,6 +206,19 @@ QL_API int ql_get_device_status(ql_stream_t stream);
 QL_API int ql_timing_start(int capacity);
 QL_API int ql_timing_stop(float *total_ms, int *launches, double *flops);
 
+/*
+ * Self-test of the failure path (no counterpart in the pages: it checks the
+ * library's own bounded waits).  Launches one kernel on `stream` whose wait on
+ * a barrier can never be satisfied; after `limit_ns` nanoseconds of wall time
+ * (0 < limit_ns <= 2e9) the kernel gives up, records the timeout in the device
+ * status word and returns, exactly as any library kernel does when a wait
+ * runs out.  A following ql_get_device_status(stream) then returns
+ * QL_ERR_TIMEOUT (and clears the word); the CUDA context stays usable.
+ * Returns QL_OK once the kernel is launched, QL_ERR_INVALID for a limit
+ * outside the range, QL_ERR_CUDA if the launch fails.
+ */
+QL_API int ql_selftest_wait(int64_t limit_ns, ql_stream_t stream);
+
 /* Number of CUDA kernels the library has launched in this process. */
 QL_API uint64_t ql_launch_count(void);
 

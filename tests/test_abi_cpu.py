@@ -71,6 +71,12 @@ def test_quantize_rejects_bad_arguments_on_host(ql):
     assert lib.nf4_quantize(buf, None, buf, 1 << 20, None) == ql.QL_ERR_INVALID
 
 
+def test_selftest_wait_rejects_bad_limits_on_host(ql):
+    for limit in (0, -5, 2_000_000_001):
+        assert ql.lib.ql_selftest_wait(limit, None) == ql.QL_ERR_INVALID
+        assert "limit" in ql.lib.ql_last_error().decode()
+
+
 def test_quotient_without_division_is_exact_on_all_bf16_pairs(tmp_path):
     """The quantizer replaces w / m by a reciprocal and one FMA correction; this
     checks that sequence against IEEE division for every pair of bf16 values
