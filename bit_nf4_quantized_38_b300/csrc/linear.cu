@@ -137,12 +137,15 @@ int linear_bwd(const LinearArgs &a) {
     LoraProblem L{};
     L.A = a.X; L.a_mn = true; L.B = gs; L.b_mn = true;
     L.P = K; L.Q = r; L.T = M; L.mode = 1; L.scale = 1.0f; L.out = a.dA; L.ldo = r;
+    // X and Gs were complete before the dX GEMM let this kernel start
+    L.wait_at_end = true;
     QL_TRY(launch_lora(L, st));
   }
   // 4. dB = s XA^T dY, computed as dB^T = s dY^T XA and stored transposed
   LoraProblem L{};
   L.A = a.dY; L.a_mn = true; L.B = xa; L.b_mn = true;
   L.P = N; L.Q = r; L.T = M; L.mode = 2; L.scale = a.scale; L.out = a.dB; L.ldo = N;
+  L.wait_at_end = true;  // dY and XA were complete before the dX GEMM started
   return launch_lora(L, st);
 }
 

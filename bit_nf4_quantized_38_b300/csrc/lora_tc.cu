@@ -34,6 +34,7 @@ struct LoraTcArgs {
   int64_t ldo;
   uint16_t *out2;
   int64_t ldo2;
+  int wait_at_end;  // 0: wait for the previous kernel before reading; 1: at the end only
   int *status;
 };
 
@@ -89,6 +90,13 @@ k_lora_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched as a programmatic dependent.  A kernel that reads the previous
+  // kernel's output waits here; one whose inputs were complete before the
+  // previous kernel let it start (wait_at_end) runs alongside that kernel and
+  // waits only before it exits, so that its completion still implies the
+  // completion of everything before it.
+  if (!a.wait_at_end) ptx::griddep_wait();
+  ptx::griddep_launch();
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- TMA
@@ -209,6 +217,7 @@ k_lora_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
   // keep this CTA's tile alive until every CTA of the cluster has read it
   ptx::cluster_sync();
   if (warp == 1) ptx::tmem_dealloc(tmem, NQ);
+  if (a.wait_at_end) ptx::griddep_wait();
 }
 
 template <bool A_MN, bool B_MN, int NQ>
@@ -236,6 +245,7 @@ int launch_t(const LoraProblem &L, cudaStream_t st) {
   LoraTcArgs a{};
   a.P = L.P; a.Q = L.Q; a.T = L.T; a.mode = L.mode; a.scale = L.scale;
   a.out = L.out; a.ldo = L.ldo; a.out2 = L.out2; a.ldo2 = L.ldo2;
+  a.wait_at_end = L.wait_at_end ? 1 : 0;
   a.status = device_status_ptr();
   const int64_t tiles = (L.P + LBP - 1) / LBP;
   const int S = lora_splits(L.P, L.T);
@@ -244,13 +254,15 @@ int launch_t(const LoraProblem &L, cudaStream_t st) {
   cfg.blockDim = dim3(LTHREADS);
   cfg.dynamicSmemBytes = G::SMEM;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)S;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, k_lora_tc<A_MN, B_MN, NQ>, tA, tB, a);
   count_launch();
   return check_cuda(e, "LoRA kernel launch");

@@ -169,6 +169,10 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // launched as a programmatic dependent: the setup above overlaps the
+  // previous kernel; its outputs (the LoRA operand) are read only from here on
+  ptx::griddep_wait();
+  ptx::griddep_launch();
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
@@ -393,6 +397,10 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // launched as a programmatic dependent: the setup above overlaps the
+  // previous kernel; its outputs (the LoRA operand) are read only from here on
+  ptx::griddep_wait();
+  ptx::griddep_launch();
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
@@ -596,9 +604,19 @@ int launch_pair(const GemmProblem &g, cudaStream_t st) {
   const Codebook &cb = codebook();
   for (int i = 0; i < 16; ++i) a.q[i] = cb.q[i];
   dim3 grid((unsigned)(2 * ((g.Nout + 255) / 256)), (unsigned)((g.M + NACC * 256 - 1) / (NACC * 256)));
-  k_nf4_gemm_pair<kTrans, NACC><<<grid, pairk::THREADS, Gm::SMEM, st>>>(tA, tA2, tB2, a);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(pairk::THREADS);
+  cfg.dynamicSmemBytes = Gm::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_nf4_gemm_pair<kTrans, NACC>, tA, tA2, tB2, a);
   count_launch();
-  return check_cuda(cudaGetLastError(), "tensor-core pair GEMM launch");
+  return check_cuda(e, "tensor-core pair GEMM launch");
 }
 
 template <bool kTrans>
@@ -632,9 +650,19 @@ int launch(const GemmProblem &g, cudaStream_t st) {
   const Codebook &cb = codebook();
   for (int i = 0; i < 16; ++i) a.q[i] = cb.q[i];
   dim3 grid((unsigned)((g.Nout + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM));
-  k_nf4_gemm<kTrans><<<grid, THREADS, SMEM_BYTES, st>>>(tA, tA2, tB2, a);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_nf4_gemm<kTrans>, tA, tA2, tB2, a);
   count_launch();
-  return check_cuda(cudaGetLastError(), "tensor-core GEMM launch");
+  return check_cuda(e, "tensor-core GEMM launch");
 }
 
 struct Timing {

@@ -64,6 +64,9 @@ struct LoraProblem {
   int64_t ldo;
   uint16_t *out2;
   int64_t ldo2;
+  // The kernel's inputs were all complete before the previous kernel in the
+  // stream let it start: run alongside that kernel, wait for it only at the end.
+  bool wait_at_end = false;
 };
 int launch_lora(const LoraProblem &L, cudaStream_t st);
 int lora_splits(int64_t P, int64_t T);
