@@ -53,7 +53,7 @@ def parse_args():
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-extras", action="store_true", help="skip the decode and quantizer sub-results")
     p.add_argument("--linears", default="", help="comma-separated subset of the 7 linears (profiling runs)")
-    p.add_argument("--only", choices=["all", "decode", "quantize"], default="all",
+    p.add_argument("--only", choices=["all", "decode", "quantize", "single"], default="all",
                    help="run only one sub-benchmark (profiling runs)")
     p.add_argument("--decode-m", default="1,4,16", help="decode token counts")
     p.add_argument("--decode-shapes", default="0,1,2", help="indices of the LLaMA-13B decode shapes")
@@ -291,6 +291,43 @@ def bench_decode(ql, dev, hbm_gbs, calls=240, Ms=(1, 4, 16), shapes=(0, 1, 2)):
     return out
 
 
+def bench_single_linear(ql, dev, iters=200):
+    """The small 1024 x 1024 linear (16 tokens, r = 8): latency of quantize,
+    forward and backward, each timed over `iters` back-to-back calls from the
+    host (launch overhead included; a latency case, no roofline claim)."""
+    import torch
+    from bit_nf4_quantized_38_b300.workloads import case_inputs, case_weight, single_linear_1024
+    c = single_linear_1024().cases[0]
+    W = case_weight(c).to(dev)
+    X, A, B, dY = (t.to(dev) for t in case_inputs(c))
+    q = ql.nf4_quantize(W)
+    Y, XA = ql.qlora_linear_fwd(X, q, A, B, c.scale)
+    dX, dA, dB = ql.qlora_linear_bwd(dY, X, XA, q, A, B, c.scale)
+    wsq = torch.empty(ql.workspace_size(ql.OP_QUANTIZE, 0, c.N, c.K, 0), dtype=torch.uint8, device=dev)
+    wsf = torch.empty(ql.workspace_size(ql.OP_LINEAR_FWD, c.M, c.N, c.K, c.r), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(ql.workspace_size(ql.OP_LINEAR_BWD, c.M, c.N, c.K, c.r), dtype=torch.uint8, device=dev)
+    calls = {
+        "quantize": lambda: ql.nf4_quantize(W, out=q, ws=wsq),
+        "fwd": lambda: ql.qlora_linear_fwd(X, q, A, B, c.scale, Y=Y, XA=XA, ws=wsf),
+        "bwd": lambda: ql.qlora_linear_bwd(dY, X, XA, q, A, B, c.scale, dX=dX, dA=dA, dB=dB, ws=wsb),
+    }
+    out = {"workload": "single linear 1024x1024, M=16, r=8, alpha=16", "iters": iters}
+    for name, fn in calls.items():
+        for _ in range(10):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        out[f"us_{name}"] = e0.elapsed_time(e1) * 1e3 / iters
+    out["us_total"] = out["us_quantize"] + out["us_fwd"] + out["us_bwd"]
+    ql.device_status()
+    return out
+
+
 def bench_quantize(ql, dev, hbm_gbs, reps=5):
     """NF4 + double quant of the 7 weights of one LLaMA-65B layer (Student-t(4)
     values with std 0.015, drawn on the device), and the dequantize round trip."""
@@ -340,6 +377,8 @@ def run_only(args):
         res = bench_decode(ql, dev, peaks["hbm_gbs"], args.decode_calls,
                            tuple(int(m) for m in args.decode_m.split(",")),
                            tuple(int(i) for i in args.decode_shapes.split(",")))
+    elif args.only == "single":
+        res = bench_single_linear(ql, dev)
     else:
         res = bench_quantize(ql, dev, peaks["hbm_gbs"])
     print(json.dumps({"only": args.only, "results": res}), flush=True)
@@ -560,6 +599,7 @@ def main():
                                                  tuple(int(m) for m in args.decode_m.split(",")),
                                                  tuple(int(i) for i in args.decode_shapes.split(",")))}
         out["quantize"] = bench_quantize(ql, dev, peaks["hbm_gbs"])
+        out["single_linear"] = bench_single_linear(ql, dev)
     if rank == 0 and world == 1 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline()
     if rank == 0:

@@ -255,15 +255,20 @@ k_decode_xa(const XaArgs a) {
     const uint32_t local = ptx::smem_u32(part);
     for (int i = tid; i < M * R; i += XA_THREADS) {
       const int m = i / R, jj = i - m * R;
-      float s = 0.0f;
-      for (uint32_t cc = 0; cc < csize; ++cc) {
-        float v;
-        asm volatile("ld.shared::cluster.f32 %0, [%1];"
-                     : "=f"(v)
-                     : "r"(ptx::mapa(local + (uint32_t)(m * 128 + jj) * 4u, cc))
-                     : "memory");
-        s += v;
+      float v[XA_CLUSTER];  // every CTA's value loaded before adding, in rank order
+#pragma unroll
+      for (uint32_t cc = 0; cc < XA_CLUSTER; ++cc) {
+        v[cc] = 0.0f;
+        if (cc < csize)
+          asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                       : "=f"(v[cc])
+                       : "r"(ptx::mapa(local + (uint32_t)(m * 128 + jj) * 4u, cc))
+                       : "memory");
       }
+      float s = 0.0f;
+#pragma unroll
+      for (uint32_t cc = 0; cc < XA_CLUSTER; ++cc)
+        if (cc < csize) s += v[cc];
       a.xap[cl * 16 * R + i] = s;
     }
   }
