@@ -133,20 +133,19 @@ int linear_bwd(const LinearArgs &a) {
     g.out = a.dX; g.Nout = K;
     QL_TRY(launch_nf4_gemm(g, st));
   }
-  {  // 3. dA = X^T Gs: X [M][K] read MN-major, Gs [M][r] MN-major
-    LoraProblem L{};
-    L.A = a.X; L.a_mn = true; L.B = gs; L.b_mn = true;
-    L.P = K; L.Q = r; L.T = M; L.mode = 1; L.scale = 1.0f; L.out = a.dA; L.ldo = r;
-    // X and Gs were complete before the dX GEMM let this kernel start
-    L.wait_at_end = true;
-    QL_TRY(launch_lora(L, st));
-  }
-  // 4. dB = s XA^T dY, computed as dB^T = s dY^T XA and stored transposed
-  LoraProblem L{};
-  L.A = a.dY; L.a_mn = true; L.B = xa; L.b_mn = true;
-  L.P = N; L.Q = r; L.T = M; L.mode = 2; L.scale = a.scale; L.out = a.dB; L.ldo = N;
-  L.wait_at_end = true;  // dY and XA were complete before the dX GEMM started
-  return launch_lora(L, st);
+  // 3. dA = X^T Gs (X [M][K] and Gs [M][r] read MN-major) and 4. dB = s XA^T dY,
+  // computed as dB^T = s dY^T XA and stored transposed: one launch.  Their
+  // inputs (X, Gs, dY, XA) were all complete before the dX GEMM let them
+  // start, so they run alongside it and wait for it only at exit.
+  LoraProblem LA{};
+  LA.A = a.X; LA.a_mn = true; LA.B = gs; LA.b_mn = true;
+  LA.P = K; LA.Q = r; LA.T = M; LA.mode = 1; LA.scale = 1.0f; LA.out = a.dA; LA.ldo = r;
+  LA.wait_at_end = true;
+  LoraProblem LB{};
+  LB.A = a.dY; LB.a_mn = true; LB.B = xa; LB.b_mn = true;
+  LB.P = N; LB.Q = r; LB.T = M; LB.mode = 2; LB.scale = a.scale; LB.out = a.dB; LB.ldo = N;
+  LB.wait_at_end = true;
+  return launch_lora2(LA, LB, st);
 }
 
 }  // namespace ql

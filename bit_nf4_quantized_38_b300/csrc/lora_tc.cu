@@ -50,7 +50,16 @@ struct LGeo {
 
 template <bool A_MN, bool B_MN, int NQ>
 __global__ void __launch_bounds__(LTHREADS, 1)
-k_lora_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const LoraTcArgs a) {
+k_lora_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
+          const __grid_constant__ LoraTcArgs a0, const __grid_constant__ CUtensorMap tmA1,
+          const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ LoraTcArgs a1, int ctas0) {
+  // Two independent products can share one launch: CTAs [0, ctas0) work on
+  // the first, the rest on the second (same operand layouts and cluster size).
+  const bool second = (int)blockIdx.x >= ctas0;
+  const LoraTcArgs &a = second ? a1 : a0;
+  const CUtensorMap *tmA = second ? &tmA1 : &tmA0;
+  const CUtensorMap *tmB = second ? &tmB1 : &tmB0;
+  const int bid = second ? (int)blockIdx.x - ctas0 : (int)blockIdx.x;
   using G = LGeo<NQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -64,7 +73,7 @@ k_lora_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t crank = ptx::cluster_ctarank(), csize = ptx::cluster_nctarank();
-  const int64_t p0 = (int64_t)(blockIdx.x / csize) * LBP;
+  const int64_t p0 = (int64_t)(bid / (int)csize) * LBP;
   const int64_t nT = (a.T + LBT - 1) / LBT;
   const int64_t ks0 = (int64_t)crank * nT / csize, ks1 = (int64_t)(crank + 1) * nT / csize;
   const int nsteps = (int)(ks1 - ks0);
@@ -79,8 +88,8 @@ k_lora_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    ptx::prefetch_tmap(&tmA);
-    ptx::prefetch_tmap(&tmB);
+    ptx::prefetch_tmap(tmA);
+    ptx::prefetch_tmap(tmB);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), NQ);
@@ -108,16 +117,16 @@ k_lora_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
       const int t0 = (int)((ks0 + i) * LBT);
       ptx::mbar_arrive_expect_tx(full(s), G::STAGE);
       if (!A_MN) {
-        ptx::tma_load_2d(a_dst, &tmA, full(s), t0, (int)p0);  // rows p, inner t
+        ptx::tma_load_2d(a_dst, tmA, full(s), t0, (int)p0);  // rows p, inner t
       } else {
-        ptx::tma_load_2d(a_dst, &tmA, full(s), (int)p0, t0);  // rows t, inner p: two 64-wide atoms
-        ptx::tma_load_2d(a_dst + 8192, &tmA, full(s), (int)p0 + 64, t0);
+        ptx::tma_load_2d(a_dst, tmA, full(s), (int)p0, t0);  // rows t, inner p: two 64-wide atoms
+        ptx::tma_load_2d(a_dst + 8192, tmA, full(s), (int)p0 + 64, t0);
       }
       if (!B_MN) {
-        ptx::tma_load_2d(b_dst, &tmB, full(s), t0, 0);
+        ptx::tma_load_2d(b_dst, tmB, full(s), t0, 0);
       } else {
 #pragma unroll
-        for (int j = 0; j < NQ / 64; ++j) ptx::tma_load_2d(b_dst + 8192 * j, &tmB, full(s), 64 * j, t0);
+        for (int j = 0; j < NQ / 64; ++j) ptx::tma_load_2d(b_dst + 8192 * j, tmB, full(s), 64 * j, t0);
       }
     }
   } else if (warp == 1 && lane == 0) {
@@ -221,7 +230,26 @@ k_lora_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 }
 
 template <bool A_MN, bool B_MN, int NQ>
-int launch_t(const LoraProblem &L, cudaStream_t st) {
+int prepare(const LoraProblem &L, CUtensorMap *tA, CUtensorMap *tB, LoraTcArgs *a) {
+  // A operand: K-major [P][T] (box 64 x 128) or MN-major [T][P] (box 64 x 64)
+  int rc = A_MN ? make_tmap(tA, L.A, (uint64_t)L.P, (uint64_t)L.T, 64)
+                : make_tmap(tA, L.A, (uint64_t)L.T, (uint64_t)L.P, LBP);
+  // B operand: K-major [Q][T] (box 64 x NQ) or MN-major [T][Q] (box 64 x 64)
+  if (!rc)
+    rc = B_MN ? make_tmap(tB, L.B, (uint64_t)L.Q, (uint64_t)L.T, 64)
+              : make_tmap(tB, L.B, (uint64_t)L.T, (uint64_t)L.Q, NQ);
+  if (rc) return rc;
+  *a = LoraTcArgs{};
+  a->P = L.P; a->Q = L.Q; a->T = L.T; a->mode = L.mode; a->scale = L.scale;
+  a->out = L.out; a->ldo = L.ldo; a->out2 = L.out2; a->ldo2 = L.ldo2;
+  a->wait_at_end = L.wait_at_end ? 1 : 0;
+  a->status = device_status_ptr();
+  return QL_OK;
+}
+
+// One launch for L0 and, if given, L1 (same layouts and width class).
+template <bool A_MN, bool B_MN, int NQ>
+int launch_t(const LoraProblem &L0, const LoraProblem *L1, cudaStream_t st) {
   using G = LGeo<NQ>;
   static bool attr_done[64] = {};
   int dev = 0;
@@ -233,24 +261,19 @@ int launch_t(const LoraProblem &L, cudaStream_t st) {
     if (rc) return rc;
     attr_done[dev] = true;
   }
-  CUtensorMap tA, tB;
-  // A operand: K-major [P][T] (box 64 x 128) or MN-major [T][P] (box 64 x 64)
-  int rc = A_MN ? make_tmap(&tA, L.A, (uint64_t)L.P, (uint64_t)L.T, 64)
-                : make_tmap(&tA, L.A, (uint64_t)L.T, (uint64_t)L.P, LBP);
-  // B operand: K-major [Q][T] (box 64 x NQ) or MN-major [T][Q] (box 64 x 64)
-  if (!rc)
-    rc = B_MN ? make_tmap(&tB, L.B, (uint64_t)L.Q, (uint64_t)L.T, 64)
-              : make_tmap(&tB, L.B, (uint64_t)L.T, (uint64_t)L.Q, NQ);
+  CUtensorMap tA0, tB0, tA1, tB1;
+  LoraTcArgs a0, a1;
+  int rc = prepare<A_MN, B_MN, NQ>(L0, &tA0, &tB0, &a0);
+  if (!rc && L1) rc = prepare<A_MN, B_MN, NQ>(*L1, &tA1, &tB1, &a1);
   if (rc) return rc;
-  LoraTcArgs a{};
-  a.P = L.P; a.Q = L.Q; a.T = L.T; a.mode = L.mode; a.scale = L.scale;
-  a.out = L.out; a.ldo = L.ldo; a.out2 = L.out2; a.ldo2 = L.ldo2;
-  a.wait_at_end = L.wait_at_end ? 1 : 0;
-  a.status = device_status_ptr();
-  const int64_t tiles = (L.P + LBP - 1) / LBP;
-  const int S = lora_splits(L.P, L.T);
+  if (!L1) {
+    tA1 = tA0; tB1 = tB0; a1 = a0;
+  }
+  const int64_t tiles0 = (L0.P + LBP - 1) / LBP, tiles1 = L1 ? (L1->P + LBP - 1) / LBP : 0;
+  int S = lora_splits(L0.P + (L1 ? L1->P : 0), L1 ? std::min(L0.T, L1->T) : L0.T);
+  const int ctas0 = (int)(tiles0 * S);
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3((unsigned)(tiles * S));
+  cfg.gridDim = dim3((unsigned)((tiles0 + tiles1) * S));
   cfg.blockDim = dim3(LTHREADS);
   cfg.dynamicSmemBytes = G::SMEM;
   cfg.stream = st;
@@ -263,14 +286,14 @@ int launch_t(const LoraProblem &L, cudaStream_t st) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_lora_tc<A_MN, B_MN, NQ>, tA, tB, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_lora_tc<A_MN, B_MN, NQ>, tA0, tB0, a0, tA1, tB1, a1, ctas0);
   count_launch();
   return check_cuda(e, "LoRA kernel launch");
 }
 
 template <bool A_MN, bool B_MN>
-int launch_ab(const LoraProblem &L, cudaStream_t st) {
-  return L.Q <= 64 ? launch_t<A_MN, B_MN, 64>(L, st) : launch_t<A_MN, B_MN, 128>(L, st);
+int launch_ab(const LoraProblem &L, const LoraProblem *L1, cudaStream_t st) {
+  return L.Q <= 64 ? launch_t<A_MN, B_MN, 64>(L, L1, st) : launch_t<A_MN, B_MN, 128>(L, L1, st);
 }
 
 }  // namespace
@@ -286,8 +309,18 @@ int lora_splits(int64_t P, int64_t T) {
 }
 
 int launch_lora(const LoraProblem &L, cudaStream_t st) {
-  if (L.a_mn) return L.b_mn ? launch_ab<true, true>(L, st) : launch_ab<true, false>(L, st);
-  return L.b_mn ? launch_ab<false, true>(L, st) : launch_ab<false, false>(L, st);
+  if (L.a_mn) return L.b_mn ? launch_ab<true, true>(L, nullptr, st) : launch_ab<true, false>(L, nullptr, st);
+  return L.b_mn ? launch_ab<false, true>(L, nullptr, st) : launch_ab<false, false>(L, nullptr, st);
+}
+
+int launch_lora2(const LoraProblem &L0, const LoraProblem &L1, cudaStream_t st) {
+  const bool same = L0.a_mn == L1.a_mn && L0.b_mn == L1.b_mn && (L0.Q <= 64) == (L1.Q <= 64);
+  if (!same) {
+    int rc = launch_lora(L0, st);
+    return rc ? rc : launch_lora(L1, st);
+  }
+  if (L0.a_mn) return L0.b_mn ? launch_ab<true, true>(L0, &L1, st) : launch_ab<true, false>(L0, &L1, st);
+  return L0.b_mn ? launch_ab<false, true>(L0, &L1, st) : launch_ab<false, false>(L0, &L1, st);
 }
 
 }  // namespace ql

@@ -69,6 +69,9 @@ struct LoraProblem {
   bool wait_at_end = false;
 };
 int launch_lora(const LoraProblem &L, cudaStream_t st);
+// L0 and L1 in one launch when their operand layouts and width class agree
+// (else two launches); both must be independent of each other.
+int launch_lora2(const LoraProblem &L0, const LoraProblem &L1, cudaStream_t st);
 int lora_splits(int64_t P, int64_t T);
 
 }  // namespace ql
