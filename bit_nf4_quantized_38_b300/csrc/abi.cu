@@ -113,6 +113,7 @@ extern "C" int nf4_quantize(const uint16_t *W, const ql_nf4_tensor *q, void *ws,
     return set_error(QL_ERR_UNSUPPORTED, "nf4_quantize: workspace %zu < %zu bytes", ws_bytes,
                      quantize_ws(q->rows, q->cols));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  note_other_call(st);
   double *sum = static_cast<double *>(ws);
   float *absmax = q->dq_blocksize ? reinterpret_cast<float *>(static_cast<char *>(ws) + 256) : q->absmax;
   const int64_t n_b = q->rows * q->cols / 64;
@@ -131,6 +132,7 @@ extern "C" int nf4_dequantize(const ql_nf4_tensor *q, uint16_t *W_out, ql_stream
   if (rc) return rc;
   if (!W_out) return set_error(QL_ERR_INVALID, "nf4_dequantize: null output");
   if (!aligned(W_out, 16)) return set_error(QL_ERR_MISALIGNED, "nf4_dequantize: output not 16-byte aligned");
+  note_other_call(reinterpret_cast<cudaStream_t>(stream));
   return check_cuda(launch_dequantize(*q, W_out, reinterpret_cast<cudaStream_t>(stream)),
                     "nf4_dequantize: launch");
 }

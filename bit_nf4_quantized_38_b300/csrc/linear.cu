@@ -13,6 +13,10 @@
 //   3. dA = X^T Gs                                          LoRA kernel
 //   4. dB = s XA^T dY                                       LoRA kernel (stores dB^T's transpose)
 #include <algorithm>
+#include <mutex>
+#include <unordered_map>
+#include <utility>
+#include <vector>
 
 #include "decode.cuh"
 #include "linear.cuh"
@@ -50,7 +54,66 @@ int check_common(const LinearArgs &a, const char *fn, size_t need) {
 
 constexpr int64_t kDecodeMaxM = 16;  // M at or below this takes the decode path
 
+// ---------------------------------------------------------------------------
+// What the previous library call on a stream may still be writing.
+//
+// Within a call the kernels are programmatic dependents of one another, and
+// so is the first kernel of a training call of the one before it.  When that
+// first kernel's inputs are disjoint from everything the previous training
+// call writes (its outputs and its workspace), it may read and compute while
+// that call's last kernels still run, and waits only before its first store:
+// every kernel older than the previous call has completed by the time the
+// previous call lets a dependent start (each call waits for its predecessor
+// before its own stores), and a kernel launched without programmatic
+// dependence in between makes the hardware fall back to full ordering.
+struct Range {
+  uintptr_t lo, hi;
+};
+struct PrevCall {
+  bool training = false;  // a training linear call (its last kernel lets dependents start)
+  std::vector<Range> writes;
+};
+std::mutex g_prev_mu;
+std::unordered_map<cudaStream_t, PrevCall> g_prev;
+
+Range range(const void *p, size_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Range{a, a + bytes};
+}
+
+// True if the stream's previous call was a training call whose writes miss all of `reads`.
+bool reads_clear_of_previous(cudaStream_t st, const std::vector<Range> &reads) {
+  std::lock_guard<std::mutex> lock(g_prev_mu);
+  auto it = g_prev.find(st);
+  if (it == g_prev.end() || !it->second.training) return false;
+  for (const Range &r : reads)
+    for (const Range &w : it->second.writes)
+      if (r.lo < w.hi && w.lo < r.hi) return false;
+  return true;
+}
+
+void note_call(cudaStream_t st, bool training, std::vector<Range> writes) {
+  std::lock_guard<std::mutex> lock(g_prev_mu);
+  PrevCall &pc = g_prev[st];
+  pc.training = training;
+  pc.writes = std::move(writes);
+}
+
+void weight_ranges(const ql_nf4_tensor &W, std::vector<Range> &out) {
+  const int64_t n_b = W.rows * W.cols / 64;
+  out.push_back(range(W.packed, (size_t)(W.rows * W.cols / 2)));
+  if (W.dq_blocksize) {
+    out.push_back(range(W.absmax_code, (size_t)n_b));
+    out.push_back(range(W.dq_step, (size_t)((n_b + 255) / 256) * 4));
+    out.push_back(range(W.dq_mean, 4));
+  } else {
+    out.push_back(range(W.absmax, (size_t)n_b * 4));
+  }
+}
+
 }  // namespace
+
+void note_other_call(cudaStream_t st) { note_call(st, false, {}); }
 
 size_t linear_fwd_ws(int64_t M, int64_t N, int64_t K, int32_t r) {
   if (M <= 0 || N <= 0 || K <= 0 || !rank_ok(r)) return 0;
@@ -75,16 +138,26 @@ int linear_fwd(const LinearArgs &a) {
     DecodeProblem d{};
     d.X = a.X; d.M = M; d.K = K; d.N = N; d.w = nf4_view(a.W); d.A = a.A; d.B = a.B; d.r = r;
     d.scale = a.scale; d.Y = a.Y; d.XA_out = a.XA; d.ws = a.ws;
+    note_call(a.stream, false, {});
     return launch_decode(d, a.stream);
   }
   QL_TRY(check_common(a, fn, fwd_ws(M, r)));
   uint16_t *xas = static_cast<uint16_t *>(a.ws);
   cudaStream_t st = a.stream;
 
+  std::vector<Range> reads = {range(a.X, (size_t)(M * K * 2)), range(a.A, (size_t)(K * r * 2)),
+                             range(a.B, (size_t)(r * N * 2))};
+  weight_ranges(a.W, reads);
+  const bool early = reads_clear_of_previous(st, reads);
+  std::vector<Range> writes = {range(a.Y, (size_t)(M * N * 2)), range(a.ws, a.ws_bytes)};
+  if (a.XA) writes.push_back(range(a.XA, (size_t)(M * r * 2)));
+  note_call(st, true, std::move(writes));
+
   LoraProblem L{};
   L.A = a.X; L.a_mn = false; L.B = a.A; L.b_mn = true;  // X [M][K], A [K][r]
   L.P = M; L.Q = r; L.T = K; L.mode = 0; L.scale = a.scale;
   L.out = xas; L.ldo = r; L.out2 = a.XA; L.ldo2 = r;
+  L.dep = early ? kDepStores : kDepStart;
   QL_TRY(launch_lora(L, st));
   GemmProblem g{};
   g.trans = false;
@@ -110,11 +183,21 @@ int linear_bwd(const LinearArgs &a) {
   uint16_t *xa_tmp = reinterpret_cast<uint16_t *>(ws + up256((size_t)M * r * 2));
   cudaStream_t st = a.stream;
 
+  std::vector<Range> reads = {range(a.dY, (size_t)(M * N * 2)), range(a.X, (size_t)(M * K * 2)),
+                             range(a.A, (size_t)(K * r * 2)), range(a.B, (size_t)(r * N * 2))};
+  if (a.XA_in) reads.push_back(range(a.XA_in, (size_t)(M * r * 2)));
+  weight_ranges(a.W, reads);
+  const bool early = reads_clear_of_previous(st, reads);
+  note_call(st, true,
+            {range(a.dX, (size_t)(M * K * 2)), range(a.dA, (size_t)(K * r * 4)), range(a.dB, (size_t)(r * N * 4)),
+             range(a.ws, a.ws_bytes)});
+
   const uint16_t *xa = a.XA_in;
   if (!xa) {  // 0. XA = X A
     LoraProblem L{};
     L.A = a.X; L.a_mn = false; L.B = a.A; L.b_mn = true;
     L.P = M; L.Q = r; L.T = K; L.mode = 0; L.scale = 1.0f; L.out = xa_tmp; L.ldo = r;
+    L.dep = early ? kDepStores : kDepStart;
     QL_TRY(launch_lora(L, st));
     xa = xa_tmp;
   }
@@ -122,6 +205,8 @@ int linear_bwd(const LinearArgs &a) {
     LoraProblem L{};
     L.A = a.dY; L.a_mn = false; L.B = a.B; L.b_mn = false;
     L.P = M; L.Q = r; L.T = N; L.mode = 0; L.scale = a.scale; L.out = gs; L.ldo = r;
+    // first kernel of the call, or reading only inputs after the recompute above
+    L.dep = (early && !a.XA_in) ? kDepStart : (early ? kDepStores : kDepStart);
     QL_TRY(launch_lora(L, st));
   }
   {  // 2. dX = dY W_hat + Gs A^T
@@ -140,11 +225,11 @@ int linear_bwd(const LinearArgs &a) {
   LoraProblem LA{};
   LA.A = a.X; LA.a_mn = true; LA.B = gs; LA.b_mn = true;
   LA.P = K; LA.Q = r; LA.T = M; LA.mode = 1; LA.scale = 1.0f; LA.out = a.dA; LA.ldo = r;
-  LA.wait_at_end = true;
+  LA.dep = kDepExit;
   LoraProblem LB{};
   LB.A = a.dY; LB.a_mn = true; LB.B = xa; LB.b_mn = true;
   LB.P = N; LB.Q = r; LB.T = M; LB.mode = 2; LB.scale = a.scale; LB.out = a.dB; LB.ldo = N;
-  LB.wait_at_end = true;
+  LB.dep = kDepExit;
   return launch_lora2(LA, LB, st);
 }
 

@@ -34,7 +34,7 @@ struct LoraTcArgs {
   int64_t ldo;
   uint16_t *out2;
   int64_t ldo2;
-  int wait_at_end;  // 0: wait for the previous kernel before reading; 1: at the end only
+  int dep;  // kDepStart, kDepStores or kDepExit (see LoraProblem)
   int *status;
 };
 
@@ -99,13 +99,11 @@ k_lora_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // Launched as a programmatic dependent.  A kernel that reads the previous
-  // kernel's output waits here; one whose inputs were complete before the
-  // previous kernel let it start (wait_at_end) runs alongside that kernel and
-  // waits only before it exits, so that its completion still implies the
-  // completion of everything before it.
-  if (!a.wait_at_end) ptx::griddep_wait();
-  ptx::griddep_launch();
+  // Launched as a programmatic dependent; where it waits for the previous
+  // kernel depends on a.dep (see LoraProblem).  Dependents are let in only
+  // once this kernel has waited, except after kDepExit.
+  if (a.dep == kDepStart) ptx::griddep_wait();
+  if (a.dep != kDepStores) ptx::griddep_launch();
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- TMA
@@ -178,6 +176,10 @@ k_lora_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
   ptx::tc_fence_before();
   __syncthreads();
   ptx::cluster_sync();
+  if (a.dep == kDepStores) {  // the first global store follows
+    ptx::griddep_wait();
+    ptx::griddep_launch();
+  }
 
   // ---------------------------------------------------------------- cluster reduction
   // CTA c finishes rows [c*128/S, (c+1)*128/S) of the tile, adding the S
@@ -226,7 +228,7 @@ k_lora_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
   // keep this CTA's tile alive until every CTA of the cluster has read it
   ptx::cluster_sync();
   if (warp == 1) ptx::tmem_dealloc(tmem, NQ);
-  if (a.wait_at_end) ptx::griddep_wait();
+  if (a.dep == kDepExit) ptx::griddep_wait();
 }
 
 template <bool A_MN, bool B_MN, int NQ>
@@ -242,7 +244,7 @@ int prepare(const LoraProblem &L, CUtensorMap *tA, CUtensorMap *tB, LoraTcArgs *
   *a = LoraTcArgs{};
   a->P = L.P; a->Q = L.Q; a->T = L.T; a->mode = L.mode; a->scale = L.scale;
   a->out = L.out; a->ldo = L.ldo; a->out2 = L.out2; a->ldo2 = L.ldo2;
-  a->wait_at_end = L.wait_at_end ? 1 : 0;
+  a->dep = L.dep;
   a->status = device_status_ptr();
   return QL_OK;
 }

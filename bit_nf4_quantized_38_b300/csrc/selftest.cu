@@ -6,6 +6,7 @@
 // the caller's limit, so the status word must read "timed out" afterwards
 // while the context stays usable.
 #include "common.cuh"
+#include "linear.cuh"
 #include "ptx.cuh"
 
 namespace ql {
@@ -33,6 +34,7 @@ extern "C" int ql_selftest_wait(int64_t limit_ns, ql_stream_t stream) {
     return set_error(QL_ERR_INVALID, "ql_selftest_wait: limit %lld ns outside (0, 2 s]", (long long)limit_ns);
   int *status = device_status_ptr();
   if (!status) return set_error(QL_ERR_CUDA, "ql_selftest_wait: no device status word");
+  note_other_call(reinterpret_cast<cudaStream_t>(stream));
   k_selftest_wait<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>((uint64_t)limit_ns, status);
   count_launch();
   return check_cuda(cudaGetLastError(), "ql_selftest_wait launch");

@@ -64,10 +64,17 @@ struct LoraProblem {
   int64_t ldo;
   uint16_t *out2;
   int64_t ldo2;
-  // The kernel's inputs were all complete before the previous kernel in the
-  // stream let it start: run alongside that kernel, wait for it only at the end.
-  bool wait_at_end = false;
+  // Ordering against the previous kernel in the stream (programmatic
+  // dependent launch):
+  //   kDepStart  wait for it before reading anything (the default);
+  //   kDepStores the inputs are not written by any kernel still running: read
+  //              and compute alongside it, wait for it before the first store;
+  //   kDepExit   the inputs were complete before it let this kernel start and
+  //              this kernel writes nothing it reads: run alongside it, wait
+  //              only before exiting (so completion still implies its completion).
+  int dep = 0;
 };
+constexpr int kDepStart = 0, kDepStores = 1, kDepExit = 2;
 int launch_lora(const LoraProblem &L, cudaStream_t st);
 // L0 and L1 in one launch when their operand layouts and width class agree
 // (else two launches); both must be independent of each other.
