@@ -32,14 +32,15 @@ def f64(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def assert_close(name, got, want):
+def assert_close(name, got, want, elem=None):
+    elem = ELEM if elem is None else elem
     got = np.asarray(got, np.float64)
     want = np.asarray(want, np.float64)
     assert got.shape == want.shape, name
     diff = got - want
     rel = np.linalg.norm(diff) / max(np.linalg.norm(want), 1e-300)
     rms = np.sqrt(np.mean(want ** 2))
-    bound = ELEM * (np.abs(want) + rms)
+    bound = elem * (np.abs(want) + rms)
     worst = np.max(np.abs(diff) / bound)
     assert rel <= REL_FRO, f"{name}: relative Frobenius error {rel:.3e}"
     assert worst <= 1.0, f"{name}: element error {worst:.3f} of the bound"
@@ -184,3 +185,54 @@ def test_llama7b_linear_full_size_sampled(ql, idx):
     G = dYf @ Bf.T
     assert_close("dA", f64(dA), s * (Xf.T @ G))
     assert_close("dB", f64(dB), s * (XAr.T @ dYf))
+
+
+def test_chained_calls_read_the_previous_calls_output(ql):
+    """Layer 2 reads layer 1's Y, and layer 1's backward reads layer 2's dX, on
+    one stream with one workspace: the kernels of a call may start alongside
+    the previous call only when their inputs are disjoint from its writes, so
+    these calls must see the finished values.  The oracle chains the same
+    layers in fp64, rounding the handed-over activations to bf16.  Both sides
+    round the intermediate activation from values that already differ within
+    one layer's tolerance (a third of its bf16 values land one step apart), so
+    a chained output may carry twice one layer's element error: its element
+    bound is 2e-2.  A read of unfinished data would miss it by orders of
+    magnitude."""
+    from bit_nf4_quantized_38_b300.workloads import normal_bf16, normal_with_outliers_bf16
+    from oracle.bf16 import bf16_bits_to_f32, f32_to_bf16_bits
+    M, K, H, N, r, s = 512, 384, 640, 448, 16, 2.0
+    dev = torch.device("cuda")
+    W1 = normal_with_outliers_bf16((H, K), 0.02, 0.001, 20.0, 71)
+    W2 = normal_with_outliers_bf16((N, H), 0.02, 0.001, 20.0, 72)
+    X = normal_bf16((M, K), 1.0, 73)
+    A1, B1 = normal_bf16((K, r), 0.25, 74), normal_bf16((r, H), 0.01, 75)
+    A2, B2 = normal_bf16((H, r), 0.25, 76), normal_bf16((r, N), 0.01, 77)
+    dY2 = normal_bf16((M, N), 1.0, 78)
+    q1, q2 = ql.nf4_quantize(W1.to(dev)), ql.nf4_quantize(W2.to(dev))
+    ws = torch.empty(max(ql.workspace_size(ql.OP_LINEAR_FWD, M, 640, 640, r),
+                         ql.workspace_size(ql.OP_LINEAR_BWD, M, 640, 640, r)), dtype=torch.uint8, device=dev)
+    Xd, A1d, B1d, A2d, B2d, dY2d = (t.to(dev) for t in (X, A1, B1, A2, B2, dY2))
+    for _ in range(3):  # repeated, so later rounds follow a training call on the stream
+        Y1, XA1 = ql.qlora_linear_fwd(Xd, q1, A1d, B1d, s, ws=ws)
+        Y2, XA2 = ql.qlora_linear_fwd(Y1, q2, A2d, B2d, s, ws=ws)
+        dY1, dA2, dB2 = ql.qlora_linear_bwd(dY2d, Y1, XA2, q2, A2d, B2d, s, ws=ws)
+        dX, dA1, dB1 = ql.qlora_linear_bwd(dY1, Xd, XA1, q1, A1d, B1d, s, ws=ws)
+    torch.cuda.synchronize()
+    ql.device_status()
+
+    def to_bf16(x):
+        return bf16_bits_to_f32(f32_to_bf16_bits(np.asarray(x, np.float32))).astype(np.float64)
+
+    Wh1 = nf4.dequantize(nf4.quantize(bits(W1)))
+    Wh2 = nf4.dequantize(nf4.quantize(bits(W2)))
+    Y1r, _ = linear.lora_forward(bits(X), Wh1, bits(A1), bits(B1), s)
+    H1 = to_bf16(Y1r)  # the activation handed to layer 2, in bf16
+    Y2r, _ = linear.lora_forward(H1, Wh2, bits(A2), bits(B2), s)
+    assert_close("Y1", f64(Y1), Y1r)
+    assert_close("Y2", f64(Y2), Y2r, elem=2 * ELEM)
+    dY1r, dA2r, _, _ = linear.lora_backward(bits(dY2), H1, Wh2, bits(A2), bits(B2), s)
+    assert_close("dX of layer 2", f64(dY1), dY1r, elem=2 * ELEM)
+    assert_close("dA of layer 2", f64(dA2), dA2r, elem=2 * ELEM)
+    dXr, dA1r, _, _ = linear.lora_backward(to_bf16(dY1r), bits(X), Wh1, bits(A1), bits(B1), s)
+    assert_close("dX of layer 1", f64(dX), dXr, elem=2 * ELEM)
+    assert_close("dA of layer 1", f64(dA1), dA1r, elem=2 * ELEM)
