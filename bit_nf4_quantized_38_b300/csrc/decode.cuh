@@ -14,10 +14,15 @@ struct DecodeProblem {
   float scale;
   uint16_t *Y;        // M x N
   uint16_t *XA_out;   // M x r or null
-  void *ws;
+  void *ws;           // any contents on entry; two halves, calls alternate
+  int half;           // the half this call uses (the other one's call may still run)
+  bool w_early;       // the previous grid writes none of the weight's arrays
+  bool x_early;       // nor X, A or B
+  bool ws_early;      // the previous grid touches none of this call's workspace half
 };
 
 size_t decode_ws(int64_t N, int64_t K, int r);
+size_t decode_ws_half(int64_t N, int r);
 int launch_decode(const DecodeProblem &p, cudaStream_t st);
 
 }  // namespace ql

@@ -55,23 +55,26 @@ int check_common(const LinearArgs &a, const char *fn, size_t need) {
 constexpr int64_t kDecodeMaxM = 16;  // M at or below this takes the decode path
 
 // ---------------------------------------------------------------------------
-// What the previous library call on a stream may still be writing.
+// What the previous library call on a stream may still be reading or writing.
 //
 // Within a call the kernels are programmatic dependents of one another, and
-// so is the first kernel of a training call of the one before it.  When that
-// first kernel's inputs are disjoint from everything the previous training
+// so is the first kernel of a linear call of the one before it.  When that
+// first kernel's inputs are disjoint from everything the previous linear
 // call writes (its outputs and its workspace), it may read and compute while
 // that call's last kernels still run, and waits only before its first store:
 // every kernel older than the previous call has completed by the time the
-// previous call lets a dependent start (each call waits for its predecessor
-// before its own stores), and a kernel launched without programmatic
-// dependence in between makes the hardware fall back to full ordering.
+// previous call lets a dependent start (a call's kernels let dependents start
+// only after waiting for their own predecessor), and a kernel launched
+// without programmatic dependence in between makes the hardware fall back to
+// full ordering.  The decode kernel may also store early, into workspace and
+// outputs that the previous call neither reads nor writes.
 struct Range {
   uintptr_t lo, hi;
 };
 struct PrevCall {
-  bool training = false;  // a training linear call (its last kernel lets dependents start)
-  std::vector<Range> writes;
+  bool linear = false;  // a linear call (its kernels let dependents start early)
+  std::vector<Range> writes, reads;
+  int decode_half = 0;  // workspace half of the stream's last decode call
 };
 std::mutex g_prev_mu;
 std::unordered_map<cudaStream_t, PrevCall> g_prev;
@@ -81,22 +84,47 @@ Range range(const void *p, size_t bytes) {
   return Range{a, a + bytes};
 }
 
-// True if the stream's previous call was a training call whose writes miss all of `reads`.
+// True if the stream's previous call was a linear call whose writes miss all of `reads`.
 bool reads_clear_of_previous(cudaStream_t st, const std::vector<Range> &reads) {
   std::lock_guard<std::mutex> lock(g_prev_mu);
   auto it = g_prev.find(st);
-  if (it == g_prev.end() || !it->second.training) return false;
+  if (it == g_prev.end() || !it->second.linear) return false;
   for (const Range &r : reads)
     for (const Range &w : it->second.writes)
       if (r.lo < w.hi && w.lo < r.hi) return false;
   return true;
 }
 
-void note_call(cudaStream_t st, bool training, std::vector<Range> writes) {
+// True if the stream's previous call was a linear call that neither reads
+// nor writes any of `writes`.
+bool writes_clear_of_previous(cudaStream_t st, const std::vector<Range> &writes) {
+  std::lock_guard<std::mutex> lock(g_prev_mu);
+  auto it = g_prev.find(st);
+  if (it == g_prev.end() || !it->second.linear) return false;
+  for (const Range &r : writes) {
+    for (const Range &w : it->second.writes)
+      if (r.lo < w.hi && w.lo < r.hi) return false;
+    for (const Range &w : it->second.reads)
+      if (r.lo < w.hi && w.lo < r.hi) return false;
+  }
+  return true;
+}
+
+void note_call(cudaStream_t st, bool linear, std::vector<Range> writes, std::vector<Range> reads = {}) {
   std::lock_guard<std::mutex> lock(g_prev_mu);
   PrevCall &pc = g_prev[st];
-  pc.training = training;
+  pc.linear = linear;
   pc.writes = std::move(writes);
+  pc.reads = std::move(reads);
+}
+
+// Decode calls on a stream alternate between the two halves of their
+// workspace, so a call never writes the half its predecessor may still use.
+int next_decode_half(cudaStream_t st) {
+  std::lock_guard<std::mutex> lock(g_prev_mu);
+  PrevCall &pc = g_prev[st];
+  pc.decode_half ^= 1;
+  return pc.decode_half;
 }
 
 void weight_ranges(const ql_nf4_tensor &W, std::vector<Range> &out) {
@@ -138,7 +166,21 @@ int linear_fwd(const LinearArgs &a) {
     DecodeProblem d{};
     d.X = a.X; d.M = M; d.K = K; d.N = N; d.w = nf4_view(a.W); d.A = a.A; d.B = a.B; d.r = r;
     d.scale = a.scale; d.Y = a.Y; d.XA_out = a.XA; d.ws = a.ws;
-    note_call(a.stream, false, {});
+    d.half = next_decode_half(a.stream);
+    std::vector<Range> reads;
+    weight_ranges(a.W, reads);
+    d.w_early = reads_clear_of_previous(a.stream, reads);
+    const std::vector<Range> xab = {range(a.X, (size_t)(M * K * 2)), range(a.A, (size_t)(K * r * 2)),
+                                    range(a.B, (size_t)(r * N * 2))};
+    d.x_early = d.w_early && reads_clear_of_previous(a.stream, xab);
+    reads.insert(reads.end(), xab.begin(), xab.end());
+    const size_t half = decode_ws_half(N, r);
+    const Range wsr = range(static_cast<char *>(a.ws) + (d.half ? half : 0), half);
+    std::vector<Range> outs = {range(a.Y, (size_t)(M * N * 2))};
+    if (a.XA) outs.push_back(range(a.XA, (size_t)(M * r * 2)));
+    d.ws_early = writes_clear_of_previous(a.stream, {wsr});
+    outs.push_back(wsr);
+    note_call(a.stream, true, std::move(outs), std::move(reads));
     return launch_decode(d, a.stream);
   }
   QL_TRY(check_common(a, fn, fwd_ws(M, r)));
@@ -151,7 +193,7 @@ int linear_fwd(const LinearArgs &a) {
   const bool early = reads_clear_of_previous(st, reads);
   std::vector<Range> writes = {range(a.Y, (size_t)(M * N * 2)), range(a.ws, a.ws_bytes)};
   if (a.XA) writes.push_back(range(a.XA, (size_t)(M * r * 2)));
-  note_call(st, true, std::move(writes));
+  note_call(st, true, std::move(writes), reads);
 
   LoraProblem L{};
   L.A = a.X; L.a_mn = false; L.B = a.A; L.b_mn = true;  // X [M][K], A [K][r]
@@ -190,7 +232,8 @@ int linear_bwd(const LinearArgs &a) {
   const bool early = reads_clear_of_previous(st, reads);
   note_call(st, true,
             {range(a.dX, (size_t)(M * K * 2)), range(a.dA, (size_t)(K * r * 4)), range(a.dB, (size_t)(r * N * 4)),
-             range(a.ws, a.ws_bytes)});
+             range(a.ws, a.ws_bytes)},
+            reads);
 
   const uint16_t *xa = a.XA_in;
   if (!xa) {  // 0. XA = X A

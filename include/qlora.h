@@ -163,6 +163,9 @@ QL_API int nf4_dequantize(const ql_nf4_tensor *q, uint16_t *W_out, ql_stream_t s
  *   scale  : s = alpha / r.
  *   ws     : ql_workspace_size(QL_OP_LINEAR_FWD, M, N, K, r) bytes.
  * M >= 1.  M <= 16 takes the decode (GEMV) path, larger M the tensor-core path.
+ * The decode path keeps partial results in `ws` (any initial contents work);
+ * successive decode calls on a stream alternate between its two halves, so a
+ * call may start while the previous one finishes.
  */
 QL_API int qlora_linear_fwd(const uint16_t *X, int64_t M, const ql_nf4_tensor *W,
                      const uint16_t *A, const uint16_t *B, int32_t r,

@@ -104,3 +104,71 @@ def test_decode_is_deterministic_and_repeatable(ql):
     outs = [ql.qlora_linear_fwd(X, q, A, B, 0.25)[0] for _ in range(3)]
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+def test_decode_chained_calls_and_any_workspace_contents(ql):
+    """Layer chains on one stream: the second call reads the first call's Y (it
+    must wait for it) while its weight may stream early.  Results must equal
+    the same calls made one at a time with a synchronisation in between, on a
+    workspace filled with arbitrary bytes (the arrival counters carry a call
+    stamp, so no initialisation is needed)."""
+    from bit_nf4_quantized_38_b300.workloads import normal_bf16
+    dev = torch.device("cuda")
+    K0, N1, N2, r = 1024, 2048, 1024, 16
+    q1 = ql.nf4_quantize(normal_bf16((N1, K0), 0.02, 11).to(dev))
+    q2 = ql.nf4_quantize(normal_bf16((N2, N1), 0.02, 12).to(dev))
+    X = normal_bf16((4, K0), 1.0, 13).to(dev)
+    A1, B1 = normal_bf16((K0, r), 0.25, 14).to(dev), normal_bf16((r, N1), 0.01, 15).to(dev)
+    A2, B2 = normal_bf16((N1, r), 0.25, 16).to(dev), normal_bf16((r, N2), 0.01, 17).to(dev)
+    nbytes = max(ql.workspace_size(ql.OP_LINEAR_FWD, 4, N1, K0, r), ql.workspace_size(ql.OP_LINEAR_FWD, 4, N2, N1, r))
+    g = torch.Generator(device="cpu").manual_seed(5)
+    ws = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, generator=g).to(dev)
+    # one at a time
+    Y1s, _ = ql.qlora_linear_fwd(X, q1, A1, B1, 1.0)
+    torch.cuda.synchronize()
+    Y2s, _ = ql.qlora_linear_fwd(Y1s.clone(), q2, A2, B2, 1.0)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        Y1, _ = ql.qlora_linear_fwd(X, q1, A1, B1, 1.0, ws=ws)
+        Y2, _ = ql.qlora_linear_fwd(Y1, q2, A2, B2, 1.0, ws=ws)
+        Y3, _ = ql.qlora_linear_fwd(X, q1, A1, B1, 1.0, ws=ws)  # reads nothing the previous call wrote
+        torch.cuda.synchronize()
+        ql.device_status()
+        assert torch.equal(Y1, Y1s) and torch.equal(Y2, Y2s) and torch.equal(Y3, Y1s)
+
+
+def test_decode_graph_replays_reuse_the_workspace(ql):
+    """A captured sequence of decode calls on one workspace (the same call
+    stamps every replay) gives the eager results on every replay."""
+    from bit_nf4_quantized_38_b300.workloads import normal_bf16
+    dev = torch.device("cuda")
+    shapes = [(1024, 1024, 1), (3072, 1024, 16), (1024, 3072, 9)]
+    calls = []
+    for i, (N, K, M) in enumerate(shapes):
+        q = ql.nf4_quantize(normal_bf16((N, K), 0.02, 30 + i).to(dev))
+        X = normal_bf16((M, K), 1.0, 40 + i).to(dev)
+        A, B = normal_bf16((K, 64), 0.125, 50 + i).to(dev), normal_bf16((64, N), 0.01, 60 + i).to(dev)
+        calls.append((X, q, A, B))
+    nbytes = max(ql.workspace_size(ql.OP_LINEAR_FWD, M, N, K, 64) for N, K, M in shapes)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    eager = []
+    for X, q, A, B in calls:
+        Y, XA = ql.qlora_linear_fwd(X, q, A, B, 0.25, ws=ws)
+        eager.append((Y.clone(), XA.clone()))
+    outs = [(torch.empty_like(Y), torch.empty_like(XA)) for Y, XA in eager]
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            for (X, q, A, B), (Y, XA) in zip(calls, outs):
+                ql.qlora_linear_fwd(X, q, A, B, 0.25, Y=Y, XA=XA, ws=ws)
+    for _ in range(4):
+        for Y, XA in outs:
+            Y.fill_(0)
+            XA.fill_(0)
+        graph.replay()
+        torch.cuda.synchronize()
+        ql.device_status()
+        for (Y, XA), (Ye, XAe) in zip(outs, eager):
+            assert torch.equal(Y, Ye) and torch.equal(XA, XAe)
