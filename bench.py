@@ -192,6 +192,62 @@ def oracle_sample_flops(s):
     return 4 * s["M"] * c.N * c.K + 6 * s["M"] * c.r * (c.N + c.K)
 
 
+def cpu_oracle_details(s):
+    """Bounded samples of the other workloads, timed once each on the host's
+    cores with the same oracle: the single 1024 x 1024 linear in full; the
+    q_proj sample on one BLAS thread; 512 rows of the 5120 x 5120 decode layer
+    (dequantize + forward, M = 1); 512 rows of an 8192-wide LLaMA-65B weight
+    (quantize, then dequantize).  Rates use the algorithmic bytes or flops of
+    the sample itself."""
+    from threadpoolctl import threadpool_limits
+    from bit_nf4_quantized_38_b300.workloads import (bf16_bits, case_inputs, case_weight, llama13b_decode,
+                                                     single_linear_1024, student_t4_bf16)
+    from oracle import linear, nf4
+    out = {"host_cores": cpu_cores(), "blas_threads": blas_threads()}
+    # the single linear (quantize + dequantize + fwd + bwd), in full
+    c = single_linear_1024().cases[0]
+    W = bf16_bits(case_weight(c))
+    X, A, B, dY = (bf16_bits(t) for t in case_inputs(c))
+    t0 = time.perf_counter()
+    Wh = nf4.dequantize(nf4.quantize(W))
+    linear.lora_forward(X, Wh, A, B, c.scale)
+    linear.lora_backward(dY, X, Wh, A, B, c.scale)
+    out["single_linear_1024_us"] = (time.perf_counter() - t0) * 1e6
+    # the q_proj training sample on one thread
+    with threadpool_limits(limits=1):
+        t0 = time.perf_counter()
+        oracle_sample_step(s)
+        dt = time.perf_counter() - t0
+    out["llama7b_q_proj_sample_1thread_tflops"] = oracle_sample_flops(s) / dt / 1e12
+    # decode: 512 of the 5120 rows of the 13B 5120 x 5120 layer, M = 1
+    c = llama13b_decode(M=1).cases[0]
+    rows = 512
+    W = bf16_bits(case_weight(c))[:rows]
+    X, A, B, _ = (bf16_bits(t) for t in case_inputs(c))
+    qt = nf4.quantize(W)
+    t0 = time.perf_counter()
+    linear.lora_forward(X, nf4.dequantize(qt), A, B[:, :rows], c.scale)
+    dt = time.perf_counter() - t0
+    n_b = rows * c.K // 64
+    byts = rows * c.K // 2 + n_b + 4 * ((n_b + 255) // 256) + 2 * c.r * (c.K + rows) + 2 * (c.K + rows)
+    out["llama13b_decode_sample_gbs"] = byts / dt / 1e9
+    # quantize / dequantize: 512 rows of an 8192-wide Student-t(4) weight
+    W = bf16_bits(student_t4_bf16((512, 8192), 0.015, 300, "cpu"))
+    n = W.size
+    t0 = time.perf_counter()
+    qt = nf4.quantize(W)
+    t1 = time.perf_counter()
+    nf4.dequantize(qt)
+    t2 = time.perf_counter()
+    byts = n * (2 + 0.5 + 1 / 64 + 4 / (64 * 256))
+    out["llama65b_quantize_sample_gbs"] = byts / (t1 - t0) / 1e9
+    out["llama65b_dequantize_sample_gbs"] = byts / (t2 - t1) / 1e9
+    out["samples"] = ("single linear 1024x1024 M=16 r=8 in full; q_proj 512-token sample on 1 BLAS thread; "
+                      "512 of 5120 rows of the 13B 5120x5120 decode layer (M=1, dequantize + fwd); "
+                      "512 x 8192 Student-t(4) weight (quantize, dequantize)")
+    return out
+
+
 def cpu_baseline(repeats=3):
     s = oracle_sample_setup()
     oracle_sample_step(s)  # warm
@@ -202,7 +258,8 @@ def cpu_baseline(repeats=3):
     return {"value": oracle_sample_flops(s) / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
             "kind": "oracle",
             "sample": f"q_proj 4096x4096 linear, {s['M']} tokens, r=64: NF4+DQ dequantize + fwd + bwd in "
-                      f"fp64 numpy, mean of {repeats} runs ({dt:.2f} s each)"}
+                      f"fp64 numpy, mean of {repeats} runs ({dt:.2f} s each)",
+            "details": cpu_oracle_details(s)}
 
 
 def run_reference(args):
