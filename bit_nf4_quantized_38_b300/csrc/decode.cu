@@ -276,9 +276,10 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
       for (int j = 0; j < 4; ++j) ptx::tma_load_2d(dst + W_BYTES + j * XR * 128, &tmX, fb, b * UNIT_K + 64 * j, 0);
   };
 
-  // Setup.  The copies that need no wait go out first (weight boxes, and X
-  // and the XA chunk when X may be read early); the lookup table is built
-  // meanwhile.
+  // Setup.  Once the barriers exist, one lane of each of warps 0..2 issues
+  // the copies of one of the first three units (weight box, and X when X may
+  // be read early) and one lane of warp 3 the first XA chunk, while the other
+  // threads build the lookup table.
   if (tid == 0) {
     for (int s = 0; s < ST_STAGES; ++s) {
       ptx::mbar_init(ptx::smem_u32(&full_bar[s]), 1);
@@ -289,15 +290,22 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     ptx::fence_mbar_init();
     abort_flag = 0;
     xa_chunks = 0;
-    ptx::prefetch_tmap(&tmW);
-    ptx::prefetch_tmap(&tmX);
+  }
+  __syncthreads();
+  if (lane == 0 && (warp < npre || (warp == ST_STAGES && xa_cta))) {
     if (!a.w_early) ptx::griddep_wait();
-    for (int i = 0; i < npre; ++i) issue(i, true, a.x_early);
-    if (!a.x_early) {  // X may still be being written: the X boxes and XA chunk follow the wait
-      ptx::griddep_wait();
-      for (int i = 0; i < npre; ++i) issue(i, false, true);
+    if (warp < npre) {
+      ptx::prefetch_tmap(&tmW);
+      ptx::prefetch_tmap(&tmX);
+      issue(warp, true, a.x_early);
+      if (!a.x_early) {  // X may still be being written: its boxes follow the wait
+        ptx::griddep_wait();
+        issue(warp, false, true);
+      }
+    } else {
+      if (!a.x_early) ptx::griddep_wait();
+      xa_issue<NT>(a, xa_base, ptx::smem_u32(&xa_bar), 0);
     }
-    if (xa_cta) xa_issue<NT>(a, xa_base, ptx::smem_u32(&xa_bar), 0);
   }
   {
     // entry e (a packed byte), lane l: bf16 pair (q[e >> 4], q[e & 15]); the
