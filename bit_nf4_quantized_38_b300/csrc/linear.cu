@@ -30,8 +30,12 @@ bool rank_ok(int r) { return r == 8 || r == 16 || r == 32 || r == 64 || r == 128
 bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 // forward workspace: XAs [M][r] bf16; backward: Gs [M][r] + recomputed XA [M][r]
-size_t fwd_ws(int64_t M, int r) { return up256((size_t)M * r * 2); }
-size_t bwd_ws(int64_t M, int r) { return 2 * up256((size_t)M * r * 2); }
+// Training workspaces have two halves; successive calls on a stream alternate
+// between them (see next_ws_half).
+size_t fwd_half(int64_t M, int r) { return up256((size_t)M * r * 2); }      // s XA, bf16 [M][r]
+size_t bwd_half(int64_t M, int r) { return 2 * up256((size_t)M * r * 2); }  // s G, XA: bf16 [M][r] each
+size_t fwd_ws(int64_t M, int r) { return 2 * fwd_half(M, r); }
+size_t bwd_ws(int64_t M, int r) { return 2 * bwd_half(M, r); }
 
 int check_common(const LinearArgs &a, const char *fn, size_t need) {
   if (a.M <= 0) return set_error(QL_ERR_INVALID, "%s: M = %lld", fn, (long long)a.M);
@@ -118,9 +122,9 @@ void note_call(cudaStream_t st, bool linear, std::vector<Range> writes, std::vec
   pc.reads = std::move(reads);
 }
 
-// Decode calls on a stream alternate between the two halves of their
+// Linear calls on a stream alternate between the two halves of their
 // workspace, so a call never writes the half its predecessor may still use.
-int next_decode_half(cudaStream_t st) {
+int next_ws_half(cudaStream_t st) {
   std::lock_guard<std::mutex> lock(g_prev_mu);
   PrevCall &pc = g_prev[st];
   pc.decode_half ^= 1;
@@ -166,7 +170,7 @@ int linear_fwd(const LinearArgs &a) {
     DecodeProblem d{};
     d.X = a.X; d.M = M; d.K = K; d.N = N; d.w = nf4_view(a.W); d.A = a.A; d.B = a.B; d.r = r;
     d.scale = a.scale; d.Y = a.Y; d.XA_out = a.XA; d.ws = a.ws;
-    d.half = next_decode_half(a.stream);
+    d.half = next_ws_half(a.stream);
     std::vector<Range> reads;
     weight_ranges(a.W, reads);
     d.w_early = reads_clear_of_previous(a.stream, reads);
@@ -184,22 +188,28 @@ int linear_fwd(const LinearArgs &a) {
     return launch_decode(d, a.stream);
   }
   QL_TRY(check_common(a, fn, fwd_ws(M, r)));
-  uint16_t *xas = static_cast<uint16_t *>(a.ws);
   cudaStream_t st = a.stream;
+  const size_t half = fwd_half(M, r);
+  char *wsh = static_cast<char *>(a.ws) + (next_ws_half(st) ? half : 0);
+  uint16_t *xas = reinterpret_cast<uint16_t *>(wsh);
 
-  std::vector<Range> reads = {range(a.X, (size_t)(M * K * 2)), range(a.A, (size_t)(K * r * 2)),
-                             range(a.B, (size_t)(r * N * 2))};
+  const std::vector<Range> xa_reads = {range(a.X, (size_t)(M * K * 2)), range(a.A, (size_t)(K * r * 2))};
+  std::vector<Range> xa_writes = {range(wsh, half)};
+  if (a.XA) xa_writes.push_back(range(a.XA, (size_t)(M * r * 2)));
+  std::vector<Range> reads = xa_reads;
+  reads.push_back(range(a.B, (size_t)(r * N * 2)));
   weight_ranges(a.W, reads);
   const bool early = reads_clear_of_previous(st, reads);
-  std::vector<Range> writes = {range(a.Y, (size_t)(M * N * 2)), range(a.ws, a.ws_bytes)};
-  if (a.XA) writes.push_back(range(a.XA, (size_t)(M * r * 2)));
+  const bool free_ = reads_clear_of_previous(st, xa_reads) && writes_clear_of_previous(st, xa_writes);
+  std::vector<Range> writes = xa_writes;
+  writes.push_back(range(a.Y, (size_t)(M * N * 2)));
   note_call(st, true, std::move(writes), reads);
 
   LoraProblem L{};
   L.A = a.X; L.a_mn = false; L.B = a.A; L.b_mn = true;  // X [M][K], A [K][r]
   L.P = M; L.Q = r; L.T = K; L.mode = 0; L.scale = a.scale;
   L.out = xas; L.ldo = r; L.out2 = a.XA; L.ldo2 = r;
-  L.dep = early ? kDepStores : kDepStart;
+  L.dep = free_ ? kDepFree : (early ? kDepStores : kDepStart);
   QL_TRY(launch_lora(L, st));
   GemmProblem g{};
   g.trans = false;
@@ -220,19 +230,23 @@ int linear_bwd(const LinearArgs &a) {
   const int64_t M = a.M, N = a.W.rows, K = a.W.cols;
   const int r = a.r;
   QL_TRY(check_common(a, fn, bwd_ws(M, r)));
-  char *ws = static_cast<char *>(a.ws);
+  cudaStream_t st = a.stream;
+  const size_t half = bwd_half(M, r);
+  char *ws = static_cast<char *>(a.ws) + (next_ws_half(st) ? half : 0);
   uint16_t *gs = reinterpret_cast<uint16_t *>(ws);
   uint16_t *xa_tmp = reinterpret_cast<uint16_t *>(ws + up256((size_t)M * r * 2));
-  cudaStream_t st = a.stream;
 
   std::vector<Range> reads = {range(a.dY, (size_t)(M * N * 2)), range(a.X, (size_t)(M * K * 2)),
                              range(a.A, (size_t)(K * r * 2)), range(a.B, (size_t)(r * N * 2))};
   if (a.XA_in) reads.push_back(range(a.XA_in, (size_t)(M * r * 2)));
   weight_ranges(a.W, reads);
   const bool early = reads_clear_of_previous(st, reads);
+  // the first kernel (XA recompute or G) may also store alongside the previous
+  // call: it reads only inputs and writes only this call's workspace half
+  const bool free_ = early && writes_clear_of_previous(st, {range(ws, half)});
   note_call(st, true,
             {range(a.dX, (size_t)(M * K * 2)), range(a.dA, (size_t)(K * r * 4)), range(a.dB, (size_t)(r * N * 4)),
-             range(a.ws, a.ws_bytes)},
+             range(ws, half)},
             reads);
 
   const uint16_t *xa = a.XA_in;
@@ -240,7 +254,7 @@ int linear_bwd(const LinearArgs &a) {
     LoraProblem L{};
     L.A = a.X; L.a_mn = false; L.B = a.A; L.b_mn = true;
     L.P = M; L.Q = r; L.T = K; L.mode = 0; L.scale = 1.0f; L.out = xa_tmp; L.ldo = r;
-    L.dep = early ? kDepStores : kDepStart;
+    L.dep = free_ ? kDepFree : (early ? kDepStores : kDepStart);
     QL_TRY(launch_lora(L, st));
     xa = xa_tmp;
   }
@@ -248,8 +262,9 @@ int linear_bwd(const LinearArgs &a) {
     LoraProblem L{};
     L.A = a.dY; L.a_mn = false; L.B = a.B; L.b_mn = false;
     L.P = M; L.Q = r; L.T = N; L.mode = 0; L.scale = a.scale; L.out = gs; L.ldo = r;
-    // first kernel of the call, or reading only inputs after the recompute above
-    L.dep = (early && !a.XA_in) ? kDepStart : (early ? kDepStores : kDepStart);
+    // first kernel of the call, or reading only inputs after the recompute
+    // above (which completes only after the previous call)
+    L.dep = free_ ? kDepFree : (early && a.XA_in ? kDepStores : kDepStart);
     QL_TRY(launch_lora(L, st));
   }
   {  // 2. dX = dY W_hat + Gs A^T

@@ -101,7 +101,8 @@ k_lora_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
   const uint32_t tmem = *tmem_slot;
   // Launched as a programmatic dependent; where it waits for the previous
   // kernel depends on a.dep (see LoraProblem).  Dependents are let in only
-  // once this kernel has waited, except after kDepExit.
+  // once this kernel has waited, except after kDepExit and kDepFree (whose
+  // dependent waits for this grid to complete before touching anything).
   if (a.dep == kDepStart) ptx::griddep_wait();
   if (a.dep != kDepStores) ptx::griddep_launch();
 
@@ -228,7 +229,8 @@ k_lora_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
   // keep this CTA's tile alive until every CTA of the cluster has read it
   ptx::cluster_sync();
   if (warp == 1) ptx::tmem_dealloc(tmem, NQ);
-  if (a.dep == kDepExit) ptx::griddep_wait();
+  if (a.dep == kDepExit || (a.dep == kDepFree && blockIdx.x == gridDim.x - 1 && threadIdx.x == 0))
+    ptx::griddep_wait();
 }
 
 template <bool A_MN, bool B_MN, int NQ>

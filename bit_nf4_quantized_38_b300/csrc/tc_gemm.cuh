@@ -71,10 +71,14 @@ struct LoraProblem {
   //              and compute alongside it, wait for it before the first store;
   //   kDepExit   the inputs were complete before it let this kernel start and
   //              this kernel writes nothing it reads: run alongside it, wait
-  //              only before exiting (so completion still implies its completion).
+  //              only before exiting (so completion still implies its completion);
+  //   kDepFree   no kernel still running writes what this kernel reads, or
+  //              reads or writes what it writes: run and store alongside it;
+  //              one CTA waits for it before exiting, so that this grid still
+  //              completes after it (the other CTAs leave their SMs at once).
   int dep = 0;
 };
-constexpr int kDepStart = 0, kDepStores = 1, kDepExit = 2;
+constexpr int kDepStart = 0, kDepStores = 1, kDepExit = 2, kDepFree = 3;
 int launch_lora(const LoraProblem &L, cudaStream_t st);
 // L0 and L1 in one launch when their operand layouts and width class agree
 // (else two launches); both must be independent of each other.
