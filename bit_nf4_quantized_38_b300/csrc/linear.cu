@@ -240,10 +240,14 @@ int linear_bwd(const LinearArgs &a) {
                              range(a.A, (size_t)(K * r * 2)), range(a.B, (size_t)(r * N * 2))};
   if (a.XA_in) reads.push_back(range(a.XA_in, (size_t)(M * r * 2)));
   weight_ranges(a.W, reads);
-  const bool early = reads_clear_of_previous(st, reads);
-  // the first kernel (XA recompute or G) may also store alongside the previous
-  // call: it reads only inputs and writes only this call's workspace half
-  const bool free_ = early && writes_clear_of_previous(st, {range(ws, half)});
+  // The first kernel (the XA recompute, or G) and G read only inputs (X and
+  // A; dY and B) and write only this call's workspace half: when those are
+  // clear of the previous call they read, compute and store alongside it.
+  const std::vector<Range> x_a = {range(a.X, (size_t)(M * K * 2)), range(a.A, (size_t)(K * r * 2))};
+  const std::vector<Range> dy_b = {range(a.dY, (size_t)(M * N * 2)), range(a.B, (size_t)(r * N * 2))};
+  const bool half_clear = writes_clear_of_previous(st, {range(ws, half)});
+  const bool g_early = reads_clear_of_previous(st, dy_b);
+  const bool x_early = reads_clear_of_previous(st, x_a);
   note_call(st, true,
             {range(a.dX, (size_t)(M * K * 2)), range(a.dA, (size_t)(K * r * 4)), range(a.dB, (size_t)(r * N * 4)),
              range(ws, half)},
@@ -254,7 +258,7 @@ int linear_bwd(const LinearArgs &a) {
     LoraProblem L{};
     L.A = a.X; L.a_mn = false; L.B = a.A; L.b_mn = true;
     L.P = M; L.Q = r; L.T = K; L.mode = 0; L.scale = 1.0f; L.out = xa_tmp; L.ldo = r;
-    L.dep = free_ ? kDepFree : (early ? kDepStores : kDepStart);
+    L.dep = (x_early && half_clear) ? kDepFree : (x_early ? kDepStores : kDepStart);
     QL_TRY(launch_lora(L, st));
     xa = xa_tmp;
   }
@@ -262,9 +266,11 @@ int linear_bwd(const LinearArgs &a) {
     LoraProblem L{};
     L.A = a.dY; L.a_mn = false; L.B = a.B; L.b_mn = false;
     L.P = M; L.Q = r; L.T = N; L.mode = 0; L.scale = a.scale; L.out = gs; L.ldo = r;
-    // first kernel of the call, or reading only inputs after the recompute
-    // above (which completes only after the previous call)
-    L.dep = free_ ? kDepFree : (early && a.XA_in ? kDepStores : kDepStart);
+    // the first kernel of the call, or the second after the recompute above
+    // (which writes nothing G touches)
+    L.dep = (g_early && half_clear && (a.XA_in || x_early)) ? kDepFree
+            : (g_early && a.XA_in)                          ? kDepStores
+                                                            : kDepStart;
     QL_TRY(launch_lora(L, st));
   }
   {  // 2. dX = dY W_hat + Gs A^T

@@ -229,7 +229,9 @@ k_lora_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
   // keep this CTA's tile alive until every CTA of the cluster has read it
   ptx::cluster_sync();
   if (warp == 1) ptx::tmem_dealloc(tmem, NQ);
-  if (a.dep == kDepExit || (a.dep == kDepFree && blockIdx.x == gridDim.x - 1 && threadIdx.x == 0))
+  // kDepExit and kDepFree: one CTA waits for the previous grid before exiting,
+  // so this grid completes after it; the others leave their SMs at once
+  if ((a.dep == kDepExit || a.dep == kDepFree) && blockIdx.x == gridDim.x - 1 && threadIdx.x == 0)
     ptx::griddep_wait();
 }
 

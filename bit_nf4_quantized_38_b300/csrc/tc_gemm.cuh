@@ -70,8 +70,9 @@ struct LoraProblem {
   //   kDepStores the inputs are not written by any kernel still running: read
   //              and compute alongside it, wait for it before the first store;
   //   kDepExit   the inputs were complete before it let this kernel start and
-  //              this kernel writes nothing it reads: run alongside it, wait
-  //              only before exiting (so completion still implies its completion);
+  //              this kernel writes nothing it reads: run alongside it; one CTA
+  //              waits for it before exiting (so completion still implies its
+  //              completion);
   //   kDepFree   no kernel still running writes what this kernel reads, or
   //              reads or writes what it writes: run and store alongside it;
   //              one CTA waits for it before exiting, so that this grid still
