@@ -110,7 +110,7 @@ k_quantize(const uint4 *__restrict__ W, int64_t n_blocks, Codebook cb, uint2 *__
         const float r = __frcp_rn(m);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint32_t o = 0;
+          uint32_t code[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float x = quotient(w[8 * h + e], m, r);
@@ -120,10 +120,14 @@ k_quantize(const uint4 *__restrict__ W, int64_t n_blocks, Codebook cb, uint2 *__
             asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
                          : "=r"(t.x), "=r"(t.y)
                          : "r"(tbase + prmt(cu, lane8, 0x5504u)));
-            const uint32_t code = t.y + (x >= __uint_as_float(t.x) ? 1u : 0u);
-            // element 2j -> high nibble of byte j
-            o |= code << (8 * (e >> 1) + ((e & 1) ? 0 : 4));
+            code[e] = t.y + (x >= __uint_as_float(t.x) ? 1u : 0u);
           }
+          // element 2j -> high nibble of byte j: each byte as 16 hi + lo, the
+          // bytes placed by multiply-adds (the fields never overlap)
+          uint32_t o = code[0] * 16u + code[1];
+          o = (code[2] * 16u + code[3]) * 0x100u + o;
+          o = (code[4] * 16u + code[5]) * 0x10000u + o;
+          o = (code[6] * 16u + code[7]) * 0x1000000u + o;
           out[h] = o;
         }
       } else if (m > 0.0f) {  // constants outside [2^-60, 2^60]: IEEE division
