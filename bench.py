@@ -267,6 +267,30 @@ def cpu_baseline(repeats=3):
             "details": cpu_oracle_details(s)}
 
 
+# ----------------------------------------------------------------------------- ranks (N > 1: replicas)
+
+def rank_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks_of(x, world, device):
+    """The largest of the ranks' values of x (each rank passes its own)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, flops_per_rank_step, ms_per_step):
+    """Whole-job rate: every rank does the same step (weak scaling), timed by the slowest."""
+    return world * flops_per_rank_step / (ms_per_step / 1e3) / 1e12
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -547,15 +571,10 @@ def main():
     flops_step = sum(4 * c.M * c.N * c.K + 6 * c.M * c.r * (c.N + c.K) for c in wl.cases)
 
     def barrier():
-        if world > 1:
-            dist.barrier()
+        rank_barrier(world)
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks_of(x, world, dev)
 
     for _ in range(args.warmup):
         step()
@@ -594,7 +613,7 @@ def main():
     clocks = sampler.summary(t_wall0, t_wall1)
 
     ms_step = ms_total / args.steps
-    value = world * flops_step / (ms_step / 1e3) / 1e12
+    value = job_tflops(world, flops_step, ms_step)
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -617,7 +636,7 @@ def main():
         e_ms = max_over_ranks(e0.elapsed_time(e1)) / args.steps
         h2d = sum(2 * c.M * (c.K + c.N) for c in wl.cases)
         d2h = sum(4 * c.r * (c.K + c.N) for c in wl.cases)
-        e2e = {"value": world * flops_step / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
+        e2e = {"value": job_tflops(world, flops_step, e_ms), "unit": "TFLOP/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "note": "per step: X and dY of all 7 linears copied from pinned host memory on a copy "
                        "stream running ahead of the compute, dA and dB read back on a second copy "
