@@ -324,12 +324,17 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     if (tid == 0) xa_chunks = n;
   }
 
-  // ---- warp w owns rows 16 w .. 16 w + 15 of the unit's row group
+  // ---- warp w owns rows 16 w .. 16 w + 15 of the unit's row group.  MMA
+  // fragment row g (and g + 8) is weight row pg = 2 (g mod 4) + g / 4 (and
+  // pg + 8) of the warp's 16: the 8-byte loads of one 16-lane phase then read
+  // rows 0, 2, 4, 6 (or 1, 3, 5, 7), whose two 16-byte chunks land in eight
+  // distinct positions under the 128-byte swizzle, so they never conflict.
   const int g = lane >> 2, t = lane & 3;
+  const int pg = ((g & 3) << 1) | (g >> 2);
   const uint32_t lanebase = (uint32_t)lane * 4u;
   const float mu = a.dq ? __ldg(a.mean) : 0.0f;
 
-  // block constants of block t of a unit for the lane's 2 rows (16 w + 8 k + g),
+  // block constants of block t of a unit for the lane's 2 rows (16 w + 8 k + pg),
   // loaded PD units ahead
   struct Pre {
     float a[2], b[2];
@@ -345,7 +350,7 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     if (i >= nu || kb >= nb_row) return p;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const int row = rg * UNIT_ROWS + warp * 16 + 8 * k + g;
+      const int row = rg * UNIT_ROWS + warp * 16 + 8 * k + pg;
       if (row < a.N) {
         const int bi = row * nb_row + kb;
         if (a.dq) {
@@ -376,7 +381,7 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
       waited = true;
     }
     float *slot = a.slots + (int64_t)(rg + c) * SLOT_FLOATS;
-    const int rl = warp * 16 + g;
+    const int rl = warp * 16 + pg;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       __stcg(reinterpret_cast<float2 *>(slot + rl * 16 + mt * 8 + 2 * t), make_float2(acc[mt][0], acc[mt][1]));
@@ -426,8 +431,8 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         const float m1 = __shfl_sync(0xffffffffu, mh[1], (g << 2) | blk);
         // packed bytes of block blk, lane t: chunk 2 blk + t/2 of the row, at
         // position chunk ^ (row mod 8) (128-byte swizzle), 8 bytes
-        const uint32_t coff = ((uint32_t)((2 * blk + (t >> 1)) ^ g) << 4) + (uint32_t)(t & 1) * 8u;
-        const uint32_t r0 = wsb + (uint32_t)(warp * 16 + g) * 128u + coff;
+        const uint32_t coff = ((uint32_t)((2 * blk + (t >> 1)) ^ pg) << 4) + (uint32_t)(t & 1) * 8u;
+        const uint32_t r0 = wsb + (uint32_t)(warp * 16 + pg) * 128u + coff;
         const uint2 wg = lds64(r0), wg8 = lds64(r0 + 8 * 128);
         float D[MT][4];
 #pragma unroll
