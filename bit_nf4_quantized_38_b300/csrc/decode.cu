@@ -496,6 +496,7 @@ struct FinArgs {
   int nbox, W, G;       // the weight stream's unit split
   int nx;               // partial XA tiles
   int x_early;          // B may be read before the stream kernel completes
+  int launch_early;     // the stream kernel fills every SM (see k_decode_finish)
   const float *xap;     // [nx][16][R]
   const float *slots;   // the stream's partial tiles
   const uint16_t *B;    // [R][N]
@@ -574,8 +575,16 @@ k_decode_finish(const __grid_constant__ FinArgs a) {
   const int rowc = blockIdx.x * FIN_ROWS + warp * 32;  // this warp's first row
   uint32_t af0[KSC][4];
   if (a.x_early) load_bfrag<NT>(a, rowc, 0, af0);
+  // The next call may start once this kernel has waited for the stream kernel
+  // (and so for every grid before it).  When the stream kernel has a CTA on
+  // every SM it may start at once instead: its CTAs (too large to share an SM
+  // with a stream CTA) then take each SM only when this call's stream CTA on
+  // it exits, which that CTA does only after the call before this one has
+  // completed; so whatever the next call starts with still sees every call
+  // before this one complete, as it would otherwise.
+  if (a.launch_early) ptx::griddep_launch();
   ptx::griddep_wait();  // the stream kernel, and every grid before it, completed
-  ptx::griddep_launch();
+  if (!a.launch_early) ptx::griddep_launch();
   if (!a.x_early) load_bfrag<NT>(a, rowc, 0, af0);
   {
     // XA = the partial tiles added in tile order, in two steps: thread t adds
@@ -858,6 +867,7 @@ int launch_decode(const DecodeProblem &p, cudaStream_t st) {
   FinArgs f{};
   f.M = a.M; f.N = a.N; f.nbox = a.nbox; f.W = a.W; f.G = G;
   f.x_early = a.x_early;
+  f.launch_early = G == di.sms;
   f.xap = a.xap; f.slots = a.slots;
   f.B = p.B; f.scale = p.scale; f.Y = p.Y; f.XA_out = p.XA_out;
   const bool mt2 = p.M > 8;
