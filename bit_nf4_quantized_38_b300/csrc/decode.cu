@@ -276,10 +276,11 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
       for (int j = 0; j < 4; ++j) ptx::tma_load_2d(dst + W_BYTES + j * XR * 128, &tmX, fb, b * UNIT_K + 64 * j, 0);
   };
 
-  // Setup.  Once the barriers exist, one lane of each of warps 0..2 issues
-  // the copies of one of the first three units (weight box, and X when X may
-  // be read early) and one lane of warp 3 the first XA chunk, while the other
-  // threads build the lookup table.
+  // Setup.  Once the barriers exist, one lane of warp 0 issues the copies of
+  // unit 0 (weight box, and X when X may be read early) and one lane of warp
+  // 3 the first XA chunk; units 1 and 2 follow once the lookup table is built,
+  // so that unit 0 is not shared out with them in the burst of every CTA's
+  // first loads and computing can start sooner.
   if (tid == 0) {
     for (int s = 0; s < ST_STAGES; ++s) {
       ptx::mbar_init(ptx::smem_u32(&full_bar[s]), 1);
@@ -292,20 +293,22 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     xa_chunks = 0;
   }
   __syncthreads();
-  if (lane == 0 && (warp < npre || (warp == ST_STAGES && xa_cta))) {
+  auto issue_first = [&](int i) {
     if (!a.w_early) ptx::griddep_wait();
-    if (warp < npre) {
-      ptx::prefetch_tmap(&tmW);
-      ptx::prefetch_tmap(&tmX);
-      issue(warp, true, a.x_early);
-      if (!a.x_early) {  // X may still be being written: its boxes follow the wait
-        ptx::griddep_wait();
-        issue(warp, false, true);
-      }
-    } else {
-      if (!a.x_early) ptx::griddep_wait();
-      xa_issue<NT>(a, xa_base, ptx::smem_u32(&xa_bar), 0);
+    issue(i, true, a.x_early);
+    if (!a.x_early) {  // X may still be being written: its boxes follow the wait
+      ptx::griddep_wait();
+      issue(i, false, true);
     }
+  };
+  if (lane == 0 && warp == 0) {
+    ptx::prefetch_tmap(&tmW);
+    ptx::prefetch_tmap(&tmX);
+    issue_first(0);
+  }
+  if (lane == 0 && warp == ST_STAGES && xa_cta) {
+    if (!a.x_early) ptx::griddep_wait();
+    xa_issue<NT>(a, xa_base, ptx::smem_u32(&xa_bar), 0);
   }
   {
     // entry e (a packed byte), lane l: bf16 pair (q[e >> 4], q[e & 15]); the
@@ -316,6 +319,7 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
       tp[(i >> 3) * 16 + (i & 7)] = make_uint4(v, v, v, v);
     }
   }
+  if (lane == 0 && warp >= 1 && warp < npre) issue_first(warp);
   __syncthreads();
   if (!a.w_early) ptx::griddep_wait();
 
