@@ -335,6 +335,11 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
   // distinct positions under the 128-byte swizzle, so they never conflict.
   const int g = lane >> 2, t = lane & 3;
   const int pg = ((g & 3) << 1) | (g >> 2);
+  // Token row of the X fragments: with one token tile, fragment column g >= M
+  // reads token g mod M instead of a zero row, so lanes share addresses and a
+  // 16-byte load of X takes one shared-memory wavefront (M <= 2) or two
+  // (M <= 4) instead of four; the products in those columns are ignored.
+  const int xg = MT == 1 ? g % a.M : g;
   const uint32_t lanebase = (uint32_t)lane * 4u;
   const float mu = a.dq ? __ldg(a.mean) : 0.0f;
 
@@ -420,14 +425,14 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
 #pragma unroll
       for (int blk = 0; blk < 4; ++blk) {
         if (b * 4 + blk >= nb_row) break;
-        // X fragments of block blk: token rows 8 mt + g, K values 16 t .. 16 t + 15
+        // X fragments of block blk: token rows 8 mt + xg, K values 16 t .. 16 t + 15
         // (16-byte chunks 2t, 2t+1 of the 128-byte row, swizzled by row mod 8)
         uint32_t xw[MT][8];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          const uint32_t rowa = xsb + (uint32_t)(blk * XR * 128 + (mt * 8 + g) * 128);
-          const uint4 x0 = lds128(rowa + ((uint32_t)((2 * t) ^ g) << 4));
-          const uint4 x1 = lds128(rowa + ((uint32_t)((2 * t + 1) ^ g) << 4));
+          const uint32_t rowa = xsb + (uint32_t)(blk * XR * 128 + (mt * 8 + xg) * 128);
+          const uint4 x0 = lds128(rowa + ((uint32_t)((2 * t) ^ xg) << 4));
+          const uint4 x1 = lds128(rowa + ((uint32_t)((2 * t + 1) ^ xg) << 4));
           xw[mt][0] = x0.x; xw[mt][1] = x0.y; xw[mt][2] = x0.z; xw[mt][3] = x0.w;
           xw[mt][4] = x1.x; xw[mt][5] = x1.y; xw[mt][6] = x1.z; xw[mt][7] = x1.w;
         }
