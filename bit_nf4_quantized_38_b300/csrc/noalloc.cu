@@ -1,8 +1,8 @@
 // nf4_quantize without a caller-provided workspace.
 //
 // Some callers cannot hand the library a scratch buffer: code that runs
-// where device allocation is not allowed or not wanted -- inside a region
-// being captured into a CUDA graph, under a memory planner that fixed every
+// where device allocation is not allowed or not wanted -- inside a host
+// runtime that owns every allocation, under a memory planner that fixed every
 // buffer up front, or on a latency-critical path where cudaMalloc's implicit
 // device synchronisation is unacceptable -- and thin C callers that have no
 // allocator of their own.  For them the quantizer's scratch (an fp64 sum and

@@ -128,10 +128,11 @@ QL_API int nf4_quantize(const uint16_t *W, const ql_nf4_tensor *q, void *ws,
 
 /*
  * nf4_quantize for callers that cannot pass a workspace (no counterpart in the
- * paper: an interface convenience of this library).  Callers inside a region
- * being captured into a CUDA graph, callers whose memory was all planned up
- * front, and callers that must not trigger cudaMalloc's implicit device
- * synchronisation cannot allocate scratch per call; this entry point uses a
+ * paper: an interface convenience of this library).  Callers whose device
+ * memory is all planned up front, callers embedded in a host runtime that owns
+ * every allocation and hands them no allocator, and callers that must not
+ * trigger cudaMalloc's implicit device synchronisation cannot allocate
+ * scratch per call; this entry point uses a
  * fixed scratch array built into the library instead (about 16 MB per GPU that
  * loads the library, held until the process exits).  It allocates nothing.
  *   W, q, stream : as for nf4_quantize.

@@ -1,8 +1,8 @@
 """The allocation-free quantize entry point (nf4_quantize_noalloc).
 
 It exists for callers that cannot allocate scratch memory per call -- code
-inside a region captured into a CUDA graph, code under a memory plan fixed up
-front, code that must avoid cudaMalloc's implicit synchronisation.  It must
+under a memory plan fixed up front, code embedded in a host runtime that owns
+every allocation, code that must avoid cudaMalloc's implicit synchronisation.  It must
 give exactly what nf4_quantize gives with a caller-provided workspace, call
 after call, since every call reuses the same built-in scratch array.  This
 file is collected last so that a run stopping at its first failure has run
