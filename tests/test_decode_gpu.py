@@ -53,6 +53,8 @@ def reference(W, X, A, B, s, dq=256):
 @pytest.mark.parametrize("N,K,M,r", [
     (1024, 1024, 1, 8), (1032, 576, 3, 8), (1032, 576, 9, 128), (520, 4160, 16, 32), (64, 64, 16, 16),
     (4096, 128, 7, 64), (256, 8192, 12, 64), (1536, 2048, 2, 16), (776, 1088, 5, 64), (512, 768, 8, 8),
+    # K long enough that each XA CTA stages its slice of A in several chunks
+    (256, 19968, 3, 64), (256, 20032, 1, 64), (512, 10240, 16, 128), (512, 40960, 4, 64),
 ])
 def test_decode_ragged_shapes(ql, N, K, M, r):
     from bit_nf4_quantized_38_b300.workloads import normal_bf16, normal_with_outliers_bf16
