@@ -84,6 +84,8 @@ SHAPES = [
     (264, 192, 129, 128),   # rank 128: two LoRA K-steps
     (328, 320, 600, 16),    # CTA-pair tiles, ragged
     (1032, 576, 1100, 32),  # CTA-pair tiles, partial pair in N and M
+    (520, 448, 300, 8),     # rank 8 on the tensor-core forward path
+    (264, 640, 17, 64),     # one token past the decode path's limit
 ]
 
 
