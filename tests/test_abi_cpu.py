@@ -71,6 +71,75 @@ def test_quantize_rejects_bad_arguments_on_host(ql):
     assert lib.nf4_quantize(buf, None, buf, 1 << 20, None) == ql.QL_ERR_INVALID
 
 
+def _fake_pointers_only_without_gpu():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("passes fake device pointers: host-side checks, run where there is no GPU")
+
+
+def test_linear_calls_reject_bad_arguments_on_host(ql):
+    """Every case fails the host-side checks, so no CUDA call is made."""
+    _fake_pointers_only_without_gpu()
+    lib, E = ql.lib, ql
+    p, odd, ws_odd = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x10002), ctypes.c_void_p(0x10010)
+    big = 1 << 40
+
+    def W(rows=256, cols=512, dq=256):
+        return ql.NF4Struct(rows, cols, 64, dq, p, None if dq else p, p, p, p)
+
+    def fwd(X=p, M=64, w=None, A=p, B=p, r=16, Y=p, XA=None, ws=p, wsb=big):
+        w = w or W()
+        return lib.qlora_linear_fwd(X, M, ctypes.byref(w), A, B, r, 1.0, Y, XA, ws, wsb, None)
+
+    def bwd(dY=p, X=p, XA=None, M=64, w=None, A=p, B=p, r=16, dX=p, dA=p, dB=p, ws=p, wsb=big):
+        w = w or W()
+        return lib.qlora_linear_bwd(dY, X, XA, M, ctypes.byref(w), A, B, r, 1.0, dX, dA, dB, ws, wsb, None)
+
+    for M in (64, 4):  # the tensor-core path and the decode path
+        assert fwd(X=None, M=M) == E.QL_ERR_INVALID
+        assert fwd(Y=None, M=M) == E.QL_ERR_INVALID
+        assert fwd(A=odd, M=M) == E.QL_ERR_MISALIGNED
+        assert fwd(XA=odd, M=M) == E.QL_ERR_MISALIGNED
+        assert fwd(r=12, M=M) == E.QL_ERR_UNSUPPORTED
+        assert "rank 12" in lib.ql_last_error().decode()
+        assert fwd(w=W(rows=100), M=M) == E.QL_ERR_UNSUPPORTED
+        assert "multiple of 8" in lib.ql_last_error().decode()
+        assert fwd(w=W(cols=100), M=M) == E.QL_ERR_UNSUPPORTED
+        assert fwd(w=W(dq=128), M=M) == E.QL_ERR_UNSUPPORTED
+        assert fwd(ws=None, M=M) == E.QL_ERR_INVALID
+        assert fwd(ws=ws_odd, M=M) == E.QL_ERR_MISALIGNED
+        need = ql.workspace_size(ql.OP_LINEAR_FWD, M, 256, 512, 16)
+        assert need > 0 and fwd(wsb=need - 1, M=M) == E.QL_ERR_UNSUPPORTED
+    assert fwd(M=0) == E.QL_ERR_INVALID
+    assert fwd(M=-3) == E.QL_ERR_INVALID
+    assert lib.qlora_linear_fwd(p, 64, None, p, p, 16, 1.0, p, None, p, big, None) == E.QL_ERR_INVALID
+
+    assert bwd(dA=None) == E.QL_ERR_INVALID
+    assert bwd(dX=odd) == E.QL_ERR_MISALIGNED
+    assert bwd(XA=odd) == E.QL_ERR_MISALIGNED
+    assert bwd(r=0) == E.QL_ERR_UNSUPPORTED
+    assert bwd(M=0) == E.QL_ERR_INVALID
+    assert bwd(w=W(rows=0)) == E.QL_ERR_INVALID
+    need = ql.workspace_size(ql.OP_LINEAR_BWD, 64, 256, 512, 16)
+    assert need > 0 and bwd(wsb=need - 1) == E.QL_ERR_UNSUPPORTED
+
+
+def test_dequantize_and_noalloc_reject_bad_arguments_on_host(ql):
+    _fake_pointers_only_without_gpu()
+    lib, E = ql.lib, ql
+    p, odd = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x10002)
+    s = ql.NF4Struct(256, 512, 64, 256, p, None, p, p, p)
+    assert lib.nf4_dequantize(ctypes.byref(s), None, None) == E.QL_ERR_INVALID
+    assert lib.nf4_dequantize(ctypes.byref(s), odd, None) == E.QL_ERR_MISALIGNED
+    s_bad = ql.NF4Struct(256, 512, 64, 256, p, None, None, p, p)
+    assert lib.nf4_dequantize(ctypes.byref(s_bad), p, None) == E.QL_ERR_INVALID
+    # the built-in scratch holds 4 Mi blocks of 64: one block more is refused
+    too_big = ql.NF4Struct((1 << 22) // 64 + 1, 64 * 64, 64, 256, p, None, p, p, p)
+    assert lib.nf4_quantize_noalloc(p, ctypes.byref(too_big), None) == E.QL_ERR_UNSUPPORTED
+    assert "scratch" in lib.ql_last_error().decode()
+    assert lib.nf4_quantize_noalloc(p, None, None) == E.QL_ERR_INVALID
+
+
 def test_selftest_wait_rejects_bad_limits_on_host(ql):
     for limit in (0, -5, 2_000_000_001):
         assert ql.lib.ql_selftest_wait(limit, None) == ql.QL_ERR_INVALID
