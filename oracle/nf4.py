@@ -10,7 +10,7 @@ What the pages fix:
     parameter, about 3 GB for a 65B model (news write-up, "Double
     Quantization" item; Finnish summary, item (2)).
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   R1 Codebook.  "Quantiles of N(0,1) normalised to [-1, 1] with an exact zero":
      16 levels with both endpoints and an exact zero cannot be symmetric, so
      the positive side gets 8 levels and the negative side 7.  The positive
