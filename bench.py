@@ -2,22 +2,31 @@
 """Benchmark of the QLoRA linear hot path on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload llama33b|llama7b]
 
-Workload (one step): the 7 LLaMA-7B linears (q/k/v/o 4096x4096, gate/up
-11008x4096, down 4096x11008) with NF4 + double-quant weights and a rank-64
-LoRA adapter (alpha 16) on all 7, M = 4 x 1024 = 4096 tokens: the forward of
-all 7 in order, then the backward of all 7 in reverse order, through the
-library's C ABI.  Inputs are seeded synthetic bf16 data shaped like the
-pages' LLaMA workloads (weights N(0, 0.02^2) with 0.1% outliers x20,
-activations N(0, 1)); the weights are quantized once before timing, as in
-QLoRA finetuning where the frozen 4-bit weights are stored once.
+Workload (one step, the default): the LLaMA-33B-shaped stack, 60 layers x 7
+QLoRA linears (q/k/v/o 6656x6656, gate/up 17920x6656, down 6656x17920) with
+NF4 + double-quant weights (16.6 GB, all resident) and a rank-64 LoRA adapter
+(alpha 16) on every linear, M = 2048 tokens: the forward of all 420 linears
+in order, then the backward of all 420 in reverse order, through the
+library's C ABI.  Every linear has its own seeded synthetic X and dY (bf16,
+N(0, 1)); weights are N(0, 0.015^2) bf16 drawn on the device and quantized
+once before timing, as in QLoRA finetuning where the frozen 4-bit weights are
+stored once.  `--workload llama7b` times the 7 LLaMA-7B linears at M = 4096
+instead (also reported as a sub-result of the default run).
 
 The metric is algorithmic TFLOP/s: 4MNK + 6Mr(N+K) per linear per step.
 One JSON line is printed by rank 0.  Extra keys: `roofline` of the dominant
-kernel (the tensor-core dequant GEMM), `cpu_baseline` (the CPU oracle on a
-bounded sample), `e2e` (the same metric with host buffers and host<->device
-copies inside the timed region), `clocks`, `gpu_launches`, and sub-results
-for the decode GEMV and the quantizer.
+kernel (the tensor-core dequant GEMM, timed inside the timed steps by its own
+first-CTA-start / last-CTA-end %globaltimer stamps), `cpu_baseline` (the CPU
+oracle on a bounded sample), `e2e` (the same metric with host buffers and
+host<->device copies inside the timed region), `clocks`, `gpu_launches`, and
+sub-results for the LLaMA-7B linears, the decode GEMV and the quantizer.
+
+With N > 1 ranks (torchrun) the run is data parallel: every rank holds the
+same weights and processes its own 2048 tokens (weak scaling), and after
+each linear's backward the adapter gradients dA, dB are summed over the
+ranks (an NCCL all-reduce on a side stream).
 
 `--impl reference` times the CPU oracle (the plain fp64 restatement of the
 method, the only reference this subject has) on the same config with a
@@ -28,7 +37,6 @@ import hashlib
 import json
 import math
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -49,6 +57,9 @@ def parse_args():
     p.add_argument("--steps", type=int, default=30)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=["llama33b", "llama7b"], default="llama33b",
+                   help="the timed step: the 60x7 LLaMA-33B stack (default) or the 7 LLaMA-7B linears")
+    p.add_argument("--layers", type=int, default=60, help="layers of the 33B stack (profiling runs only)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-extras", action="store_true", help="skip the decode and quantizer sub-results")
@@ -73,21 +84,24 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def profile_traffic(name, src_files):
-    """Per-launch DRAM bytes recorded in profiles/<name>.md for the current kernel source, else None."""
-    path = os.path.join(ROOT, "profiles", name + ".md")
+def ncu_traffic(kernel, src_files):
+    """DRAM bytes per launch of `kernel` from the ncu capture recorded in
+    profiles/ncu_traffic.json, if it was taken on the current kernel source
+    (sha256 over `src_files`), else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
-        text = open(path).read()
-    except OSError:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec:
         return None
     h = hashlib.sha256()
     for f in src_files:
         h.update(open(os.path.join(ROOT, f), "rb").read())
-    m_src = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_src or not m_tr or m_src.group(1) != h.hexdigest():
+    if rec.get("source_sha256") != h.hexdigest():
         return None
-    return float(m_tr.group(1))
+    return rec.get("dram_bytes_per_launch")
 
 
 class ClockSampler:
@@ -149,34 +163,20 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def cpu_cores():
-    try:
-        return len(os.sched_getaffinity(0))
-    except AttributeError:
-        return os.cpu_count() or 1
-
-
-def blas_threads():
-    try:
-        from threadpoolctl import threadpool_info
-        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
-        return max(n) if n else cpu_cores()
-    except Exception:
-        return cpu_cores()
-
-
 # ----------------------------------------------------------------------------- CPU oracle sample
 
-def oracle_sample_setup(M_sample=512):
-    """The first LLaMA-7B linear (q_proj 4096x4096) quantized by the oracle, with M_sample tokens."""
-    from bit_nf4_quantized_38_b300.workloads import bf16_bits, case_inputs, case_weight, llama7b_linears
+def oracle_sample_setup(workload="llama33b", M_sample=512):
+    """The workload's first linear (q_proj: 6656x6656 for the 33B stack,
+    4096x4096 for the 7B linears) quantized by the oracle, with M_sample tokens."""
+    from bit_nf4_quantized_38_b300.workloads import bf16_bits, case_inputs, case_weight, llama33b_stack, \
+        llama7b_linears
     from oracle import nf4
-    case = llama7b_linears().cases[0]
+    case = (llama7b_linears() if workload == "llama7b" else llama33b_stack(layers=1)).cases[0]
     W = case_weight(case)
     X, A, B, dY = case_inputs(case, M=M_sample)
     qt = nf4.quantize(bf16_bits(W))
     return dict(case=case, qt=qt, X=bf16_bits(X), A=bf16_bits(A), B=bf16_bits(B), dY=bf16_bits(dY),
-                M=M_sample)
+                M=M_sample, workload=workload)
 
 
 def oracle_sample_step(s):
@@ -192,13 +192,20 @@ def oracle_sample_flops(s):
     return 4 * s["M"] * c.N * c.K + 6 * s["M"] * c.r * (c.N + c.K)
 
 
-def cpu_oracle_details(s):
+def oracle_sample_text(s):
+    c = s["case"]
+    return (f"{c.name} {c.N}x{c.K} linear of the workload, {s['M']} tokens, r={c.r}: NF4+DQ dequantize + fwd + "
+            f"bwd in fp64 numpy")
+
+
+def cpu_oracle_details(s, workload_flops_step):
     """Bounded samples of the other workloads, timed once each on the host's
     cores with the same oracle: the single 1024 x 1024 linear in full; the
-    q_proj sample on one BLAS thread; 512 rows of the 5120 x 5120 decode layer
-    (dequantize + forward, M = 1); 512 rows of an 8192-wide LLaMA-65B weight
-    (quantize, then dequantize).  Rates use the algorithmic bytes or flops of
-    the sample itself."""
+    training sample on one BLAS thread; 512 rows of the 5120 x 5120 decode
+    layer (dequantize + forward, M = 1); 512 rows of an 8192-wide LLaMA-65B
+    weight (quantize, then dequantize).  Rates use the algorithmic bytes or
+    flops of the sample itself; the time of a whole step of the workload at
+    the sample's rate is given as an extrapolation."""
     from bit_nf4_quantized_38_b300.workloads import (bf16_bits, case_inputs, case_weight, llama13b_decode,
                                                      single_linear_1024, student_t4_bf16)
     from oracle import linear, nf4
@@ -212,17 +219,18 @@ def cpu_oracle_details(s):
     linear.lora_forward(X, Wh, A, B, c.scale)
     linear.lora_backward(dY, X, Wh, A, B, c.scale)
     out["single_linear_1024_us"] = (time.perf_counter() - t0) * 1e6
-    # the q_proj training sample on one thread: a child process started with
-    # the BLAS thread counts set to 1 (they are fixed when numpy loads)
+    # the training sample on one thread: a child process started with the
+    # BLAS thread counts set to 1 (they are fixed when numpy loads)
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    code = ("import sys, time, json; sys.path.insert(0, %r); import bench; s = bench.oracle_sample_setup(); "
+    code = ("import sys, time, json; sys.path.insert(0, %r); import bench; s = bench.oracle_sample_setup(%r); "
             "t0 = time.perf_counter(); bench.oracle_sample_step(s); dt = time.perf_counter() - t0; "
-            "print(json.dumps(bench.oracle_sample_flops(s) / dt / 1e12))" % os.path.dirname(os.path.abspath(__file__)))
+            "print(json.dumps(bench.oracle_sample_flops(s) / dt / 1e12))"
+            % (os.path.dirname(os.path.abspath(__file__)), s["workload"]))
     try:
         r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
-        out["llama7b_q_proj_sample_1thread_tflops"] = json.loads(r.stdout.strip().splitlines()[-1])
+        out["training_sample_1thread_tflops"] = json.loads(r.stdout.strip().splitlines()[-1])
     except Exception as e:  # the all-core figures above and below stand on their own
-        out["llama7b_q_proj_sample_1thread_tflops"] = None
+        out["training_sample_1thread_tflops"] = None
         out["one_thread_error"] = f"{type(e).__name__}: {e}"[:200]
     # decode: 512 of the 5120 rows of the 13B 5120 x 5120 layer, M = 1
     c = llama13b_decode(M=1).cases[0]
@@ -247,24 +255,41 @@ def cpu_oracle_details(s):
     byts = n * (2 + 0.5 + 1 / 64 + 4 / (64 * 256))
     out["llama65b_quantize_sample_gbs"] = byts / (t1 - t0) / 1e9
     out["llama65b_dequantize_sample_gbs"] = byts / (t2 - t1) / 1e9
-    out["samples"] = ("single linear 1024x1024 M=16 r=8 in full; q_proj 512-token sample on 1 BLAS thread; "
+    out["samples"] = ("single linear 1024x1024 M=16 r=8 in full; the training sample on 1 BLAS thread; "
                       "512 of 5120 rows of the 13B 5120x5120 decode layer (M=1, dequantize + fwd); "
                       "512 x 8192 Student-t(4) weight (quantize, dequantize)")
     return out
 
 
-def cpu_baseline(repeats=3):
-    s = oracle_sample_setup()
+def cpu_baseline(workload, workload_flops_step, repeats=3):
+    s = oracle_sample_setup(workload)
     oracle_sample_step(s)  # warm
     t0 = time.perf_counter()
     for _ in range(repeats):
         oracle_sample_step(s)
     dt = (time.perf_counter() - t0) / repeats
-    return {"value": oracle_sample_flops(s) / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
-            "kind": "oracle",
-            "sample": f"q_proj 4096x4096 linear, {s['M']} tokens, r=64: NF4+DQ dequantize + fwd + bwd in "
-                      f"fp64 numpy, mean of {repeats} runs ({dt:.2f} s each)",
-            "details": cpu_oracle_details(s)}
+    rate = oracle_sample_flops(s) / dt / 1e12
+    return {"value": rate, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{oracle_sample_text(s)}, mean of {repeats} runs ({dt:.2f} s each)",
+            "extrapolated_s_per_step": workload_flops_step / (rate * 1e12),
+            "extrapolation": "one step of the whole workload at the sample's rate (extrapolated, not run)",
+            "details": cpu_oracle_details(s, workload_flops_step)}
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else cpu_cores()
+    except Exception:
+        return cpu_cores()
 
 
 # ----------------------------------------------------------------------------- ranks (N > 1: replicas)
@@ -291,11 +316,36 @@ def job_tflops(world, flops_per_rank_step, ms_per_step):
     return world * flops_per_rank_step / (ms_per_step / 1e3) / 1e12
 
 
+def workload_of(name, layers=60):
+    from bit_nf4_quantized_38_b300.workloads import llama33b_stack, llama7b_linears
+    return llama7b_linears() if name == "llama7b" else llama33b_stack(layers=layers)
+
+
+def step_flops(wl):
+    return sum(4 * c.M * c.N * c.K + 6 * c.M * c.r * (c.N + c.K) for c in wl.cases)
+
+
+def config_of(wl, world):
+    c0 = wl.cases[0]
+    shapes = []
+    for c in wl.cases:
+        name = c.name.split(".")[-1]
+        if (name, c.N, c.K) not in shapes:
+            shapes.append((name, c.N, c.K))
+    return {"workload": wl.name, "layers": wl.layers, "linears_per_layer": [f"{n} {N}x{K}" for n, N, K in shapes],
+            "M": c0.M, "r": c0.r, "alpha": c0.alpha, "quant": "NF4 block 64 + double quant block 256",
+            "step": f"fwd of {len(wl.cases)} linears in order, then bwd in reverse",
+            "l2": "inputs larger than L2 (each linear has its own weight and activations; one step touches "
+                  f"{'~80' if wl.layers > 1 else '~0.7'} GB)",
+            "parallelism": f"data parallel x{world} (own tokens per rank, dA/dB all-reduced)" if world > 1
+            else "single GPU"}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    s = oracle_sample_setup()
+    s = oracle_sample_setup(args.workload)
     for _ in range(args.warmup):
         oracle_sample_step(s)
     t0 = time.perf_counter()
@@ -303,17 +353,15 @@ def run_reference(args):
         oracle_sample_step(s)
     dt = (time.perf_counter() - t0) / args.steps
     v = oracle_sample_flops(s) / dt / 1e12
-    from bit_nf4_quantized_38_b300.workloads import llama7b_linears
-    wl = llama7b_linears()
+    wl = workload_of(args.workload, args.layers)
+    cfg = config_of(wl, 1)
+    cfg["sample_per_step"] = oracle_sample_text(s)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "linears": [c.name for c in wl.cases], "M": 4096, "r": 64,
-                   "alpha": 16, "sample_per_step": "q_proj linear, 512 tokens"},
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
         "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-                         "sample": "per step: q_proj 4096x4096 linear, 512 tokens, r=64: NF4+DQ dequantize "
-                                   "+ fwd + bwd in fp64 numpy"},
+                         "sample": "per step: " + oracle_sample_text(s)},
         "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -472,6 +520,203 @@ def run_only(args):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+def build_layers(ql, dev, wl):
+    """Quantized weights and seeded inputs / outputs of every linear, on the device."""
+    import torch
+    from bit_nf4_quantized_38_b300.workloads import case_inputs, case_weight
+    layers = []
+    for c in wl.cases:
+        W = case_weight(c, device=dev)
+        q = ql.nf4_quantize(W)
+        del W
+        X, A, B, dY = case_inputs(c, device=dev)
+        layers.append(dict(case=c, q=q, X=X, A=A, B=B, dY=dY,
+                           Y=torch.empty(c.M, c.N, dtype=torch.bfloat16, device=dev),
+                           XA=torch.empty(c.M, c.r, dtype=torch.bfloat16, device=dev),
+                           dX=torch.empty(c.M, c.K, dtype=torch.bfloat16, device=dev),
+                           dA=torch.empty(c.K, c.r, dtype=torch.float32, device=dev),
+                           dB=torch.empty(c.r, c.N, dtype=torch.float32, device=dev)))
+    torch.cuda.synchronize()
+    return layers
+
+
+def run_workload(ql, dev, wl, args, world, sampler=None, e2e=True):
+    """Time args.steps steps of the workload (after args.warmup untimed ones).
+    Returns the result dict (value, ms_per_step, roofline, launches, e2e)."""
+    import torch
+    import torch.distributed as dist
+    layers = build_layers(ql, dev, wl)
+    ws_bytes = max(max(ql.workspace_size(ql.OP_LINEAR_FWD, c.M, c.N, c.K, c.r),
+                       ql.workspace_size(ql.OP_LINEAR_BWD, c.M, c.N, c.K, c.r)) for c in wl.cases)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    comm = torch.cuda.Stream() if world > 1 else None
+    for L in layers:
+        L["ev_bwd"], L["ev_red"] = torch.cuda.Event(), torch.cuda.Event()
+        L["ev_red"].record(stream)
+
+    def bwd(L):
+        if comm is not None:
+            stream.wait_event(L["ev_red"])  # the previous step's all-reduce of dA, dB is done
+        ql.qlora_linear_bwd(L["dY"], L["X"], L["XA"], L["q"], L["A"], L["B"], L["case"].scale,
+                            dX=L["dX"], dA=L["dA"], dB=L["dB"], ws=ws)
+        if comm is not None:  # data parallel: the adapter gradients summed over the ranks
+            L["ev_bwd"].record(stream)
+            comm.wait_event(L["ev_bwd"])
+            with torch.cuda.stream(comm):
+                dist.all_reduce(L["dA"])
+                dist.all_reduce(L["dB"])
+            L["ev_red"].record(comm)
+
+    def step():
+        for L in layers:
+            ql.qlora_linear_fwd(L["X"], L["q"], L["A"], L["B"], L["case"].scale, Y=L["Y"], XA=L["XA"], ws=ws)
+        for L in reversed(layers):
+            bwd(L)
+
+    flops = step_flops(wl)
+    for _ in range(args.warmup):
+        step()
+    if comm is not None:
+        stream.wait_stream(comm)
+    torch.cuda.synchronize()
+
+    n_gemm = 2 * len(layers) * args.steps
+    spans = torch.empty(2 * n_gemm, dtype=torch.int64, device=dev)
+    ql.spans_start(spans)
+    torch.cuda.synchronize()
+    rank_barrier(world)
+    n_launch0 = ql.launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    if comm is not None:
+        stream.wait_stream(comm)  # the last all-reduces belong to the timed region
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    rank_barrier(world)
+    launches = ql.launch_count() - n_launch0
+    n_rec, gemm_flops = ql.spans_stop()
+    ql.device_status()
+    sp = spans.view(-1, 2)[:n_rec].cpu()
+    busy_ms = float((sp[:, 1] - sp[:, 0]).sum()) / 1e6
+    ms_total = max_over_ranks_of(ev0.elapsed_time(ev1), world, dev)
+    ms_step = ms_total / args.steps
+    res = {"value": job_tflops(world, flops, ms_step), "ms_per_step": ms_step, "ms_total": ms_total,
+           "flops_per_step": flops, "gpu_launches": launches, "t_wall": (t_wall0, t_wall1),
+           "gemm": {"launches": n_rec, "flops": gemm_flops, "busy_ms": busy_ms}}
+
+    # ---- end to end through the public API with host buffers
+    if e2e:
+        res["e2e"] = run_e2e(ql, dev, layers, ws, stream, args, world, flops)
+    del layers, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_e2e(ql, dev, layers, ws, stream, args, world, flops):
+    """The same step with every linear's X and dY copied from pinned host
+    memory on a copy stream running ahead of the compute, and dA, dB read back
+    on a second copy stream after each backward.  The host holds the inputs of
+    up to 8 layers (each distinct and seeded); layer l copies from host set
+    l mod 8.  Y and dX stay on the device."""
+    import torch
+    per_layer = 7 if len(layers) % 7 == 0 else len(layers)
+    n_sets = min(8, len(layers) // per_layer)
+    host = []
+    for i in range(n_sets * per_layer):
+        L = layers[i]
+        host.append(dict(X=torch.empty(L["X"].shape, dtype=torch.bfloat16).pin_memory(),
+                         dY=torch.empty(L["dY"].shape, dtype=torch.bfloat16).pin_memory(),
+                         dA=torch.empty(L["dA"].shape, dtype=torch.float32).pin_memory(),
+                         dB=torch.empty(L["dB"].shape, dtype=torch.float32).pin_memory()))
+        host[-1]["X"].copy_(L["X"])
+        host[-1]["dY"].copy_(L["dY"])
+    h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    for i, L in enumerate(layers):
+        L["h"] = host[i % len(host)]
+        L["ev_x"], L["ev_dy"] = torch.cuda.Event(), torch.cuda.Event()
+        L["ev_b"], L["ev_d2h"] = torch.cuda.Event(), torch.cuda.Event()
+        L["ev_b"].record(stream)
+        L["ev_d2h"].record(stream)
+
+    def step_e2e():
+        for L in layers:
+            h2d_stream.wait_event(L["ev_b"])  # the previous step's backward is done with X
+            with torch.cuda.stream(h2d_stream):
+                L["X"].copy_(L["h"]["X"], non_blocking=True)
+            L["ev_x"].record(h2d_stream)
+        for L in reversed(layers):
+            with torch.cuda.stream(h2d_stream):
+                L["dY"].copy_(L["h"]["dY"], non_blocking=True)
+            L["ev_dy"].record(h2d_stream)
+        for L in layers:
+            stream.wait_event(L["ev_x"])
+            ql.qlora_linear_fwd(L["X"], L["q"], L["A"], L["B"], L["case"].scale, Y=L["Y"], XA=L["XA"], ws=ws)
+        for L in reversed(layers):
+            stream.wait_event(L["ev_dy"])
+            stream.wait_event(L["ev_d2h"])  # the previous step's read-back of dA, dB is done
+            ql.qlora_linear_bwd(L["dY"], L["X"], L["XA"], L["q"], L["A"], L["B"], L["case"].scale,
+                                dX=L["dX"], dA=L["dA"], dB=L["dB"], ws=ws)
+            L["ev_b"].record(stream)
+            d2h_stream.wait_event(L["ev_b"])
+            with torch.cuda.stream(d2h_stream):
+                L["h"]["dA"].copy_(L["dA"], non_blocking=True)
+                L["h"]["dB"].copy_(L["dB"], non_blocking=True)
+            L["ev_d2h"].record(d2h_stream)
+
+    steps = args.steps if len(layers) <= 7 else min(args.steps, 5)
+    for _ in range(2):
+        step_e2e()
+    torch.cuda.synchronize()
+    rank_barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    h2d_stream.wait_event(e0)
+    d2h_stream.wait_event(e0)
+    for _ in range(steps):
+        step_e2e()
+    stream.wait_stream(d2h_stream)  # the last read-backs belong to the timed region
+    stream.wait_stream(h2d_stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    rank_barrier(world)
+    e_ms = max_over_ranks_of(e0.elapsed_time(e1), world, dev) / steps
+    h2d = sum(2 * L["case"].M * (L["case"].K + L["case"].N) for L in layers)
+    d2h = sum(4 * L["case"].r * (L["case"].K + L["case"].N) for L in layers)
+    return {"value": job_tflops(world, flops, e_ms), "unit": "TFLOP/s", "ms_per_step": e_ms, "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "note": f"per step: X and dY of all {len(layers)} linears copied from pinned host memory "
+                    f"({len(host)} distinct linears' inputs held on the host, reused in turn) on a copy stream "
+                    "running ahead of the compute, dA and dB read back on a second copy stream; Y and dX stay "
+                    "on the device"}
+
+
+def roofline_of(res, peaks, peak_src, wl):
+    """The tensor-core GEMM inside the timed steps: algorithmic flops of its
+    launches over the sum of their in-step durations (first CTA past its
+    dependency wait to last CTA done, %globaltimer)."""
+    g = res["gemm"]
+    achieved = g["flops"] / (g["busy_ms"] / 1e3) / 1e12 if g["busy_ms"] > 0 else 0.0
+    long_region = res["ms_total"] >= 1000.0
+    peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+    traffic = ncu_traffic("k_nf4_gemm_pair " + wl.name, ["bit_nf4_quantized_38_b300/csrc/tc_gemm.cu"])
+    return {"kernel": "k_nf4_gemm_pair (tcgen05 fused NF4-dequant GEMM, fwd Y and bwd dX)",
+            "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": traffic,
+            "peak_source": f"{peak_src} bf16 dense, "
+                           f"{'sustained (timed region of seconds)' if long_region else 'burst'}",
+            "frac_of_burst": achieved / peaks["bf16_tflops"],
+            "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+            "launches_timed": g["launches"], "kernel_ms_per_step": g["busy_ms"] / res["ms_total"] * res["ms_per_step"],
+            "share_of_step": g["busy_ms"] / res["ms_total"] if res["ms_total"] else None,
+            "timing": "per launch: earliest CTA start after its dependency wait to latest CTA end "
+                      "(%globaltimer stamps the kernel records in the timed steps themselves)"}
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -493,186 +738,36 @@ def main():
     dev = torch.device("cuda", local)
 
     from bit_nf4_quantized_38_b300 import qlora as ql
-    from bit_nf4_quantized_38_b300.workloads import case_inputs, case_weight, llama7b_linears
 
-    wl = llama7b_linears()
-    if args.linears:
-        keep = set(args.linears.split(","))
-        wl.cases = [c for c in wl.cases if c.name in keep]
-        wl.name += "_subset_" + "+".join(c.name for c in wl.cases)
-    layers = []
-    for c in wl.cases:
-        W = case_weight(c).to(dev)
-        q = ql.nf4_quantize(W)
-        del W
-        X, A, B, dY = case_inputs(c)
-        L = dict(case=c, q=q, X=X.to(dev), A=A.to(dev), B=B.to(dev), dY=dY.to(dev),
-                 Y=torch.empty(c.M, c.N, dtype=torch.bfloat16, device=dev),
-                 XA=torch.empty(c.M, c.r, dtype=torch.bfloat16, device=dev),
-                 dX=torch.empty(c.M, c.K, dtype=torch.bfloat16, device=dev),
-                 dA=torch.empty(c.K, c.r, dtype=torch.float32, device=dev),
-                 dB=torch.empty(c.r, c.N, dtype=torch.float32, device=dev))
-        if not args.no_e2e:
-            L["X_h"] = X.pin_memory()
-            L["dY_h"] = dY.pin_memory()
-            L["dA_h"] = torch.empty(c.K, c.r, dtype=torch.float32).pin_memory()
-            L["dB_h"] = torch.empty(c.r, c.N, dtype=torch.float32).pin_memory()
-        layers.append(L)
-    ws_bytes = max(max(ql.workspace_size(ql.OP_LINEAR_FWD, c.M, c.N, c.K, c.r),
-                       ql.workspace_size(ql.OP_LINEAR_BWD, c.M, c.N, c.K, c.r)) for c in wl.cases)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
-    torch.cuda.synchronize()
-
-    def step():
-        for L in layers:
-            ql.qlora_linear_fwd(L["X"], L["q"], L["A"], L["B"], L["case"].scale, Y=L["Y"], XA=L["XA"], ws=ws)
-        for L in reversed(layers):
-            ql.qlora_linear_bwd(L["dY"], L["X"], L["XA"], L["q"], L["A"], L["B"], L["case"].scale,
-                                dX=L["dX"], dA=L["dA"], dB=L["dB"], ws=ws)
-
-    # End to end: the inputs of every linear come from pinned host memory and
-    # dA, dB go back to it, as a training loop would do it: host-to-device
-    # copies on their own stream run ahead of the compute (each waits until
-    # the previous step's backward has finished with that linear's buffers),
-    # the device-to-host copies on a third stream follow each backward.
-    h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
-    for L in layers:
-        L["ev_x"], L["ev_dy"] = torch.cuda.Event(), torch.cuda.Event()
-        L["ev_bwd"], L["ev_d2h"] = torch.cuda.Event(), torch.cuda.Event()
-        L["ev_bwd"].record(stream)
-        L["ev_d2h"].record(stream)
-
-    def step_e2e():
-        for L in layers:
-            h2d_stream.wait_event(L["ev_bwd"])
-            with torch.cuda.stream(h2d_stream):
-                L["X"].copy_(L["X_h"], non_blocking=True)
-            L["ev_x"].record(h2d_stream)
-        for L in reversed(layers):
-            with torch.cuda.stream(h2d_stream):
-                L["dY"].copy_(L["dY_h"], non_blocking=True)
-            L["ev_dy"].record(h2d_stream)
-        for L in layers:
-            stream.wait_event(L["ev_x"])
-            ql.qlora_linear_fwd(L["X"], L["q"], L["A"], L["B"], L["case"].scale, Y=L["Y"], XA=L["XA"], ws=ws)
-        for L in reversed(layers):
-            stream.wait_event(L["ev_dy"])
-            stream.wait_event(L["ev_d2h"])  # the previous step's read-back of dA, dB is done
-            ql.qlora_linear_bwd(L["dY"], L["X"], L["XA"], L["q"], L["A"], L["B"], L["case"].scale,
-                                dX=L["dX"], dA=L["dA"], dB=L["dB"], ws=ws)
-            L["ev_bwd"].record(stream)
-            d2h_stream.wait_event(L["ev_bwd"])
-            with torch.cuda.stream(d2h_stream):
-                L["dA_h"].copy_(L["dA"], non_blocking=True)
-                L["dB_h"].copy_(L["dB"], non_blocking=True)
-            L["ev_d2h"].record(d2h_stream)
-
-    flops_step = sum(4 * c.M * c.N * c.K + 6 * c.M * c.r * (c.N + c.K) for c in wl.cases)
-
-    def barrier():
-        rank_barrier(world)
-
-    def max_over_ranks(x):
-        return max_over_ranks_of(x, world, dev)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-
+    peaks, peak_src = load_peaks()
+    wl = workload_of(args.workload, args.layers)
     uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     sampler = ClockSampler(uuid)
     sampler.start()
     time.sleep(0.2)
-
-    barrier()
-    torch.cuda.synchronize()
-    n_launch0 = ql.launch_count()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_wall0 = time.time()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
-    barrier()
-    launches = ql.launch_count() - n_launch0
-    # The GEMM launch durations for the roofline come from a second pass of the
-    # same steps with a CUDA event pair around every GEMM launch (events between
-    # kernels would stop the programmatic overlap the timed pass above uses).
-    ql.timing_start(14 * args.steps)
-    for _ in range(args.steps):
-        step()
-    torch.cuda.synchronize()
-    gemm_ms, gemm_launches, gemm_flops = ql.timing_stop()
-    ql.device_status()
-    ms_total = max_over_ranks(ev0.elapsed_time(ev1))
+    res = run_workload(ql, dev, wl, args, world, e2e=not args.no_e2e)
     time.sleep(0.1)
-    sampler.stop()
-    clocks = sampler.summary(t_wall0, t_wall1)
-
-    ms_step = ms_total / args.steps
-    value = job_tflops(world, flops_step, ms_step)
-
-    # ---- end to end through the public API with host buffers
-    e2e = None
-    if not args.no_e2e:
-        for _ in range(2):
-            step_e2e()
-        torch.cuda.synchronize()
-        barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        h2d_stream.wait_event(e0)
-        d2h_stream.wait_event(e0)
-        for _ in range(args.steps):
-            step_e2e()
-        stream.wait_stream(d2h_stream)  # the last read-backs belong to the timed region
-        stream.wait_stream(h2d_stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        e_ms = max_over_ranks(e0.elapsed_time(e1)) / args.steps
-        h2d = sum(2 * c.M * (c.K + c.N) for c in wl.cases)
-        d2h = sum(4 * c.r * (c.K + c.N) for c in wl.cases)
-        e2e = {"value": job_tflops(world, flops_step, e_ms), "unit": "TFLOP/s", "ms_per_step": e_ms,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "note": "per step: X and dY of all 7 linears copied from pinned host memory on a copy "
-                       "stream running ahead of the compute, dA and dB read back on a second copy "
-                       "stream; Y and dX stay on the device"}
-
-    peaks, peak_src = load_peaks()
-    achieved = gemm_flops / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else 0.0
-    traffic = profile_traffic("nf4_gemm_llama7b", ["bit_nf4_quantized_38_b300/csrc/tc_gemm.cu"])
-    roofline = {"kernel": "k_nf4_gemm (tcgen05 fused NF4-dequant GEMM, fwd Y and bwd dX)",
-                "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
-                "peak_source": f"{peak_src} bf16 dense (burst)",
-                "frac_of_sustained": achieved / peaks.get("bf16_tflops_sustained", 1400.0),
-                "launches_timed": gemm_launches, "kernel_ms_per_step": gemm_ms / args.steps,
-                "timing": "CUDA event pair around each GEMM launch, in a second pass of the same steps",
-                "share_of_step": gemm_ms / ms_total if ms_total else None}
+    clocks = sampler.summary(*res["t_wall"])
 
     out = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "linears": [f"{c.name} {c.N}x{c.K}" for c in wl.cases], "M": 4096,
-                   "r": 64, "alpha": 16, "quant": "NF4 block 64 + double quant block 256",
-                   "step": "fwd of 7 linears in order, then bwd in reverse",
-                   "l2": "inputs larger than L2 (each step touches ~0.7 GB of weights, activations "
-                         "and gradients)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": roofline,
-        "gpu_launches": launches,
+        "metric": METRIC, "value": res["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(wl, world),
+        "roofline": roofline_of(res, peaks, peak_src, wl),
+        "gpu_launches": res["gpu_launches"],
         "clocks": clocks,
     }
-    if e2e:
-        out["e2e"] = e2e
+    if "e2e" in res:
+        out["e2e"] = res["e2e"]
     if not args.no_extras and world == 1:
-        del layers, ws
-        torch.cuda.empty_cache()
+        if args.workload != "llama7b":
+            wl7 = workload_of("llama7b")
+            r7 = run_workload(ql, dev, wl7, argparse.Namespace(steps=max(args.steps, 20), warmup=args.warmup),
+                              1, e2e=False)
+            out["llama7b"] = {"workload": wl7.name, "value": r7["value"], "unit": "TFLOP/s",
+                              "ms_per_step": r7["ms_per_step"], "steps": max(args.steps, 20),
+                              "roofline": roofline_of(r7, peaks, peak_src, wl7),
+                              "clocks": sampler.summary(*r7["t_wall"])}
         out["decode"] = {"workload": "llama13b decode shapes, M in {1,4,16}, r=64, fwd, CUDA graph over "
                                      "weight copies > 3x L2",
                          "peak_hbm_gbs": peaks["hbm_gbs"],
@@ -681,8 +776,9 @@ def main():
                                                  tuple(int(i) for i in args.decode_shapes.split(",")))}
         out["quantize"] = bench_quantize(ql, dev, peaks["hbm_gbs"])
         out["single_linear"] = bench_single_linear(ql, dev)
+    sampler.stop()
     if rank == 0 and world == 1 and not args.no_cpu:
-        out["cpu_baseline"] = cpu_baseline()
+        out["cpu_baseline"] = cpu_baseline(args.workload, step_flops(wl))
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -100,30 +100,78 @@ extern "C" int ql_get_device_status(ql_stream_t stream) {
   return QL_OK;
 }
 
-extern "C" int nf4_quantize(const uint16_t *W, const ql_nf4_tensor *q, void *ws, size_t ws_bytes,
-                            ql_stream_t stream) {
-  g_msg[0] = 0;
-  int rc = check_tensor(q, "nf4_quantize", true);
-  if (rc) return rc;
-  if (!W) return set_error(QL_ERR_INVALID, "nf4_quantize: null W");
-  if (!aligned(W, 16)) return set_error(QL_ERR_MISALIGNED, "nf4_quantize: W not 16-byte aligned");
-  if (!ws) return set_error(QL_ERR_INVALID, "nf4_quantize: null workspace");
-  if (!aligned(ws, 256)) return set_error(QL_ERR_MISALIGNED, "nf4_quantize: workspace not 256-byte aligned");
+namespace {
+
+int check_quant_ws(const ql_nf4_tensor *q, void *ws, size_t ws_bytes, const char *fn) {
+  if (!ws) return set_error(QL_ERR_INVALID, "%s: null workspace", fn);
+  if (!aligned(ws, 256)) return set_error(QL_ERR_MISALIGNED, "%s: workspace not 256-byte aligned", fn);
   if (ws_bytes < quantize_ws(q->rows, q->cols))
-    return set_error(QL_ERR_UNSUPPORTED, "nf4_quantize: workspace %zu < %zu bytes", ws_bytes,
+    return set_error(QL_ERR_UNSUPPORTED, "%s: workspace %zu < %zu bytes", fn, ws_bytes,
                      quantize_ws(q->rows, q->cols));
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return QL_OK;
+}
+
+// First-level quantization: codes, block absmax (into the workspace when
+// double quantization follows) and the fp64 absmax sum at the workspace head.
+int quantize_first(const uint16_t *W, const ql_nf4_tensor *q, void *ws, size_t ws_bytes, cudaStream_t st,
+                   const char *fn) {
+  int rc = check_tensor(q, fn, true);
+  if (rc) return rc;
+  if (!W) return set_error(QL_ERR_INVALID, "%s: null W", fn);
+  if (!aligned(W, 16)) return set_error(QL_ERR_MISALIGNED, "%s: W not 16-byte aligned", fn);
+  rc = check_quant_ws(q, ws, ws_bytes, fn);
+  if (rc) return rc;
   note_other_call(st);
   double *sum = static_cast<double *>(ws);
   float *absmax = q->dq_blocksize ? reinterpret_cast<float *>(static_cast<char *>(ws) + 256) : q->absmax;
-  const int64_t n_b = q->rows * q->cols / 64;
-  rc = check_cuda(cudaMemsetAsync(sum, 0, sizeof(double), st), "nf4_quantize: clear sum");
+  rc = check_cuda(cudaMemsetAsync(sum, 0, sizeof(double), st), "quantize: clear sum");
   if (rc) return rc;
-  rc = check_cuda(launch_quantize(W, q->rows, q->cols, q->packed, absmax, sum, st), "nf4_quantize: launch");
-  if (rc || !q->dq_blocksize) return rc;
-  return check_cuda(launch_double_quant(absmax, n_b, q->dq_blocksize, sum, q->absmax_code, q->dq_step,
-                                        q->dq_mean, st),
-                    "nf4_quantize: double-quant launch");
+  return check_cuda(launch_quantize(W, q->rows, q->cols, q->packed, absmax, sum, st), "quantize: launch");
+}
+
+// Second level: mu = fl32(S / total_blocks) from the fp64 sum at the
+// workspace head, then the codes and steps of this tensor's blocks.
+int quantize_second(const ql_nf4_tensor *q, void *ws, int64_t total_blocks, cudaStream_t st) {
+  if (!q->dq_blocksize) return QL_OK;
+  const int64_t n_b = q->rows * q->cols / 64;
+  float *absmax = reinterpret_cast<float *>(static_cast<char *>(ws) + 256);
+  return check_cuda(launch_double_quant(absmax, n_b, total_blocks, q->dq_blocksize, static_cast<double *>(ws),
+                                        q->absmax_code, q->dq_step, q->dq_mean, st),
+                    "quantize: double-quant launch");
+}
+
+}  // namespace
+
+extern "C" int nf4_quantize(const uint16_t *W, const ql_nf4_tensor *q, void *ws, size_t ws_bytes,
+                            ql_stream_t stream) {
+  g_msg[0] = 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int rc = quantize_first(W, q, ws, ws_bytes, st, "nf4_quantize");
+  if (rc) return rc;
+  return quantize_second(q, ws, q->rows * q->cols / 64, st);
+}
+
+extern "C" int nf4_quantize_shard_begin(const uint16_t *W, const ql_nf4_tensor *q, void *ws, size_t ws_bytes,
+                                        ql_stream_t stream) {
+  g_msg[0] = 0;
+  return quantize_first(W, q, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), "nf4_quantize_shard_begin");
+}
+
+extern "C" int nf4_quantize_shard_end(const ql_nf4_tensor *q, void *ws, size_t ws_bytes, int64_t total_blocks,
+                                      ql_stream_t stream) {
+  g_msg[0] = 0;
+  const char *fn = "nf4_quantize_shard_end";
+  int rc = check_tensor(q, fn, true);
+  if (rc) return rc;
+  rc = check_quant_ws(q, ws, ws_bytes, fn);
+  if (rc) return rc;
+  const int64_t n_b = q->rows * q->cols / 64;
+  if (total_blocks < n_b)
+    return set_error(QL_ERR_INVALID, "%s: total_blocks %lld < the shard's %lld blocks", fn, (long long)total_blocks,
+                     (long long)n_b);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  note_other_call(st);
+  return quantize_second(q, ws, total_blocks, st);
 }
 
 extern "C" int nf4_dequantize(const ql_nf4_tensor *q, uint16_t *W_out, ql_stream_t stream) {

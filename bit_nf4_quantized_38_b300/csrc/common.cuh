@@ -60,8 +60,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 cudaError_t launch_quantize(const uint16_t *W, int64_t rows, int64_t cols, uint8_t *packed,
                             float *absmax, double *sum_acc, cudaStream_t st);
-cudaError_t launch_double_quant(const float *absmax, int64_t n_b, int dq_bs, const double *sum,
-                                int8_t *code, float *step, float *mean, cudaStream_t st);
+// mu = fl32(sum / total_blocks); codes and steps of the n_b blocks given.
+cudaError_t launch_double_quant(const float *absmax, int64_t n_b, int64_t total_blocks, int dq_bs,
+                                const double *sum, int8_t *code, float *step, float *mean, cudaStream_t st);
 cudaError_t launch_dequantize(const ql_nf4_tensor &q, uint16_t *W_out, cudaStream_t st);
 
 }  // namespace ql

@@ -842,7 +842,8 @@ size_t decode_ws(int64_t N, int64_t K, int r) {
 
 size_t decode_ws_half(int64_t N, int r) { return ws_layout(N, r).total; }
 
-int launch_decode(const DecodeProblem &p, cudaStream_t st) {
+int launch_decode(const DecodeProblem &p, cudaStream_t st, bool *early_dependents) {
+  *early_dependents = false;
   int dev = 0;
   int rc = check_cuda(cudaGetDevice(&dev), "decode: current device");
   if (rc) return rc;
@@ -877,6 +878,7 @@ int launch_decode(const DecodeProblem &p, cudaStream_t st) {
   f.M = a.M; f.N = a.N; f.nbox = a.nbox; f.W = a.W; f.G = G;
   f.x_early = a.x_early;
   f.launch_early = G == di.sms;
+  *early_dependents = f.launch_early;
   f.xap = a.xap; f.slots = a.slots;
   f.B = p.B; f.scale = p.scale; f.Y = p.Y; f.XA_out = p.XA_out;
   const bool mt2 = p.M > 8;

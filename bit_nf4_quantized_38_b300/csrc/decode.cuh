@@ -23,6 +23,8 @@ struct DecodeProblem {
 
 size_t decode_ws(int64_t N, int64_t K, int r);
 size_t decode_ws_half(int64_t N, int r);
-int launch_decode(const DecodeProblem &p, cudaStream_t st);
+// *early_dependents is set when the finishing kernel lets dependents launch
+// before its own wait (the stream kernel then fills every SM).
+int launch_decode(const DecodeProblem &p, cudaStream_t st, bool *early_dependents);
 
 }  // namespace ql

@@ -75,24 +75,54 @@ constexpr int64_t kDecodeMaxM = 16;  // M at or below this takes the decode path
 struct Range {
   uintptr_t lo, hi;
 };
+//
+// A decode call whose finishing kernel lets dependents launch before it has
+// waited for its own predecessor (`early_dependents`) relies on the next
+// call's stream CTAs being too large to share an SM with its stream CTAs
+// (which fill every SM), so that the call before it has completed by the time
+// the next call's CTAs run.  That holds only for a decode call after it; any
+// other call after it waits for it in full.
 struct PrevCall {
   bool linear = false;  // a linear call (its kernels let dependents start early)
+  bool early_dependents = false;  // a decode call that let dependents launch before its own wait
   std::vector<Range> writes, reads;
   int decode_half = 0;  // workspace half of the stream's last decode call
 };
+// Keyed by (device, stream): the legacy and per-thread default stream handles
+// are the same value on every device.
+struct StreamKey {
+  int dev;
+  cudaStream_t st;
+  bool operator==(const StreamKey &o) const { return dev == o.dev && st == o.st; }
+};
+struct StreamKeyHash {
+  size_t operator()(const StreamKey &k) const {
+    return std::hash<const void *>()(static_cast<const void *>(k.st)) * 31u + (size_t)k.dev;
+  }
+};
 std::mutex g_prev_mu;
-std::unordered_map<cudaStream_t, PrevCall> g_prev;
+std::unordered_map<StreamKey, PrevCall, StreamKeyHash> g_prev;
+
+StreamKey key_of(cudaStream_t st) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return StreamKey{dev, st};
+}
 
 Range range(const void *p, size_t bytes) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p);
   return Range{a, a + bytes};
 }
 
+// True if early modes are allowed after the stream's previous call for a call
+// of the given kind (see PrevCall).
+bool early_ok(const PrevCall &pc, bool decode_next) { return pc.linear && (decode_next || !pc.early_dependents); }
+
 // True if the stream's previous call was a linear call whose writes miss all of `reads`.
-bool reads_clear_of_previous(cudaStream_t st, const std::vector<Range> &reads) {
+bool reads_clear_of_previous(cudaStream_t st, const std::vector<Range> &reads, bool decode_next = false) {
   std::lock_guard<std::mutex> lock(g_prev_mu);
-  auto it = g_prev.find(st);
-  if (it == g_prev.end() || !it->second.linear) return false;
+  auto it = g_prev.find(key_of(st));
+  if (it == g_prev.end() || !early_ok(it->second, decode_next)) return false;
   for (const Range &r : reads)
     for (const Range &w : it->second.writes)
       if (r.lo < w.hi && w.lo < r.hi) return false;
@@ -101,10 +131,10 @@ bool reads_clear_of_previous(cudaStream_t st, const std::vector<Range> &reads) {
 
 // True if the stream's previous call was a linear call that neither reads
 // nor writes any of `writes`.
-bool writes_clear_of_previous(cudaStream_t st, const std::vector<Range> &writes) {
+bool writes_clear_of_previous(cudaStream_t st, const std::vector<Range> &writes, bool decode_next = false) {
   std::lock_guard<std::mutex> lock(g_prev_mu);
-  auto it = g_prev.find(st);
-  if (it == g_prev.end() || !it->second.linear) return false;
+  auto it = g_prev.find(key_of(st));
+  if (it == g_prev.end() || !early_ok(it->second, decode_next)) return false;
   for (const Range &r : writes) {
     for (const Range &w : it->second.writes)
       if (r.lo < w.hi && w.lo < r.hi) return false;
@@ -114,10 +144,12 @@ bool writes_clear_of_previous(cudaStream_t st, const std::vector<Range> &writes)
   return true;
 }
 
-void note_call(cudaStream_t st, bool linear, std::vector<Range> writes, std::vector<Range> reads = {}) {
+void note_call(cudaStream_t st, bool linear, std::vector<Range> writes, std::vector<Range> reads = {},
+               bool early_dependents = false) {
   std::lock_guard<std::mutex> lock(g_prev_mu);
-  PrevCall &pc = g_prev[st];
+  PrevCall &pc = g_prev[key_of(st)];
   pc.linear = linear;
+  pc.early_dependents = early_dependents;
   pc.writes = std::move(writes);
   pc.reads = std::move(reads);
 }
@@ -126,7 +158,7 @@ void note_call(cudaStream_t st, bool linear, std::vector<Range> writes, std::vec
 // workspace, so a call never writes the half its predecessor may still use.
 int next_ws_half(cudaStream_t st) {
   std::lock_guard<std::mutex> lock(g_prev_mu);
-  PrevCall &pc = g_prev[st];
+  PrevCall &pc = g_prev[key_of(st)];
   pc.decode_half ^= 1;
   return pc.decode_half;
 }
@@ -173,19 +205,22 @@ int linear_fwd(const LinearArgs &a) {
     d.half = next_ws_half(a.stream);
     std::vector<Range> reads;
     weight_ranges(a.W, reads);
-    d.w_early = reads_clear_of_previous(a.stream, reads);
+    d.w_early = reads_clear_of_previous(a.stream, reads, true);
     const std::vector<Range> xab = {range(a.X, (size_t)(M * K * 2)), range(a.A, (size_t)(K * r * 2)),
                                     range(a.B, (size_t)(r * N * 2))};
-    d.x_early = d.w_early && reads_clear_of_previous(a.stream, xab);
+    d.x_early = d.w_early && reads_clear_of_previous(a.stream, xab, true);
     reads.insert(reads.end(), xab.begin(), xab.end());
     const size_t half = decode_ws_half(N, r);
     const Range wsr = range(static_cast<char *>(a.ws) + (d.half ? half : 0), half);
     std::vector<Range> outs = {range(a.Y, (size_t)(M * N * 2))};
     if (a.XA) outs.push_back(range(a.XA, (size_t)(M * r * 2)));
-    d.ws_early = writes_clear_of_previous(a.stream, {wsr});
+    d.ws_early = writes_clear_of_previous(a.stream, {wsr}, true);
     outs.push_back(wsr);
-    note_call(a.stream, true, std::move(outs), std::move(reads));
-    return launch_decode(d, a.stream);
+    bool early_dependents = false;
+    const int rc = launch_decode(d, a.stream, &early_dependents);
+    // recorded even when the launch failed part-way: the next call then waits in full
+    note_call(a.stream, rc == QL_OK, std::move(outs), std::move(reads), early_dependents);
+    return rc;
   }
   QL_TRY(check_common(a, fn, fwd_ws(M, r)));
   cudaStream_t st = a.stream;

@@ -45,6 +45,12 @@ constexpr int kQLanes = 4;
 constexpr int kQBlocksPerStep = 32 / kQLanes;
 constexpr int kQUnroll = 2;  // warp steps in flight per thread
 
+// fma(x, 32, 1.5 * 2^23 + 32) has the bit pattern 0x4B400000 + rne(32 x + 32)
+// for x in [-1, 1]; kCellTop is that of x = 1 (cell 64).  Finite x in [-1, 1]
+// lie at or below it; NaN patterns (either sign) and anything above clamp to it.
+constexpr uint32_t kCellTop = 0x4B400000u + 64u;
+static_assert(kCells == 65, "cells 0..64");
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
@@ -114,8 +120,10 @@ k_quantize(const uint4 *__restrict__ W, int64_t n_blocks, Codebook cb, uint2 *__
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float x = quotient(w[8 * h + e], m, r);
-            // rne(32 x + 32) in the low byte, through the 1.5 * 2^23 rounding constant
-            const uint32_t cu = __float_as_uint(__fmaf_rn(x, 32.0f, 12582944.0f));
+            // rne(32 x + 32) in the low byte, through the 1.5 * 2^23 rounding constant;
+            // the unsigned min keeps the cell index in [0, 64] for any input
+            // (a NaN element gives cell 64 instead of reading past the table)
+            const uint32_t cu = min(__float_as_uint(__fmaf_rn(x, 32.0f, 12582944.0f)), kCellTop);
             uint2 t;
             asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
                          : "=r"(t.x), "=r"(t.y)
@@ -137,8 +145,8 @@ k_quantize(const uint4 *__restrict__ W, int64_t n_blocks, Codebook cb, uint2 *__
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float x = __fdiv_rn(w[8 * h + e], m);
-            const uint32_t cu = __float_as_uint(__fmaf_rn(x, 32.0f, 12582944.0f));
-            const uint2 t = table[((cu & 0x7Fu) << 5) + lane];
+            const uint32_t cu = min(__float_as_uint(__fmaf_rn(x, 32.0f, 12582944.0f)), kCellTop);
+            const uint2 t = table[((cu & 0xFFu) << 5) + lane];
             const uint32_t code = t.y + (x >= __uint_as_float(t.x) ? 1u : 0u);
             o |= code << (8 * (e >> 1) + ((e & 1) ? 0 : 4));
           }
@@ -163,10 +171,10 @@ k_quantize(const uint4 *__restrict__ W, int64_t n_blocks, Codebook cb, uint2 *__
 }
 
 __global__ void __launch_bounds__(256)
-k_double_quant(const float *__restrict__ absmax, int64_t n_b, const double *__restrict__ sum,
+k_double_quant(const float *__restrict__ absmax, int64_t n_b, int64_t total_blocks, const double *__restrict__ sum,
                int8_t *__restrict__ code, float *__restrict__ step, float *__restrict__ mean) {
   __shared__ float red[8];
-  const float mu = __double2float_rn(__ddiv_rn(*sum, (double)n_b));
+  const float mu = __double2float_rn(__ddiv_rn(*sum, (double)total_blocks));
   const int64_t g = blockIdx.x;
   const int64_t i = g * 256 + threadIdx.x;
   const bool valid = i < n_b;
@@ -281,11 +289,11 @@ cudaError_t launch_quantize(const uint16_t *W, int64_t rows, int64_t cols, uint8
   return cudaGetLastError();
 }
 
-cudaError_t launch_double_quant(const float *absmax, int64_t n_b, int dq_bs, const double *sum,
-                                int8_t *code, float *step, float *mean, cudaStream_t st) {
+cudaError_t launch_double_quant(const float *absmax, int64_t n_b, int64_t total_blocks, int dq_bs,
+                                const double *sum, int8_t *code, float *step, float *mean, cudaStream_t st) {
   (void)dq_bs;  // 256, checked by the caller
   const int64_t n_2 = (n_b + 255) / 256;
-  k_double_quant<<<(unsigned)n_2, 256, 0, st>>>(absmax, n_b, sum, code, step, mean);
+  k_double_quant<<<(unsigned)n_2, 256, 0, st>>>(absmax, n_b, total_blocks, sum, code, step, mean);
   count_launch();
   return cudaGetLastError();
 }

@@ -47,6 +47,9 @@ struct GemmArgs {
   uint16_t *out;
   int64_t ldo;
   int *status;
+  // Optional span record (null when off): [0] earliest CTA start after the
+  // dependency wait, [1] latest CTA end, in %globaltimer nanoseconds.
+  unsigned long long *span;
   float q[16];
 };
 
@@ -99,6 +102,25 @@ __device__ __forceinline__ void convert_rowblock(const uint4 &p0, const uint4 &p
   }
 }
 
+// Wait for phase `parity` of a barrier for at most `limit_ns`, ignoring the
+// abort flag (used only after an abort, for work already in flight).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 100000000ull) {
+  const uint64_t t0 = ptx::globaltimer();
+#pragma unroll 1
+  while (!ptx::mbar_try_wait(bar, parity) && ptx::globaltimer() - t0 < limit_ns) {
+  }
+}
+
+// After an abort: a fixed 50 us pause so that tensor copies already issued
+// into shared memory land before the CTA exits (their barriers may never
+// complete, since the other roles stopped arriving on them).
+__device__ __forceinline__ void settle() {
+  const uint64_t t0 = ptx::globaltimer();
+#pragma unroll 1
+  while (ptx::globaltimer() - t0 < 50000ull) {
+  }
+}
+
 __device__ __forceinline__ void zero_row(uint32_t dst) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) ptx::sts128(dst + (j << 4), 0, 0, 0, 0);
@@ -137,11 +159,12 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_u32(smem);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 1);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 2);
   volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
   auto full = [&](int s) { return ptx::smem_u32(&bars[s]); };
   auto empty = [&](int s) { return ptx::smem_u32(&bars[STAGES + s]); };
   const uint32_t accf = ptx::smem_u32(&bars[2 * STAGES]);
+  const uint32_t drainb = ptx::smem_u32(&bars[2 * STAGES + 1]);  // MMAs in flight after an abort
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
@@ -153,6 +176,7 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
       ptx::mbar_init(empty(s), 1);
     }
     ptx::mbar_init(accf, 1);
+    ptx::mbar_init(drainb, 1);
     *abort = 0;
     ptx::fence_mbar_init();
   }
@@ -173,6 +197,7 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
   // previous kernel; its outputs (the LoRA operand) are read only from here on
   ptx::griddep_wait();
   ptx::griddep_launch();
+  if (p.span && threadIdx.x == 0) atomicMin(p.span, (unsigned long long)ptx::globaltimer());
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
@@ -230,7 +255,12 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         }
         ptx::mma_commit(empty(s));
       }
-      if (ok) ptx::mma_commit(accf);
+      if (ok) {
+        ptx::mma_commit(accf);
+      } else {  // gave up: let the MMAs already issued finish before TMEM is freed
+        ptx::mma_commit(drainb);
+        drain_wait(drainb, 0);
+      }
     }
   } else {
     // ---------------------------------------------------------------- converters
@@ -315,8 +345,11 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
       }
     }
   }
+  // after an abort, copies already issued into the ring are given time to land
+  if (*abort && threadIdx.x == 0) settle();
   ptx::tc_fence_before();
   __syncthreads();
+  if (p.span && threadIdx.x == 0) atomicMax(p.span + 1, (unsigned long long)ptx::globaltimer());
   if (warp == 1) ptx::tmem_dealloc(tmem, TMEM_COLS);
 }
 
@@ -362,11 +395,12 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_u32(smem);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + PSTAGES * G::STAGE_BYTES);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * PSTAGES + 1);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * PSTAGES + 2);
   volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
   auto full = [&](int s) { return ptx::smem_u32(&bars[s]); };
   auto empty = [&](int s) { return ptx::smem_u32(&bars[PSTAGES + s]); };
   const uint32_t accf = ptx::smem_u32(&bars[2 * PSTAGES]);
+  const uint32_t drainb = ptx::smem_u32(&bars[2 * PSTAGES + 1]);  // MMAs in flight after an abort
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t crank = ptx::cluster_ctarank();
@@ -380,6 +414,7 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       ptx::mbar_init(empty(s), 1);
     }
     ptx::mbar_init(accf, 1);
+    ptx::mbar_init(drainb, 1);
     *abort = 0;
     ptx::fence_mbar_init();
   }
@@ -401,6 +436,7 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   // previous kernel; its outputs (the LoRA operand) are read only from here on
   ptx::griddep_wait();
   ptx::griddep_launch();
+  if (p.span && threadIdx.x == 0) atomicMin(p.span, (unsigned long long)ptx::globaltimer());
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
@@ -458,7 +494,12 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
         ptx::mma_commit_pair(empty(s));
       }
-      if (ok) ptx::mma_commit_pair(accf);
+      if (ok) {
+        ptx::mma_commit_pair(accf);
+      } else {  // gave up: let the MMAs already issued finish before TMEM is freed
+        ptx::mma_commit_pair(drainb);
+        drain_wait(drainb, 0);
+      }
     }
   } else {
     // ---------------------------------------------------------------- converters
@@ -532,8 +573,11 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       }
     }
   }
+  // after an abort, copies already issued into the ring are given time to land
+  if (*abort && threadIdx.x == 0) settle();
   ptx::tc_fence_before();
   __syncthreads();
+  if (p.span && threadIdx.x == 0) atomicMax(p.span + 1, (unsigned long long)ptx::globaltimer());
   ptx::cluster_sync();
   if (warp == 1) ptx::tmem_dealloc_pair(tmem, G::TMEM_COLS);
 }
@@ -573,7 +617,7 @@ int make_tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer, 
 namespace {
 
 template <bool kTrans, int NACC>
-int launch_pair(const GemmProblem &g, cudaStream_t st) {
+int launch_pair(const GemmProblem &g, unsigned long long *span, cudaStream_t st) {
   using Gm = pairk::Geo<NACC>;
   static bool attr_done[64] = {};
   int dev = 0;
@@ -601,6 +645,7 @@ int launch_pair(const GemmProblem &g, cudaStream_t st) {
   a.out = g.out;
   a.ldo = g.Nout;
   a.status = device_status_ptr();
+  a.span = span;
   const Codebook &cb = codebook();
   for (int i = 0; i < 16; ++i) a.q[i] = cb.q[i];
   dim3 grid((unsigned)(2 * ((g.Nout + 255) / 256)), (unsigned)((g.M + NACC * 256 - 1) / (NACC * 256)));
@@ -620,7 +665,7 @@ int launch_pair(const GemmProblem &g, cudaStream_t st) {
 }
 
 template <bool kTrans>
-int launch(const GemmProblem &g, cudaStream_t st) {
+int launch(const GemmProblem &g, unsigned long long *span, cudaStream_t st) {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -647,6 +692,7 @@ int launch(const GemmProblem &g, cudaStream_t st) {
   a.out = g.out;
   a.ldo = g.Nout;
   a.status = device_status_ptr();
+  a.span = span;
   const Codebook &cb = codebook();
   for (int i = 0; i < 16; ++i) a.q[i] = cb.q[i];
   dim3 grid((unsigned)((g.Nout + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM));
@@ -673,20 +719,36 @@ struct Timing {
 };
 thread_local Timing g_timing;
 
+// Span records of the GEMM launches (ql_spans_start / ql_spans_stop).
+struct Spans {
+  bool on = false;
+  unsigned long long *buf = nullptr;
+  int capacity = 0, used = 0;
+  double flops = 0.0;
+};
+thread_local Spans g_spans;
+
 }  // namespace
 
 int launch_nf4_gemm(const GemmProblem &g, cudaStream_t st) {
   Timing &t = g_timing;
   const bool timed = t.on && t.used < t.capacity;
   if (timed) cudaEventRecord(t.ev[2 * t.used], st);
+  Spans &sp = g_spans;
+  unsigned long long *span = (sp.on && sp.used < sp.capacity) ? sp.buf + 2 * sp.used : nullptr;
   int rc;
-  if (g.M <= 128) rc = g.trans ? launch<true>(g, st) : launch<false>(g, st);
-  else if (g.M <= 256) rc = g.trans ? launch_pair<true, 1>(g, st) : launch_pair<false, 1>(g, st);
-  else rc = g.trans ? launch_pair<true, 2>(g, st) : launch_pair<false, 2>(g, st);
+  if (g.M <= 128) rc = g.trans ? launch<true>(g, span, st) : launch<false>(g, span, st);
+  else if (g.M <= 256) rc = g.trans ? launch_pair<true, 1>(g, span, st) : launch_pair<false, 1>(g, span, st);
+  else rc = g.trans ? launch_pair<true, 2>(g, span, st) : launch_pair<false, 2>(g, span, st);
+  const double flops = 2.0 * (double)g.M * (double)g.Nout * (double)(g.Kred + g.r);
   if (timed && rc == QL_OK) {
     cudaEventRecord(t.ev[2 * t.used + 1], st);
-    t.flops[t.used] = 2.0 * (double)g.M * (double)g.Nout * (double)(g.Kred + g.r);
+    t.flops[t.used] = flops;
     ++t.used;
+  }
+  if (span && rc == QL_OK) {
+    ++sp.used;
+    sp.flops += flops;
   }
   return rc;
 }
@@ -731,4 +793,29 @@ extern "C" int ql_timing_stop(float *total_ms, int *launches, double *flops) {
   if (flops) *flops = fl;
   t = Timing{};
   return rc;
+}
+
+extern "C" int ql_spans_start(uint64_t *device_buffer, int capacity) {
+  using namespace ql;
+  Spans &sp = g_spans;
+  if (sp.on) return set_error(QL_ERR_INVALID, "ql_spans_start: span recording already on");
+  if (!device_buffer || capacity <= 0)
+    return set_error(QL_ERR_INVALID, "ql_spans_start: null buffer or capacity %d", capacity);
+  if (reinterpret_cast<uintptr_t>(device_buffer) & 7)
+    return set_error(QL_ERR_MISALIGNED, "ql_spans_start: buffer not 8-byte aligned");
+  sp = Spans{};
+  sp.on = true;
+  sp.buf = reinterpret_cast<unsigned long long *>(device_buffer);
+  sp.capacity = capacity;
+  return QL_OK;
+}
+
+extern "C" int ql_spans_stop(int *launches, double *flops) {
+  using namespace ql;
+  Spans &sp = g_spans;
+  if (!sp.on) return set_error(QL_ERR_INVALID, "ql_spans_stop: span recording is off");
+  if (launches) *launches = sp.used;
+  if (flops) *flops = sp.flops;
+  sp = Spans{};
+  return QL_OK;
 }

@@ -31,6 +31,8 @@ _SIGNATURES = {
     "ql_nf4_codebook": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float)]),
     "nf4_quantize": (ctypes.c_int, [_c_p, ctypes.POINTER(NF4Struct), _c_p, _c_sz, _c_p]),
     "nf4_quantize_noalloc": (ctypes.c_int, [_c_p, ctypes.POINTER(NF4Struct), _c_p]),
+    "nf4_quantize_shard_begin": (ctypes.c_int, [_c_p, ctypes.POINTER(NF4Struct), _c_p, _c_sz, _c_p]),
+    "nf4_quantize_shard_end": (ctypes.c_int, [ctypes.POINTER(NF4Struct), _c_p, _c_sz, _c_i64, _c_p]),
     "nf4_dequantize": (ctypes.c_int, [ctypes.POINTER(NF4Struct), _c_p, _c_p]),
     "qlora_linear_fwd": (ctypes.c_int, [_c_p, _c_i64, ctypes.POINTER(NF4Struct), _c_p, _c_p, _c_i32,
                                         _c_f32, _c_p, _c_p, _c_p, _c_sz, _c_p]),
@@ -43,6 +45,8 @@ _SIGNATURES = {
     "ql_timing_start": (ctypes.c_int, [ctypes.c_int]),
     "ql_timing_stop": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int),
                                       ctypes.POINTER(ctypes.c_double)]),
+    "ql_spans_start": (ctypes.c_int, [_c_p, ctypes.c_int]),
+    "ql_spans_stop": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_double)]),
 }
 
 
@@ -131,6 +135,25 @@ def timing_stop():
     return float(ms.value), int(n.value), float(fl.value)
 
 
+def spans_start(buf):
+    """Record the first-start / last-end %globaltimer of the next len(buf) // 2
+    tensor-core GEMM launches into the int64 CUDA tensor `buf` (see
+    ql_spans_start); the pairs are initialised here on the current stream."""
+    if buf.dtype != torch.int64 or not buf.is_cuda or buf.numel() % 2:
+        raise ValueError("buf must be an even-length int64 CUDA tensor")
+    v = buf.view(-1, 2)
+    v[:, 0].fill_(-1)  # UINT64_MAX as int64
+    v[:, 1].fill_(0)
+    _check(lib.ql_spans_start(_ptr(buf), buf.numel() // 2))
+
+
+def spans_stop():
+    """Returns (recorded launches, their summed algorithmic flops)."""
+    n, fl = ctypes.c_int(), ctypes.c_double()
+    _check(lib.ql_spans_stop(ctypes.byref(n), ctypes.byref(fl)))
+    return int(n.value), float(fl.value)
+
+
 def _workspace(nbytes, device, ws):
     if nbytes == 0:
         return None, 0
@@ -196,6 +219,28 @@ def nf4_quantize_noalloc(W, dq_blocksize=256, blocksize=64, out=None, stream=Non
     q = out if out is not None else NF4Tensor.empty(rows, cols, W.device, dq_blocksize, blocksize)
     s = q.struct()
     _check(lib.nf4_quantize_noalloc(_ptr(W), ctypes.byref(s), _stream(stream)))
+    return q
+
+
+def nf4_quantize_shard_begin(W_shard, dq_blocksize=256, blocksize=64, out=None, ws=None, stream=None):
+    """First half of a row-sharded quantization (see include/qlora.h).
+    Returns (q_shard, ws, partial_sum) where partial_sum is a float64 CUDA
+    view of the shard's absmax sum at the head of ws."""
+    _need(W_shard, torch.bfloat16, "W_shard")
+    rows, cols = W_shard.shape
+    q = out if out is not None else NF4Tensor.empty(rows, cols, W_shard.device, dq_blocksize, blocksize)
+    ws, nbytes = _workspace(workspace_size(OP_QUANTIZE, 0, rows, cols, 0), W_shard.device, ws)
+    s = q.struct()
+    _check(lib.nf4_quantize_shard_begin(_ptr(W_shard), ctypes.byref(s), _ptr(ws), nbytes, _stream(stream)))
+    return q, ws, ws[:8].view(torch.float64)
+
+
+def nf4_quantize_shard_end(q, ws, total_blocks, stream=None):
+    """Second half: the double-quant codes of this shard with mu taken from the
+    (all-reduced) sum at the head of ws over `total_blocks` blocks."""
+    s = q.struct()
+    _check(lib.nf4_quantize_shard_end(ctypes.byref(s), _ptr(ws), ws.numel(), int(total_blocks),
+                                      _stream(stream)))
     return q
 
 

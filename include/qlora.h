@@ -148,6 +148,34 @@ QL_API int nf4_quantize(const uint16_t *W, const ql_nf4_tensor *q, void *ws,
 QL_API int nf4_quantize_noalloc(const uint16_t *W, const ql_nf4_tensor *q, ql_stream_t stream);
 
 /*
+ * Row-sharded quantization for data-parallel training (the QLoRA project
+ * page runs multi-GPU finetuning through Accelerate; every rank then holds
+ * the same frozen weight, and may quantize its share of the rows).  Rows are
+ * independent except for the double-quant mean mu = fl32(S / n_b), which
+ * needs the sum S of ALL block absmax values and the total block count n_b.
+ *   nf4_quantize_shard_begin(W_shard, q_shard, ws, ws_bytes, stream):
+ *     q_shard describes this rank's rows (rows_shard x cols); writes the
+ *     packed codes (and, with double quant off, the absmax) and leaves this
+ *     shard's fp64 absmax sum as one double at the head of `ws` (device).
+ *   The caller then replaces that double with the sum over all shards (an
+ *   fp64 all-reduce; each partial sum is exact for real weights, so the
+ *   total is the same in any order and equals the unsharded sum).
+ *   nf4_quantize_shard_end(q_shard, ws, ws_bytes, total_blocks, stream):
+ *     mu = fl32(S / total_blocks); writes this shard's second-level codes,
+ *     steps and mu (nothing to do with double quant off).
+ * The shard's blocks must start on a 256-block group boundary of the whole
+ * tensor (rows_before * cols / 64 a multiple of 256) for its codes and steps
+ * to equal the unsharded ones; the same workspace must be passed to both
+ * calls, with nothing else using it in between.  ws_bytes as for
+ * nf4_quantize on the shard.  nf4_quantize(W, q, ...) is exactly begin + end
+ * with total_blocks = the tensor's own block count.
+ */
+QL_API int nf4_quantize_shard_begin(const uint16_t *W_shard, const ql_nf4_tensor *q_shard, void *ws,
+                                    size_t ws_bytes, ql_stream_t stream);
+QL_API int nf4_quantize_shard_end(const ql_nf4_tensor *q_shard, void *ws, size_t ws_bytes,
+                                  int64_t total_blocks, ql_stream_t stream);
+
+/*
  * Dequantize to bf16 (the weight the linear layer computes with).
  *   q     : host struct of device inputs; W_out : rows x cols bf16 (device).
  */
@@ -209,6 +237,26 @@ QL_API int ql_get_device_status(ql_stream_t stream);
  */
 QL_API int ql_timing_start(int capacity);
 QL_API int ql_timing_stop(float *total_ms, int *launches, double *flops);
+
+/*
+ * Optional span record of the tensor-core GEMM launches, off by default (no
+ * counterpart in the pages: it measures the library's own kernels inside a
+ * running sequence of calls, where event records between launches would
+ * stop the programmatic overlap of consecutive kernels).
+ * ql_spans_start(buf, capacity): from now on, tensor-core GEMM launch i that
+ *   this host thread makes (i < capacity) records into the caller's DEVICE
+ *   buffer `buf` (2 * capacity uint64, 8-byte aligned): buf[2i] = the
+ *   earliest %globaltimer (ns) at which one of its CTAs passed its dependency
+ *   wait (atomic min), buf[2i + 1] = the latest at which one finished (atomic
+ *   max).  The caller sets buf[2i] = UINT64_MAX and buf[2i + 1] = 0 first.
+ * ql_spans_stop(launches, flops): turns recording off and writes the number
+ *   of recorded launches and their summed algorithmic flops
+ *   (2 M N_out (K_red + r) each) to host memory.  The caller reads `buf`
+ *   once the launches have completed.
+ * Each recording CTA adds two global atomics; nothing else changes.
+ */
+QL_API int ql_spans_start(uint64_t *device_buffer, int capacity);
+QL_API int ql_spans_stop(int *launches, double *flops);
 
 /*
  * Self-test of the failure path (no counterpart in the pages: it checks the

@@ -59,6 +59,23 @@ def lora_backward(dY, X, W_hat, A, B, s):
     return dX, dA, dB, G
 
 
+def lora_xa(X, A):
+    """XA = X A in fp64: the adapter's down-projection on its own (no weight)."""
+    X, A = map(as_f64, (X, A))
+    return X @ A
+
+
+def lora_adapter_grads(dY, X, A, B, s):
+    """The adapter gradients on their own, without the frozen weight, in fp64:
+    G = dY B^T, dA = s X^T G, dB = s (X A)^T dY.  Returns (dA, dB, XA).
+    Pinned separately from lora_backward by finite differences of <Y, dY>."""
+    dY, X, A, B = map(as_f64, (dY, X, A, B))
+    s = float(s)
+    XA = X @ A
+    G = dY @ B.T
+    return s * (X.T @ G), s * (XA.T @ dY), XA
+
+
 def merged_weight(W_hat, A, B, s):
     """W' = W_hat + s (A B)^T: the merged dense weight (fp64)."""
     W_hat, A, B = map(as_f64, (W_hat, A, B))

@@ -188,7 +188,23 @@ def double_quantize(absmax, dq_blocksize=DQ_BLOCKSIZE):
     a = np.asarray(absmax, dtype=np.float32).reshape(-1)
     n_b = a.size
     S, exact = exact_sum_f64(a)
-    mean = np.float32(S / float(n_b))
+    mean = dq_mean_from_sum(S, n_b)
+    code, step = double_quantize_codes(a, mean, dq_blocksize)
+    return code, step, mean, exact
+
+
+def dq_mean_from_sum(S, n_b):
+    """mu = fl32(S / n_b): the fp64 sum of all block absmax values over their count (R5)."""
+    return np.float32(float(S) / float(n_b))
+
+
+def double_quantize_codes(absmax, mean, dq_blocksize=DQ_BLOCKSIZE):
+    """The second-level codes and steps of consecutive block absmax values,
+    given the mean mu (R5): groups of dq_blocksize start at the first value.
+    Returns (code int8[n], step float32[ceil(n / dq_blocksize)])."""
+    a = np.asarray(absmax, dtype=np.float32).reshape(-1)
+    n_b = a.size
+    mean = np.float32(mean)
     c = (a - mean).astype(np.float32)
     n_2 = (n_b + dq_blocksize - 1) // dq_blocksize
     code = np.zeros(n_b, dtype=np.int8)
@@ -202,7 +218,7 @@ def double_quantize(absmax, dq_blocksize=DQ_BLOCKSIZE):
             continue
         r = np.rint((cg / st).astype(np.float32))
         code[g * dq_blocksize:(g + 1) * dq_blocksize] = np.clip(r, -127, 127).astype(np.int8)
-    return code, step, mean, exact
+    return code, step
 
 
 def double_dequantize(code, step, mean, dq_blocksize=DQ_BLOCKSIZE):

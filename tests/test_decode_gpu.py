@@ -1,13 +1,17 @@
 """GPU parity of the decode-sized forward (M <= 16 tokens) against the fp64
 oracle.  The decode path applies each block constant to fp32 partial sums of
 x * bf16(q[code]) instead of using bf16(q[code] * constant) per weight; the
-difference is one bf16 rounding per weight and stays inside the tolerance
-(relative Frobenius error <= 5e-3, |err| <= 1e-2 (|ref| + rms(ref)))."""
+difference is at most one bf16 step per weight (pinned bit for bit by one-hot
+tokens below) and the outputs stay inside the path's tolerance against the
+oracle on w_hat (relative Frobenius error <= 5e-3,
+|err| <= 1e-2 (|ref| + rms(ref)))."""
 import numpy as np
 import pytest
 import torch
 
 from oracle import linear, nf4
+from oracle.bf16 import bf16_bits_to_f32, f32_to_bf16_bits
+from parity import assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -22,18 +26,6 @@ def ql():
 
 def bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-
-
-def assert_close(name, got, want, rel_fro=5e-3, elem=1e-2):
-    got = np.asarray(got, np.float64)
-    want = np.asarray(want, np.float64)
-    diff = got - want
-    rel = np.linalg.norm(diff) / max(np.linalg.norm(want), 1e-300)
-    rms = np.sqrt(np.mean(want ** 2))
-    worst = np.max(np.abs(diff) / (elem * (np.abs(want) + rms)))
-    assert rel <= rel_fro, f"{name}: relative Frobenius error {rel:.3e}"
-    assert worst <= 1.0, f"{name}: element error {worst:.3f} of the bound"
-    return rel
 
 
 def run(ql, W, X, A, B, s, dq=256):
@@ -66,8 +58,8 @@ def test_decode_ragged_shapes(ql, N, K, M, r):
     s = 16.0 / r
     _, Y, XA = run(ql, W, X, A, B, s)
     Yr, XAr = reference(W, X, A, B, s)
-    assert_close("Y", Y.float().cpu().numpy(), Yr)
-    assert_close("XA", XA.float().cpu().numpy(), XAr)
+    assert_close(f"decode Y {N}x{K} M={M} r={r}", Y.float().cpu().numpy(), Yr)
+    assert_close(f"decode XA {N}x{K} M={M} r={r}", XA.float().cpu().numpy(), XAr)
 
 
 def test_decode_double_quant_off(ql):
@@ -78,7 +70,7 @@ def test_decode_double_quant_off(ql):
     B = normal_bf16((16, 512), 0.01, 4)
     _, Y, _ = run(ql, W, X, A, B, 1.0, dq=0)
     Yr, _ = reference(W, X, A, B, 1.0, dq=0)
-    assert_close("Y", Y.float().cpu().numpy(), Yr)
+    assert_close("decode Y dq off", Y.float().cpu().numpy(), Yr)
 
 
 @pytest.mark.parametrize("M", [1, 4, 16])
@@ -91,8 +83,8 @@ def test_decode_llama13b_full_size(ql, idx, M):
     X, A, B, _ = case_inputs(case)
     _, Y, XA = run(ql, W, X, A, B, case.scale)
     Yr, XAr = reference(W, X, A, B, case.scale)
-    assert_close("Y", Y.float().cpu().numpy(), Yr)
-    assert_close("XA", XA.float().cpu().numpy(), XAr)
+    assert_close(f"decode Y llama13b {case.N}x{case.K} M={M}", Y.float().cpu().numpy(), Yr)
+    assert_close(f"decode XA llama13b {case.N}x{case.K} M={M}", XA.float().cpu().numpy(), XAr)
 
 
 def test_decode_is_deterministic_and_repeatable(ql):
@@ -174,3 +166,44 @@ def test_decode_graph_replays_reuse_the_workspace(ql):
         ql.device_status()
         for (Y, XA), (Ye, XAe) in zip(outs, eager):
             assert torch.equal(Y, Ye) and torch.equal(XA, XAe)
+
+
+@pytest.mark.parametrize("dq", [256, 0])
+@pytest.mark.parametrize("M", [16, 1])
+def test_decode_weight_values_one_hot(ql, M, dq):
+    """The decode path's per-weight value, read out bit for bit: with B = 0 and
+    one-hot token rows, Y[m, n] is the decode weight of (n, k_m), i.e.
+    bf16(fl32(bf16(q[c]) * m_hat)) -- the block constant applied in fp32 to
+    the bf16-rounded level -- and it lies within one bf16 step of the
+    oracle's w_hat = bf16(fl32(q[c] * m_hat))."""
+    from bit_nf4_quantized_38_b300.workloads import normal_with_outliers_bf16
+    dev = torch.device("cuda")
+    N, K, r = 264, 512, 8
+    W = normal_with_outliers_bf16((N, K), 0.02, 0.001, 20.0, 81 + dq)
+    ref = nf4.quantize(bits(W), dq_blocksize=dq)
+    Wh = nf4.dequantize(ref)
+    codes = nf4.unpack_nibbles(ref["packed"]).reshape(N, K)
+    mh = np.repeat(nf4.absmax_hat(ref).reshape(N, K // 64), 64, axis=1)
+    lv = bf16_bits_to_f32(f32_to_bf16_bits(nf4.nf4_levels()))
+    expect = f32_to_bf16_bits((lv[codes] * mh).astype(np.float32))
+    q = ql.nf4_quantize(W.to(dev), dq_blocksize=dq)
+    A = torch.randn(K, r, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16).to(dev)
+    Bz = torch.zeros(r, N, dtype=torch.bfloat16, device=dev)
+    ks = np.arange(K) if M == 16 else np.array([0, 1, 63, 64, 200, 255, 256, 511])
+    got = np.empty((ks.size, N), dtype=np.uint16)
+    for i0 in range(0, ks.size, M):
+        sel = ks[i0:i0 + M]
+        X = torch.zeros(M, K, dtype=torch.bfloat16)
+        X[torch.arange(sel.size), torch.from_numpy(sel)] = 1.0
+        Y, _ = ql.qlora_linear_fwd(X.to(dev), q, A, Bz, 2.0)
+        got[i0:i0 + sel.size] = bits(Y)[:sel.size]
+    torch.cuda.synchronize()
+    ql.device_status()
+    assert np.array_equal(got, expect.T[ks])
+    # adjacent or equal bf16 values of one sign: bit patterns at most 1 apart
+    wh = Wh.T[ks].astype(np.int32)
+    g = got.astype(np.int32)
+    assert np.all((g >> 15) == (wh >> 15))
+    steps = np.abs(g - wh)
+    assert steps.max() <= 1
+    print(f"decode weights one bf16 step from w_hat: {np.mean(steps):.4f} of {steps.size}")

@@ -47,6 +47,31 @@ def test_backward_matches_central_finite_differences(seed):
         assert np.allclose(fd, grad, rtol=1e-10, atol=1e-10), name
 
 
+@pytest.mark.parametrize("seed", [3, 4])
+def test_adapter_grads_alone_match_central_finite_differences(seed):
+    """lora_adapter_grads (no weight argument) against finite differences of
+    the full layer's loss in A and B, and lora_xa against one-hot X rows."""
+    X, W, A, B, R = _tiny(seed, M=4, K=64, N=6, r=3)
+    s = 1.25
+    dA, dB, XA = linear.lora_adapter_grads(R, X, A, B, s)
+    h = 0.5
+    for name, P, grad in (("A", A, dA), ("B", B, dB)):
+        fd = np.zeros_like(P)
+        for idx in np.ndindex(P.shape):
+            Pp = P.copy(); Pp[idx] += h
+            Pm = P.copy(); Pm[idx] -= h
+            if name == "A":
+                lp, lm = _loss(X, W, Pp, B, R, s), _loss(X, W, Pm, B, R, s)
+            else:
+                lp, lm = _loss(X, W, A, Pp, R, s), _loss(X, W, A, Pm, R, s)
+            fd[idx] = (lp - lm) / (2 * h)
+        assert np.allclose(fd, grad, rtol=1e-10, atol=1e-10), name
+    # XA: one-hot token rows read out rows of A
+    E = np.zeros((3, 64)); E[np.arange(3), [1, 17, 63]] = 1.0
+    assert np.array_equal(linear.lora_xa(E, A), A[[1, 17, 63]])
+    assert np.allclose(XA, linear.lora_xa(X, A), rtol=0, atol=0)
+
+
 def test_frozen_weight_gets_no_gradient_and_dW_would_be_nonzero():
     # dX uses W; W itself receives nothing (only dX, dA, dB are returned)
     X, W, A, B, R = _tiny(2)
