@@ -6,6 +6,7 @@
 
 #include "common.cuh"
 #include "linear.cuh"
+#include "merge.cuh"
 
 namespace ql {
 
@@ -50,6 +51,8 @@ int check_tensor(const ql_nf4_tensor *q, const char *fn, bool need_absmax_dq_off
   if (q->dq_blocksize != 0 && q->dq_blocksize != 256)
     return set_error(QL_ERR_UNSUPPORTED, "%s: dq_blocksize %d (only 0 or 256)", fn, q->dq_blocksize);
   if (q->cols % 64) return set_error(QL_ERR_UNSUPPORTED, "%s: cols %lld not a multiple of 64", fn, (long long)q->cols);
+  if (q->quant_type != QL_NF4 && q->quant_type != QL_FP4)
+    return set_error(QL_ERR_UNSUPPORTED, "%s: quant_type %d (0 = NF4, 1 = FP4)", fn, q->quant_type);
   if (!q->packed) return set_error(QL_ERR_INVALID, "%s: null packed", fn);
   if (!aligned(q->packed, 16)) return set_error(QL_ERR_MISALIGNED, "%s: packed not 16-byte aligned", fn);
   if (q->dq_blocksize) {
@@ -126,7 +129,8 @@ int quantize_first(const uint16_t *W, const ql_nf4_tensor *q, void *ws, size_t w
   float *absmax = q->dq_blocksize ? reinterpret_cast<float *>(static_cast<char *>(ws) + 256) : q->absmax;
   rc = check_cuda(cudaMemsetAsync(sum, 0, sizeof(double), st), "quantize: clear sum");
   if (rc) return rc;
-  return check_cuda(launch_quantize(W, q->rows, q->cols, q->packed, absmax, sum, st), "quantize: launch");
+  return check_cuda(launch_quantize(W, q->rows, q->cols, q->quant_type, q->packed, absmax, sum, st),
+                    "quantize: launch");
 }
 
 // Second level: mu = fl32(S / total_blocks) from the fp64 sum at the
@@ -210,4 +214,23 @@ extern "C" int qlora_linear_bwd(const uint16_t *dY, const uint16_t *X, const uin
   a.dX = dX; a.dA = dA; a.dB = dB; a.ws = ws; a.ws_bytes = ws_bytes;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   return linear_bwd(a);
+}
+
+extern "C" int qlora_merge(const ql_nf4_tensor *W, const uint16_t *A, const uint16_t *B, int32_t r, float scale,
+                           uint16_t *W_out, ql_stream_t stream) {
+  g_msg[0] = 0;
+  const char *fn = "qlora_merge";
+  int rc = check_tensor(W, fn, true);
+  if (rc) return rc;
+  if (!A || !B || !W_out) return set_error(QL_ERR_INVALID, "%s: null A, B or W_out", fn);
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(W_out, 16))
+    return set_error(QL_ERR_MISALIGNED, "%s: A, B or W_out not 16-byte aligned", fn);
+  if (r != 8 && r != 16 && r != 32 && r != 64 && r != 128)
+    return set_error(QL_ERR_UNSUPPORTED, "%s: rank %d (8, 16, 32, 64 or 128)", fn, r);
+  if (W->rows % 8) return set_error(QL_ERR_UNSUPPORTED, "%s: N = %lld not a multiple of 8", fn, (long long)W->rows);
+  if (W->rows > ((int64_t)1 << 30) || W->cols > ((int64_t)1 << 30))
+    return set_error(QL_ERR_UNSUPPORTED, "%s: dimension above 2^30", fn);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  note_other_call(st);
+  return launch_merge(*W, A, B, r, scale, W_out, st);
 }

@@ -25,10 +25,21 @@ struct Codebook {
   // code(x) = cell_lo[c] + (x >= cell_u[c]).
   float cell_u[kCells];  // smallest fp32 above the cell's threshold (or +inf)
   int32_t cell_lo[kCells];
+  // For the quantizer's division-free test: x = RN(w / m) >= u exactly when
+  // w - m t' > 0, t' = (pred(u) + u) / 2 the rounding boundary below u (no
+  // quotient of two bf16 values equals t').  t' = u - delta with delta a
+  // power of two; cell_d holds delta's bits with cell_lo + 1 in its five low
+  // mantissa bits (the perturbation, under 2^-18 delta, never changes the
+  // sign of w - m u + m delta for bf16 w, m).  Cells without a threshold
+  // hold delta = 2^-30.
+  uint32_t cell_d[kCells];
+  // True when no quotient w / m of two normal bf16 values lies in [t', u)
+  // for any threshold: then w - m u >= 0 alone decides (one FMA, no delta).
+  bool one_fma;
 };
 
-// Host: the codebook (built once, thread-safe).
-const Codebook &codebook();
+// Host: the code table of a quant type (QL_NF4 or QL_FP4; built once, thread-safe).
+const Codebook &codebook(int quant_type = QL_NF4);
 
 // ---------------------------------------------------------------------------
 // errors
@@ -58,7 +69,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // ---------------------------------------------------------------------------
 // launchers (quant.cu)
 
-cudaError_t launch_quantize(const uint16_t *W, int64_t rows, int64_t cols, uint8_t *packed,
+cudaError_t launch_quantize(const uint16_t *W, int64_t rows, int64_t cols, int quant_type, uint8_t *packed,
                             float *absmax, double *sum_acc, cudaStream_t st);
 // mu = fl32(sum / total_blocks); codes and steps of the n_b blocks given.
 cudaError_t launch_double_quant(const float *absmax, int64_t n_b, int64_t total_blocks, int dq_bs,

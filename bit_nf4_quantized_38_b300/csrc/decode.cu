@@ -870,7 +870,7 @@ int launch_decode(const DecodeProblem &p, cudaStream_t st, bool *early_dependent
   a.xap = reinterpret_cast<float *>(ws);
   a.slots = reinterpret_cast<float *>(ws + l.slots);
   a.status = device_status_ptr();
-  const Codebook &cb = codebook();
+  const Codebook &cb = codebook(p.w.qt);
   for (int i = 0; i < 16; ++i) a.q[i] = cb.q[i];
   // every CTA gets at least one unit, so the CTAs of a row group are consecutive
   const int G = (int)std::min<int64_t>(std::min(di.sms, G_MAX), a.W);

@@ -235,6 +235,9 @@ int linear_fwd(const LinearArgs &a) {
   reads.push_back(range(a.B, (size_t)(r * N * 2)));
   weight_ranges(a.W, reads);
   const bool early = reads_clear_of_previous(st, reads);
+  std::vector<Range> main_reads = {range(a.X, (size_t)(M * K * 2))};
+  weight_ranges(a.W, main_reads);
+  const bool gemm_early = reads_clear_of_previous(st, main_reads);
   const bool free_ = reads_clear_of_previous(st, xa_reads) && writes_clear_of_previous(st, xa_writes);
   std::vector<Range> writes = xa_writes;
   writes.push_back(range(a.Y, (size_t)(M * N * 2)));
@@ -252,6 +255,7 @@ int linear_fwd(const LinearArgs &a) {
   g.A2 = xas; g.B2 = a.B; g.r = r;
   g.w = nf4_view(a.W);
   g.out = a.Y; g.Nout = N;
+  g.early_main = gemm_early;
   return launch_nf4_gemm(g, st);
 }
 
@@ -283,6 +287,9 @@ int linear_bwd(const LinearArgs &a) {
   const bool half_clear = writes_clear_of_previous(st, {range(ws, half)});
   const bool g_early = reads_clear_of_previous(st, dy_b);
   const bool x_early = reads_clear_of_previous(st, x_a);
+  std::vector<Range> main_reads = {range(a.dY, (size_t)(M * N * 2))};
+  weight_ranges(a.W, main_reads);
+  const bool gemm_early = reads_clear_of_previous(st, main_reads);
   note_call(st, true,
             {range(a.dX, (size_t)(M * K * 2)), range(a.dA, (size_t)(K * r * 4)), range(a.dB, (size_t)(r * N * 4)),
              range(ws, half)},
@@ -315,6 +322,7 @@ int linear_bwd(const LinearArgs &a) {
     g.A2 = gs; g.B2 = a.A; g.r = r;
     g.w = nf4_view(a.W);
     g.out = a.dX; g.Nout = K;
+    g.early_main = gemm_early;
     QL_TRY(launch_nf4_gemm(g, st));
   }
   // 3. dA = X^T Gs (X [M][K] and Gs [M][r] read MN-major) and 4. dB = s XA^T dY,

@@ -6,9 +6,10 @@
 //   quantize   reads 2 B/param (bf16), writes 0.5 B/param + 4 B/block absmax
 //   double q.  reads 4 B/block, writes 1 B/block + 4 B per 256 blocks
 //   dequantize reads 0.5 B/param + 1 B/block, writes 2 B/param
-// A warp covers 4 consecutive 64-element blocks per step (8 lanes per block,
-// 16 B of bf16 or 4 B of nibbles per lane), so every load and store is a
-// contiguous, fully used 128-512 B run.
+// Every load and store of a warp is a contiguous, fully used run (the
+// quantizer: 2 lanes per block, 64 B of bf16 in and 16 B of nibbles out per
+// lane; the dequantizer: 8 lanes per block, 4 B of nibbles in and 16 B of
+// bf16 out per lane).
 #include "common.cuh"
 
 namespace ql {
@@ -23,52 +24,92 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
-
-// x = fl32(w / m) for |w| <= m, without a division per element: with
-// r = RN(1/m) and x0 = RN(w r), the residual w - x0 m is exact under FMA and
-// RN(x0 + residual * r) is the correctly rounded quotient (Markstein's
-// correction step for division).  Checked exhaustively over every pair of
-// bf16 values with |w| <= m and m in [2^-60, 2^60]: it equals the IEEE
-// quotient whenever |x| >= 2^-12; smaller quotients (only with subnormal w)
-// may differ in the last bit, but every quotient that small codes to the zero
-// level either way.  Blocks with m outside that range take the IEEE division.
-__device__ __forceinline__ float quotient(float w, float m, float r) {
-  float x0 = __fmul_rn(w, r);
-  float res = __fmaf_rn(-x0, m, w);
-  return __fmaf_rn(res, r, x0);
+// 32 contiguous bytes (a whole sector) in one load; p 32-byte aligned.
+__device__ __forceinline__ void ld_stream32(const uint4 *p, uint4 &a, uint4 &b) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+               : "l"(p));
 }
 
-// Quantizer layout: 4 lanes per 64-element block, 16 consecutive elements
-// (32 bytes of bf16) each, so one warp step covers 8 consecutive blocks
-// (1 KB of W) and writes 8 bytes of nibbles per lane.
-constexpr int kQLanes = 4;
+// Quantizer layout: 2 lanes per 64-element block, 32 consecutive elements
+// (64 bytes of bf16) each, so one warp step covers 16 consecutive blocks
+// (2 KB of W) and every lane writes 16 bytes of nibbles.
+constexpr int kQLanes = 2;
 constexpr int kQBlocksPerStep = 32 / kQLanes;
-constexpr int kQUnroll = 2;  // warp steps in flight per thread
-
-// fma(x, 32, 1.5 * 2^23 + 32) has the bit pattern 0x4B400000 + rne(32 x + 32)
-// for x in [-1, 1]; kCellTop is that of x = 1 (cell 64).  Finite x in [-1, 1]
-// lie at or below it; NaN patterns (either sign) and anything above clamp to it.
-constexpr uint32_t kCellTop = 0x4B400000u + 64u;
-static_assert(kCells == 65, "cells 0..64");
+constexpr int kQCells = 256;                            // table rows: every byte value is a valid index
+constexpr size_t kQTableBytes = (size_t)kQCells * 32 * 8;  // one 8-byte entry per cell and lane
+// fma(x, 32, 1.5 * 2^23 + 32) = 0x4B400000 + rne(32 x + 32) as a bit pattern for x in [-1, 1]
+constexpr float kCellRound = 12582944.0f;
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
 }
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
 
-__global__ void __launch_bounds__(kThreads)
-k_quantize(const uint4 *__restrict__ W, int64_t n_blocks, Codebook cb, uint2 *__restrict__ packed,
+// NF4 code of w in a block with absmax m (2^-60 <= m <= 2^60), without a
+// division.  The coding cell comes from w * (32 / m) with an approximate
+// reciprocal: the cell is either the one of the exact quotient or its
+// neighbour across a boundary no threshold lies near (the host checks that
+// every threshold keeps 2^-16 from every boundary), so either cell decides
+// correctly.  The decision x = RN(w / m) >= u is taken exactly as the sign of
+// (w - m u) + m delta (two FMAs): t' = u - delta is the point where RN
+// switches to u, no quotient of two bf16 values equals it, and near it
+// w - m u is exact.  The result equals the code of the IEEE quotient for
+// every pair of bf16 values with |w| <= m in the range (checked exhaustively
+// on the host, also with the reciprocal perturbed by two ulps either way).
+// kOneFma: no bf16 quotient lies between t' and u for this codebook (the host
+// checks every threshold), so the sign of w - m u alone decides.
+template <bool kOneFma>
+__device__ __forceinline__ uint32_t nf4_code_fast(float w, float m, float r32, uint32_t tbase, uint32_t lane8) {
+  const uint32_t cu = __float_as_uint(__fmaf_rn(w, r32, kCellRound));
+  uint2 t;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(t.x), "=r"(t.y) : "r"(tbase + prmt(cu, lane8, 0x5504u)));
+  const float e = __fmaf_rn(-m, __uint_as_float(t.x), w);
+  const float v = kOneFma ? e : __fmaf_rn(m, __uint_as_float(t.y), e);
+  // lower code + 1 sits in the low five bits of t.y; minus 1 when v < 0
+  return (t.y & 31u) + (uint32_t)((int32_t)__float_as_uint(v) >> 31);
+}
+
+// The same decision from the IEEE quotient (block constants outside [2^-60, 2^60]).
+__device__ __forceinline__ uint32_t nf4_code_ieee(float w, float m, uint32_t tbase, uint32_t lane8) {
+  const float x = __fdiv_rn(w, m);
+  const uint32_t cu = __float_as_uint(__fmaf_rn(x, 32.0f, kCellRound));
+  uint2 t;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(t.x), "=r"(t.y) : "r"(tbase + prmt(cu, lane8, 0x5504u)));
+  return (t.y & 31u) - 1u + (x >= __uint_as_float(t.x) ? 1u : 0u);
+}
+
+// Eight codes (elements 2j in the high nibble of byte j) -> one word.
+__device__ __forceinline__ uint32_t pack8(const uint32_t (&c)[8]) {
+  uint32_t o = c[0] * 16u + c[1];
+  o = (c[2] * 16u + c[3]) * 0x100u + o;
+  o = (c[4] * 16u + c[5]) * 0x10000u + o;
+  return (c[6] * 16u + c[7]) * 0x1000000u + o;
+}
+
+// kWide: W is 32-byte aligned, so a lane's bytes load as whole sectors.
+template <bool kOneFma, bool kWide>
+__global__ void __launch_bounds__(kThreads, 3)
+k_quantize(const uint4 *__restrict__ W, int64_t n_blocks, Codebook cb, uint4 *__restrict__ packed,
            float *__restrict__ absmax, double *__restrict__ sum_acc) {
-  // Coding table, one copy per lane so lookups never conflict on a bank: cell
-  // c, lane l at byte c * 256 + l * 8 (threshold bits, lower code).  The
-  // lookup address comes from one byte permute of the cell index (the low
-  // byte of the rounding-constant sum below) and l * 8.
-  __shared__ __align__(16) uint2 table[kCells * 32];
+  // Coding table, one copy per lane so lookups never conflict on a bank:
+  // cell c, lane l at byte c * 256 + l * 8 (threshold bits, rounding step |
+  // lower code + 1).  The address is one byte permute of the cell index (the
+  // low byte of the rounding-constant sum) and l * 8; all 256 byte values
+  // are rows, so no input (a NaN element included) reads outside the table.
+  // Rows past the last cell hold no threshold and code 7 + 1.
+  extern __shared__ __align__(16) uint2 table[];
   __shared__ double red[kThreads / 32];
-  for (int i = threadIdx.x; i < kCells * 32; i += kThreads) {
+  for (int i = threadIdx.x; i < kQCells * 32; i += kThreads) {
     const int c = i >> 5;
-    table[i] = make_uint2(__float_as_uint(cb.cell_u[c]), (uint32_t)cb.cell_lo[c]);
+    table[i] = c < kCells ? make_uint2(__float_as_uint(cb.cell_u[c]), cb.cell_d[c])
+                          : make_uint2(0x7F800000u, 0x30800000u | 8u);
   }
   __syncthreads();
 
@@ -78,83 +119,72 @@ k_quantize(const uint4 *__restrict__ W, int64_t n_blocks, Codebook cb, uint2 *__
   const uint32_t lane8 = (uint32_t)lane * 8u;
   const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  const int64_t stride = nwarps * kQBlocksPerStep;
   double local = 0.0;
 
-  for (int64_t base = warp * kQBlocksPerStep * kQUnroll; base < n_blocks;
-       base += nwarps * kQBlocksPerStep * kQUnroll) {
-    uint4 v[kQUnroll][2];
+  // A lane's 64 bytes as two whole 32-byte sectors: a load of half a sector
+  // (16 bytes) would fetch the sector from L2 twice when L1 is bypassed.
+  auto load = [&](int64_t base, uint4 (&v)[4]) {
+    const int64_t b = base + lane / kQLanes;
+    if (b < n_blocks && kWide) {
+      ld_stream32(W + b * 8 + sub * 4, v[0], v[1]);
+      ld_stream32(W + b * 8 + sub * 4 + 2, v[2], v[3]);
+    } else if (b < n_blocks) {
 #pragma unroll
-    for (int u = 0; u < kQUnroll; ++u) {
-      const int64_t b = base + u * kQBlocksPerStep + lane / kQLanes;
-      const bool in = b < n_blocks;
-      v[u][0] = in ? ld_stream(W + b * 8 + sub * 2) : make_uint4(0, 0, 0, 0);
-      v[u][1] = in ? ld_stream(W + b * 8 + sub * 2 + 1) : make_uint4(0, 0, 0, 0);
+      for (int k = 0; k < 4; ++k) v[k] = ld_stream(W + b * 8 + sub * 4 + k);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] = make_uint4(0, 0, 0, 0);
     }
+  };
+  uint4 nxt[4];
+  int64_t base = warp * kQBlocksPerStep;
+  if (base < n_blocks) load(base, nxt);
+  for (; base < n_blocks; base += stride) {
+    uint4 v[4];
 #pragma unroll
-    for (int u = 0; u < kQUnroll; ++u) {
-      const int64_t b = base + u * kQBlocksPerStep + lane / kQLanes;
-      float w[16];
-      const uint32_t words[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w,
-                                 v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
+    for (int k = 0; k < 4; ++k) v[k] = nxt[k];
+    if (base + stride < n_blocks) load(base + stride, nxt);
+    const int64_t b = base + lane / kQLanes;
+    float w[32];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        w[2 * i] = bf16lo_to_f32(words[i]);
-        w[2 * i + 1] = bf16hi_to_f32(words[i]);
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t words[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        w[8 * k + 2 * i] = bf16lo_to_f32(words[i]);
+        w[8 * k + 2 * i + 1] = bf16hi_to_f32(words[i]);
       }
-      float m = 0.0f;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(w[e]));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-      if (b >= n_blocks) continue;
-      if (sub == 0) {
-        absmax[b] = m;
-        local += (double)m;
-      }
-      uint32_t out[2] = {0x77777777u, 0x77777777u};  // all-zero block: the zero level everywhere
-      if (m >= 0x1p-60f && m <= 0x1p60f) {
-        const float r = __frcp_rn(m);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t code[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float x = quotient(w[8 * h + e], m, r);
-            // rne(32 x + 32) in the low byte, through the 1.5 * 2^23 rounding constant;
-            // the unsigned min keeps the cell index in [0, 64] for any input
-            // (a NaN element gives cell 64 instead of reading past the table)
-            const uint32_t cu = min(__float_as_uint(__fmaf_rn(x, 32.0f, 12582944.0f)), kCellTop);
-            uint2 t;
-            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
-                         : "=r"(t.x), "=r"(t.y)
-                         : "r"(tbase + prmt(cu, lane8, 0x5504u)));
-            code[e] = t.y + (x >= __uint_as_float(t.x) ? 1u : 0u);
-          }
-          // element 2j -> high nibble of byte j: each byte as 16 hi + lo, the
-          // bytes placed by multiply-adds (the fields never overlap)
-          uint32_t o = code[0] * 16u + code[1];
-          o = (code[2] * 16u + code[3]) * 0x100u + o;
-          o = (code[4] * 16u + code[5]) * 0x10000u + o;
-          o = (code[6] * 16u + code[7]) * 0x1000000u + o;
-          out[h] = o;
-        }
-      } else if (m > 0.0f) {  // constants outside [2^-60, 2^60]: IEEE division
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t o = 0;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float x = __fdiv_rn(w[8 * h + e], m);
-            const uint32_t cu = min(__float_as_uint(__fmaf_rn(x, 32.0f, 12582944.0f)), kCellTop);
-            const uint2 t = table[((cu & 0xFFu) << 5) + lane];
-            const uint32_t code = t.y + (x >= __uint_as_float(t.x) ? 1u : 0u);
-            o |= code << (8 * (e >> 1) + ((e & 1) ? 0 : 4));
-          }
-          out[h] = o;
-        }
-      }
-      packed[b * kQLanes + sub] = make_uint2(out[0], out[1]);
     }
+    float m = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) m = fmaxf(m, fabsf(w[e]));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    if (b >= n_blocks) continue;
+    if (sub == 0) {
+      absmax[b] = m;
+      local += (double)m;
+    }
+    uint32_t out[4] = {0x77777777u, 0x77777777u, 0x77777777u, 0x77777777u};  // all-zero block: zero level
+    if (m >= 0x1p-60f && m <= 0x1p60f) {
+      const float r32 = rcp_approx(m) * 32.0f;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        uint32_t c[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) c[e] = nf4_code_fast<kOneFma>(w[8 * h + e], m, r32, tbase, lane8);
+        out[h] = pack8(c);
+      }
+    } else if (m > 0.0f) {  // block constants outside [2^-60, 2^60]: IEEE division
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        uint32_t c[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) c[e] = nf4_code_ieee(w[8 * h + e], m, tbase, lane8);
+        out[h] = pack8(c);
+      }
+    }
+    packed[b * kQLanes + sub] = make_uint4(out[0], out[1], out[2], out[3]);
   }
 
   // fp64 sum of this CTA's block absmax values (exact for real weights, so the
@@ -256,7 +286,7 @@ int grid_for_q(int64_t n_blocks, int ctas_per_sm) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 148;
   }
-  const int64_t per_cta = (int64_t)kQBlocksPerStep * kQUnroll * (kThreads / 32);
+  const int64_t per_cta = (int64_t)kQBlocksPerStep * (kThreads / 32);
   int64_t need = (n_blocks + per_cta - 1) / per_cta;
   int64_t g = (int64_t)sms * ctas_per_sm;
   if (need < g) g = need;
@@ -279,12 +309,31 @@ int grid_for(int64_t n_blocks, int ctas_per_sm) {
 
 }  // namespace
 
-cudaError_t launch_quantize(const uint16_t *W, int64_t rows, int64_t cols, uint8_t *packed,
+cudaError_t launch_quantize(const uint16_t *W, int64_t rows, int64_t cols, int quant_type, uint8_t *packed,
                             float *absmax, double *sum_acc, cudaStream_t st) {
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !attr_done[dev]) {
+    // the table is the only shared memory the kernel needs; streaming loads bypass L1
+    for (auto fn : {k_quantize<true, true>, k_quantize<false, true>, k_quantize<true, false>,
+                    k_quantize<false, false>}) {
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQTableBytes);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    }
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
   const int64_t n_blocks = rows * cols / 64;
-  k_quantize<<<grid_for_q(n_blocks, 8), kThreads, 0, st>>>(
-      reinterpret_cast<const uint4 *>(W), n_blocks, codebook(), reinterpret_cast<uint2 *>(packed),
-      absmax, sum_acc);
+  const Codebook &cb = codebook(quant_type);
+  const int grid = grid_for_q(n_blocks, 3);
+  const bool wide = (reinterpret_cast<uintptr_t>(W) & 31) == 0;
+  auto fn = cb.one_fma ? (wide ? k_quantize<true, true> : k_quantize<true, false>)
+                       : (wide ? k_quantize<false, true> : k_quantize<false, false>);
+  fn<<<grid, kThreads, kQTableBytes, st>>>(reinterpret_cast<const uint4 *>(W), n_blocks, cb,
+                                           reinterpret_cast<uint4 *>(packed), absmax, sum_acc);
   count_launch();
   return cudaGetLastError();
 }
@@ -305,10 +354,10 @@ cudaError_t launch_dequantize(const ql_nf4_tensor &q, uint16_t *W_out, cudaStrea
   uint4 *o = reinterpret_cast<uint4 *>(W_out);
   if (q.dq_blocksize)
     k_dequantize<true><<<g, kThreads, 0, st>>>(p, n_blocks, q.absmax_code, q.dq_step, q.dq_mean,
-                                               nullptr, codebook(), o);
+                                               nullptr, codebook(q.quant_type), o);
   else
     k_dequantize<false><<<g, kThreads, 0, st>>>(p, n_blocks, nullptr, nullptr, nullptr, q.absmax,
-                                                codebook(), o);
+                                                codebook(q.quant_type), o);
   count_launch();
   return cudaGetLastError();
 }

@@ -50,6 +50,10 @@ struct GemmArgs {
   // Optional span record (null when off): [0] earliest CTA start after the
   // dependency wait, [1] latest CTA end, in %globaltimer nanoseconds.
   unsigned long long *span;
+  // The main-loop operands (A and the weight) are not written by any kernel
+  // that may still run: start the main loop at once and wait for the
+  // previous kernel only before the LoRA steps (pair kernel; see there).
+  int early_main;
   float q[16];
 };
 
@@ -397,6 +401,7 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + PSTAGES * G::STAGE_BYTES);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * PSTAGES + 2);
   volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *dep_seen = reinterpret_cast<volatile int *>(tmem_slot + 2);  // gate CTA: predecessor done
   auto full = [&](int s) { return ptx::smem_u32(&bars[s]); };
   auto empty = [&](int s) { return ptx::smem_u32(&bars[PSTAGES + s]); };
   const uint32_t accf = ptx::smem_u32(&bars[2 * PSTAGES]);
@@ -416,6 +421,7 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     ptx::mbar_init(accf, 1);
     ptx::mbar_init(drainb, 1);
     *abort = 0;
+    *dep_seen = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -432,15 +438,48 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // launched as a programmatic dependent: the setup above overlaps the
-  // previous kernel; its outputs (the LoRA operand) are read only from here on
-  ptx::griddep_wait();
-  ptx::griddep_launch();
+  // Launched as a programmatic dependent of the previous kernel, whose
+  // output (the LoRA operand) is read only after griddep_wait.
+  //  - Default: wait here, then let dependents launch.
+  //  - early_main: the main loop reads only operands no running kernel
+  //    writes, so it starts at once; the producer waits before the first LoRA
+  //    step, and the epilogue (after the last MMA) follows that wait.  This
+  //    GEMM's main loop thus runs in the SMs the previous GEMM's last wave
+  //    leaves idle.  Dependents may launch once every CTA has started, except
+  //    that the gate CTA (block 0, 0) lets them launch only after one of its
+  //    threads has seen the previous kernel complete: so, as with the
+  //    default, no kernel of the next call starts before every kernel older
+  //    than this one's predecessor has completed.  (Each thread of the gate
+  //    CTA triggers only after that wait: idle lanes wait themselves, the
+  //    working roles trigger once they see `dep_seen`.)
+  const bool gate = p.early_main && blockIdx.x == 0 && blockIdx.y == 0;
+  bool triggered = false;
+  if (!p.early_main) {
+    ptx::griddep_wait();
+    ptx::griddep_launch();
+    triggered = true;
+  } else if (!gate) {
+    ptx::griddep_launch();
+    triggered = true;
+  } else if ((warp == 0 && lane != 0) || (warp == 1 && lane != 0)) {
+    ptx::griddep_wait();
+    if (warp == 0 && lane == 1) *dep_seen = 1;
+    ptx::griddep_launch();
+    triggered = true;
+  }
+  // gate CTA, working threads: trigger once the predecessor is known complete
+  auto poll_trigger = [&]() {
+    if (!triggered && *dep_seen) {
+      ptx::griddep_launch();
+      triggered = true;
+    }
+  };
   if (p.span && threadIdx.x == 0) atomicMin(p.span, (unsigned long long)ptx::globaltimer());
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
+      bool waited = !p.early_main;
       for (int ks = 0; ks < nsteps; ++ks) {
         const int s = ks % PSTAGES;
         const uint32_t ph = (ks / PSTAGES) & 1;
@@ -448,6 +487,13 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const uint32_t a_dst = sbase + s * G::STAGE_BYTES;
         const uint32_t lead_full = ptx::mapa(full(s), 0);
         const bool lora = ks >= p.ksteps_main;
+        if (lora && !waited) {  // early_main: the LoRA operand is the previous kernel's output
+          ptx::griddep_wait();
+          waited = true;
+          ptx::griddep_launch();
+          triggered = true;
+        }
+        poll_trigger();
         ptx::mbar_arrive_expect_tx_cluster(lead_full, G::A_BYTES + (lora ? G::B_BYTES : 0));
         const int x = (lora ? ks - p.ksteps_main : ks) * PBK;
 #pragma unroll
@@ -463,6 +509,8 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           }
         }
       }
+      // a CTA that gave up before its LoRA steps still completes after its predecessor
+      if (!waited) ptx::griddep_wait();
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA (even CTA)
@@ -475,6 +523,7 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const uint32_t ph = (ks / PSTAGES) & 1;
         if (!ptx::mbar_wait_cluster(full(s), ph, abort, p.status)) { ok = false; break; }
         ptx::tc_fence_after();
+        poll_trigger();
         const uint32_t a_addr = sbase + s * G::STAGE_BYTES;
         const uint32_t b_addr = a_addr + G::A_BYTES;
         const bool bmn = kTrans != (ks >= p.ksteps_main);
@@ -532,6 +581,7 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       const int s = ks % PSTAGES;
       const uint32_t ph = (ks / PSTAGES) & 1;
       if (ks + 2 < p.ksteps_main) nxt = fetch(ks + 2);
+      poll_trigger();
       if (!ptx::mbar_wait_cluster(empty(s), ph ^ 1, abort, p.status)) break;
       if (ks < p.ksteps_main) {
         const uint32_t b_addr = sbase + s * G::STAGE_BYTES + G::A_BYTES;
@@ -573,6 +623,8 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       }
     }
   }
+  // gate CTA: a thread that has not triggered yet exits only after the predecessor
+  if (!triggered) ptx::griddep_wait();
   // after an abort, copies already issued into the ring are given time to land
   if (*abort && threadIdx.x == 0) settle();
   ptx::tc_fence_before();
@@ -646,7 +698,8 @@ int launch_pair(const GemmProblem &g, unsigned long long *span, cudaStream_t st)
   a.ldo = g.Nout;
   a.status = device_status_ptr();
   a.span = span;
-  const Codebook &cb = codebook();
+  a.early_main = g.early_main ? 1 : 0;
+  const Codebook &cb = codebook(g.w.qt);
   for (int i = 0; i < 16; ++i) a.q[i] = cb.q[i];
   dim3 grid((unsigned)(2 * ((g.Nout + 255) / 256)), (unsigned)((g.M + NACC * 256 - 1) / (NACC * 256)));
   cudaLaunchConfig_t cfg{};
@@ -693,7 +746,7 @@ int launch(const GemmProblem &g, unsigned long long *span, cudaStream_t st) {
   a.ldo = g.Nout;
   a.status = device_status_ptr();
   a.span = span;
-  const Codebook &cb = codebook();
+  const Codebook &cb = codebook(g.w.qt);
   for (int i = 0; i < 16; ++i) a.q[i] = cb.q[i];
   dim3 grid((unsigned)((g.Nout + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM));
   cudaLaunchConfig_t cfg{};

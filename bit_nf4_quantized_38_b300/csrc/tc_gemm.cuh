@@ -15,10 +15,12 @@ struct NF4View {
   const float *absmax;
   int64_t rows, cols;
   int dq;
+  int qt;  // quant type: the code table the codes index
 };
 
 inline NF4View nf4_view(const ql_nf4_tensor &t) {
-  return NF4View{t.packed, t.absmax_code, t.dq_step, t.dq_mean, t.absmax, t.rows, t.cols, t.dq_blocksize != 0};
+  return NF4View{t.packed, t.absmax_code, t.dq_step, t.dq_mean, t.absmax, t.rows, t.cols, t.dq_blocksize != 0,
+                 t.quant_type};
 }
 
 // out[M][Nout] = A[M][Kred] . op(W_hat) + A2[M][r] . op2(B2)
@@ -38,6 +40,10 @@ struct GemmProblem {
   NF4View w;
   uint16_t *out;
   int64_t Nout;
+  // A and the weight are written by no kernel that may still be running
+  // (the previous library call writes neither): the CTA-pair kernel then
+  // starts its main loop before its predecessor completes.
+  bool early_main = false;
 };
 int launch_nf4_gemm(const GemmProblem &g, cudaStream_t st);
 

@@ -14,6 +14,7 @@ import torch
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libqlora.so")
 
 QL_OK, QL_ERR_INVALID, QL_ERR_UNSUPPORTED, QL_ERR_MISALIGNED, QL_ERR_CUDA, QL_ERR_TIMEOUT = range(6)
+QL_NF4, QL_FP4 = 0, 1
 OP_QUANTIZE, OP_DEQUANTIZE, OP_LINEAR_FWD, OP_LINEAR_BWD = range(4)
 
 _c_i64, _c_i32, _c_f32, _c_p, _c_sz = (ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
@@ -23,12 +24,13 @@ _c_i64, _c_i32, _c_f32, _c_p, _c_sz = (ctypes.c_int64, ctypes.c_int32, ctypes.c_
 class NF4Struct(ctypes.Structure):
     _fields_ = [("rows", _c_i64), ("cols", _c_i64), ("blocksize", _c_i32), ("dq_blocksize", _c_i32),
                 ("packed", _c_p), ("absmax", _c_p), ("absmax_code", _c_p), ("dq_step", _c_p),
-                ("dq_mean", _c_p)]
+                ("dq_mean", _c_p), ("quant_type", _c_i32)]
 
 
 _SIGNATURES = {
     "ql_workspace_size": (_c_sz, [ctypes.c_int, _c_i64, _c_i64, _c_i64, _c_i32]),
     "ql_nf4_codebook": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float)]),
+    "ql_codebook": (ctypes.c_int, [_c_i32, ctypes.POINTER(ctypes.c_float)]),
     "nf4_quantize": (ctypes.c_int, [_c_p, ctypes.POINTER(NF4Struct), _c_p, _c_sz, _c_p]),
     "nf4_quantize_noalloc": (ctypes.c_int, [_c_p, ctypes.POINTER(NF4Struct), _c_p]),
     "nf4_quantize_shard_begin": (ctypes.c_int, [_c_p, ctypes.POINTER(NF4Struct), _c_p, _c_sz, _c_p]),
@@ -38,6 +40,7 @@ _SIGNATURES = {
                                         _c_f32, _c_p, _c_p, _c_p, _c_sz, _c_p]),
     "qlora_linear_bwd": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, ctypes.POINTER(NF4Struct), _c_p,
                                         _c_p, _c_i32, _c_f32, _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p]),
+    "qlora_merge": (ctypes.c_int, [ctypes.POINTER(NF4Struct), _c_p, _c_p, _c_i32, _c_f32, _c_p, _c_p]),
     "ql_get_device_status": (ctypes.c_int, [_c_p]),
     "ql_selftest_wait": (ctypes.c_int, [ctypes.c_int64, _c_p]),
     "ql_last_error": (ctypes.c_char_p, []),
@@ -104,6 +107,13 @@ def workspace_size(op, M=0, N=0, K=0, r=0):
 def nf4_codebook():
     buf = (ctypes.c_float * 16)()
     _check(lib.ql_nf4_codebook(buf))
+    return [float(v) for v in buf]
+
+
+def codebook(quant_type=QL_NF4):
+    """The 16 levels of a code table (QL_NF4 or QL_FP4), ascending."""
+    buf = (ctypes.c_float * 16)()
+    _check(lib.ql_codebook(int(quant_type), buf))
     return [float(v) for v in buf]
 
 
@@ -174,12 +184,13 @@ class NF4Tensor:
     dq_mean: torch.Tensor = None
     blocksize: int = 64
     dq_blocksize: int = 256
+    quant_type: int = QL_NF4
 
     @classmethod
-    def empty(cls, rows, cols, device, dq_blocksize=256, blocksize=64):
+    def empty(cls, rows, cols, device, dq_blocksize=256, blocksize=64, quant_type=QL_NF4):
         n_b = rows * cols // blocksize
         t = cls(rows, cols, torch.empty(rows * cols // 2, dtype=torch.uint8, device=device),
-                blocksize=blocksize, dq_blocksize=dq_blocksize)
+                blocksize=blocksize, dq_blocksize=dq_blocksize, quant_type=quant_type)
         if dq_blocksize:
             t.absmax_code = torch.empty(n_b, dtype=torch.int8, device=device)
             t.dq_step = torch.empty((n_b + dq_blocksize - 1) // dq_blocksize, dtype=torch.float32,
@@ -192,7 +203,7 @@ class NF4Tensor:
     def struct(self):
         return NF4Struct(self.rows, self.cols, self.blocksize, self.dq_blocksize,
                          _ptr(self.packed), _ptr(self.absmax), _ptr(self.absmax_code),
-                         _ptr(self.dq_step), _ptr(self.dq_mean))
+                         _ptr(self.dq_step), _ptr(self.dq_mean), self.quant_type)
 
     def nbytes(self):
         return sum(t.numel() * t.element_size() for t in
@@ -200,11 +211,11 @@ class NF4Tensor:
                    if t is not None)
 
 
-def nf4_quantize(W, dq_blocksize=256, blocksize=64, out=None, ws=None, stream=None):
-    """Quantize a bf16 (rows x cols) CUDA tensor to NF4 (+ double quant)."""
+def nf4_quantize(W, dq_blocksize=256, blocksize=64, out=None, ws=None, stream=None, quant_type=QL_NF4):
+    """Quantize a bf16 (rows x cols) CUDA tensor to NF4 (or FP4) codes (+ double quant)."""
     _need(W, torch.bfloat16, "W")
     rows, cols = W.shape
-    q = out if out is not None else NF4Tensor.empty(rows, cols, W.device, dq_blocksize, blocksize)
+    q = out if out is not None else NF4Tensor.empty(rows, cols, W.device, dq_blocksize, blocksize, quant_type)
     ws, nbytes = _workspace(workspace_size(OP_QUANTIZE, 0, rows, cols, 0), W.device, ws)
     s = q.struct()
     _check(lib.nf4_quantize(_ptr(W), ctypes.byref(s), _ptr(ws), nbytes, _stream(stream)))
@@ -297,3 +308,16 @@ def qlora_linear_bwd(dY, X, XA, q, A, B, scale, dX=None, dA=None, dB=None, ws=No
                                 float(scale), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(ws), nbytes,
                                 _stream(stream)))
     return dX, dA, dB
+
+
+def qlora_merge(q, A, B, scale, out=None, stream=None):
+    """W' = bf16(w_hat + scale (A B)^T): the merged dense bf16 weight (rows x cols)."""
+    r = A.shape[1]
+    _need(A, torch.bfloat16, "A", (q.cols, r))
+    _need(B, torch.bfloat16, "B", (r, q.rows))
+    if out is None:
+        out = torch.empty(q.rows, q.cols, dtype=torch.bfloat16, device=A.device)
+    _need(out, torch.bfloat16, "out", (q.rows, q.cols))
+    s = q.struct()
+    _check(lib.qlora_merge(ctypes.byref(s), _ptr(A), _ptr(B), r, float(scale), _ptr(out), _stream(stream)))
+    return out

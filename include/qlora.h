@@ -76,10 +76,12 @@ enum ql_op {
  *   absmax_code    : n_b int8 second-level codes   (dq_blocksize != 0)
  *   dq_step        : n_2 = ceil(n_b/256) floats     (dq_blocksize != 0)
  *   dq_mean        : 1 float                         (dq_blocksize != 0)
+ *   quant_type     : QL_NF4 (0, the default) or QL_FP4 (1): which 16-level
+ *                    code table the 4-bit codes index (see ql_codebook).
  * Block b = row*(cols/64) + j covers row `row`, columns [64j, 64j+64).
  * Decoded block constant: dq off: absmax[b];
  *   dq on: fl32(fl32(absmax_code[b] * dq_step[b/256]) + dq_mean[0]).
- * Dequantized weight: bf16_rne(fl32(q[code] * constant)), q = NF4 codebook.
+ * Dequantized weight: bf16_rne(fl32(q[code] * constant)), q = the code table.
  */
 typedef struct {
   int64_t rows;
@@ -91,7 +93,14 @@ typedef struct {
   int8_t *absmax_code;
   float *dq_step;
   float *dq_mean;
+  int32_t quant_type;
 } ql_nf4_tensor;
+
+/* Code tables (ql_nf4_tensor.quant_type). */
+enum ql_quant_type {
+  QL_NF4 = 0, /* 4-bit NormalFloat: normal quantiles, the QLoRA data type */
+  QL_FP4 = 1  /* 4-bit float E2M1 values, the baseline NF4 is compared with */
+};
 
 /*
  * Bytes of workspace the op needs for the given sizes (M tokens, N out, K in,
@@ -109,14 +118,28 @@ QL_API size_t ql_workspace_size(int op, int64_t M, int64_t N, int64_t K, int32_t
 QL_API int ql_nf4_codebook(float *out16);
 
 /*
+ * The 16 levels of a code table (ascending fp32, host memory `out16`):
+ *   QL_NF4 as ql_nf4_codebook;
+ *   QL_FP4: the values of the 4-bit float format E2M1 (sign, 2 exponent bits,
+ *   1 mantissa bit: 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives) divided
+ *   by the largest, 6, so the endpoints are -1 and +1; the 15 distinct
+ *   values ascending (one zero, at index 7 as in NF4) and index 15 repeating
+ *   +1 (never produced by the quantizer: ties go to the lower index).  The
+ *   QLoRA pages compare NF4 against 4-bit floats; this is the plainest 4-bit
+ *   float.  Returns QL_OK, or QL_ERR_UNSUPPORTED for an unknown type.
+ */
+QL_API int ql_codebook(int32_t quant_type, float *out16);
+
+/*
  * NF4 quantization with optional double quantization (QLoRA abstract,
  * innovations (a) and (b); news write-up: "Double Quantization" saves about
  * 0.37 bit per parameter).
  *   W  : rows x cols bf16 (device), finite.
  *   q  : host struct describing the device outputs (all written).
  *   ws : ql_workspace_size(QL_OP_QUANTIZE, 0, rows, cols, 0) bytes.
- * Block absmax m = max|w| over 64 elements; code = index of the nearest NF4
- * level to fl32(w / m) (ties to the lower index; all-zero block -> code 7).
+ * Block absmax m = max|w| over 64 elements; code = index of the nearest
+ * level of the tensor's code table (q->quant_type) to fl32(w / m) (ties to
+ * the lower index; all-zero block -> code 7).
  * Double quant: mu = fl32(S / n_b) with S the fp64 sum of all m (exact when
  * the exponents of the block absmax values span fewer than
  * 45 - log2(n_b) binades, which holds for real weights); per 256 blocks
@@ -216,6 +239,21 @@ QL_API int qlora_linear_bwd(const uint16_t *dY, const uint16_t *X, const uint16_
                      const uint16_t *B, int32_t r, float scale, uint16_t *dX,
                      float *dA, float *dB, void *ws, size_t ws_bytes,
                      ql_stream_t stream);
+
+/*
+ * LoRA merge for inference (LoRA tutorial, Lit-LLaMA translation: the
+ * low-rank update can be added into the weight after training, W' = W + dW,
+ * so that inference costs nothing extra):
+ *   W_out = bf16(w_hat + s (A B)^T)   N x K bf16 (device), row n, column k:
+ *           bf16_rne(fl32(w_hat[n][k] + s * acc)), acc = sum_j A[k][j] B[j][n]
+ *           accumulated in fp32, w_hat the dequantized weight.
+ *   W : N x K NF4 (input), A : K x r bf16, B : r x N bf16, scale : s.
+ * With B = 0 the output is w_hat exactly.  To store the merged weight in NF4
+ * again, pass W_out to nf4_quantize.  Reads the weight once and writes W_out
+ * once; no workspace.
+ */
+QL_API int qlora_merge(const ql_nf4_tensor *W, const uint16_t *A, const uint16_t *B, int32_t r, float scale,
+                       uint16_t *W_out, ql_stream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status

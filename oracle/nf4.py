@@ -37,6 +37,12 @@ Readings taken where the pages are silent:
      -127, 127) (0 when step is 0).  Decode: fl32(fl32(code * step) + mu),
      with no fused multiply-add.
   R6 Dequantized weight: w_hat = bf16_rne(fl32(q[code] * absmax_hat)).
+  R17 FP4 (the 4-bit float the pages say NF4 beats; its format is not on the
+     pages): the plainest 4-bit float, E2M1 (values 0, 0.5, 1, 1.5, 2, 3, 4, 6
+     and negatives), scaled by 1/6 to [-1, 1]; codes index the ascending
+     table of its 15 distinct values (zero at 7, as for NF4), the 16th entry
+     repeating +1.  Coding, packing, double quantization and dequantization
+     are the same as for NF4 with this table.
 
 Parity: the codebook, coding, packing, DQ and dequantization are pinned by
 tests against closed forms, brute force and error bounds; the exact codebook
@@ -86,19 +92,56 @@ def nf4_levels():
     return nf4_levels_f64().astype(np.float32)
 
 
-def nf4_midpoints():
-    """Decision thresholds t_j = (q_j + q_{j+1}) / 2 of the fp32 codebook, exact in fp64."""
-    q = nf4_levels().astype(np.float64)
+QT_NF4, QT_FP4 = 0, 1
+
+
+def e2m1_values():
+    """Every value of the 4-bit float E2M1 (1 sign, 2 exponent, 1 mantissa
+    bit, exponent bias 1, no infinities or NaN): exponent field 0 gives the
+    subnormals 0 and 0.5; field e > 0 gives 2^(e-1) (1 + m/2).  16 encodings."""
+    vals = []
+    for s in (0, 1):
+        for e in range(4):
+            for m in (0, 1):
+                mag = 0.5 * m if e == 0 else 2.0 ** (e - 1) * (1.0 + 0.5 * m)
+                vals.append(-mag if s else mag)
+    return np.array(vals, dtype=np.float64)
+
+
+def fp4_levels():
+    """The FP4 comparison code table (reading R17): the distinct E2M1 values
+    divided by the largest magnitude (6) so the endpoints are -1 and +1,
+    ascending (15 values, one zero at index 7), rounded once to fp32, with a
+    16th entry repeating +1 (the nearest-level rule with ties to the lower
+    index never picks it)."""
+    v = e2m1_values()
+    distinct = np.unique(v) + 0.0  # -0 and +0 compare equal: one zero, made +0
+    lv = (distinct / np.max(np.abs(distinct))).astype(np.float32)
+    return np.concatenate([lv, lv[-1:]])
+
+
+def code_levels(quant_type=QT_NF4):
+    """The 16-entry level table a quant type's 4-bit codes index."""
+    if quant_type == QT_NF4:
+        return nf4_levels()
+    if quant_type == QT_FP4:
+        return fp4_levels()
+    raise ValueError(f"quant type {quant_type}")
+
+
+def nf4_midpoints(levels=None):
+    """Decision thresholds t_j = (q_j + q_{j+1}) / 2 of the fp32 code table, exact in fp64."""
+    q = (nf4_levels() if levels is None else np.asarray(levels, np.float32)).astype(np.float64)
     return (q[:-1] + q[1:]) / 2.0
 
 
-def nearest_code(x):
-    """Index of the nearest fp32 codebook level to each fp32 x (ties to the lower index, R3).
+def nearest_code(x, levels=None):
+    """Index of the nearest fp32 level to each fp32 x (ties to the lower index, R3).
 
-    code = #{ j : x > t_j } over the 15 exact fp64 midpoints.
+    code = #{ j : x > t_j } over the 15 exact fp64 midpoints (NF4 by default).
     """
     x = np.asarray(x, dtype=np.float32).astype(np.float64)
-    t = nf4_midpoints()
+    t = nf4_midpoints(levels)
     return (x[..., None] > t).sum(axis=-1).astype(np.uint8)
 
 
@@ -113,7 +156,7 @@ def block_absmax(w_f32, blocksize=BLOCKSIZE):
     return np.abs(w_f32.reshape(rows, cols // blocksize, blocksize)).max(axis=2)
 
 
-def nf4_codes(w_f32, absmax, blocksize=BLOCKSIZE, rows_per_chunk=512):
+def nf4_codes(w_f32, absmax, blocksize=BLOCKSIZE, rows_per_chunk=512, levels=None):
     """NF4 code of every element, given its block's absmax (R3).
 
     x = fl32(w / absmax) as an IEEE single division; all-zero blocks code to 7.
@@ -129,7 +172,7 @@ def nf4_codes(w_f32, absmax, blocksize=BLOCKSIZE, rows_per_chunk=512):
         zero = m == 0
         safe = np.where(zero, np.float32(1.0), m)
         x = (w3 / safe).astype(np.float32)
-        codes = nearest_code(x)
+        codes = nearest_code(x, levels)
         codes = np.where(zero, np.uint8(ZERO_CODE), codes)
         out[r0:r1] = codes.reshape(r1 - r0, cols)
     return out
@@ -229,28 +272,30 @@ def double_dequantize(code, step, mean, dq_blocksize=DQ_BLOCKSIZE):
     return (prod + np.float32(mean)).astype(np.float32)
 
 
-def dequantize_codes(codes, absmax_hat, blocksize=BLOCKSIZE):
+def dequantize_codes(codes, absmax_hat, blocksize=BLOCKSIZE, levels=None):
     """w_hat = bf16_rne(fl32(q[code] * absmax_hat)) (R6); returns bf16 bits, same shape as codes."""
     rows, cols = codes.shape
-    q = nf4_levels()
+    q = nf4_levels() if levels is None else np.asarray(levels, np.float32)
     vals = q[codes.astype(np.int64)].reshape(rows, cols // blocksize, blocksize)
     prod = (vals * absmax_hat.reshape(rows, cols // blocksize, 1).astype(np.float32)).astype(np.float32)
     return f32_to_bf16_bits(prod.reshape(rows, cols))
 
 
-def quantize(w_bits, blocksize=BLOCKSIZE, dq_blocksize=DQ_BLOCKSIZE):
+def quantize(w_bits, blocksize=BLOCKSIZE, dq_blocksize=DQ_BLOCKSIZE, quant_type=QT_NF4):
     """Quantize a bf16 (rows, cols) weight matrix given as uint16 bit patterns.
 
-    Returns a dict with: rows, cols, blocksize, dq_blocksize, packed (uint8,
-    rows*cols/2), absmax (float32, n_b), and, when dq_blocksize > 0, code
-    (int8, n_b), step (float32, n_2), mean (float32), mean_exact (bool).
+    Returns a dict with: rows, cols, blocksize, dq_blocksize, quant_type,
+    packed (uint8, rows*cols/2), absmax (float32, n_b), and, when
+    dq_blocksize > 0, code (int8, n_b), step (float32, n_2), mean (float32),
+    mean_exact (bool).  quant_type selects the code table (NF4, or FP4 for
+    comparison).
     """
     w_bits = np.asarray(w_bits, dtype=np.uint16)
     rows, cols = w_bits.shape
     w = bf16_bits_to_f32(w_bits)
     absmax = block_absmax(w, blocksize)
-    codes = nf4_codes(w, absmax, blocksize)
-    out = dict(rows=rows, cols=cols, blocksize=blocksize, dq_blocksize=dq_blocksize,
+    codes = nf4_codes(w, absmax, blocksize, levels=code_levels(quant_type))
+    out = dict(rows=rows, cols=cols, blocksize=blocksize, dq_blocksize=dq_blocksize, quant_type=quant_type,
                packed=pack_nibbles(codes), absmax=absmax.reshape(-1))
     if dq_blocksize:
         code, step, mean, exact = double_quantize(absmax.reshape(-1), dq_blocksize)
@@ -272,7 +317,7 @@ def dequantize(qt, rows=None):
     mh = absmax_hat(qt).reshape(R, C // bs)
     if rows is not None:
         codes, mh = codes[rows], mh[rows]
-    return dequantize_codes(codes, mh, bs)
+    return dequantize_codes(codes, mh, bs, levels=code_levels(qt.get("quant_type", QT_NF4)))
 
 
 def constant_bits_per_param(rows, cols, blocksize=BLOCKSIZE, dq_blocksize=DQ_BLOCKSIZE):

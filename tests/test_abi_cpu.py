@@ -156,3 +156,60 @@ def test_quotient_without_division_is_exact_on_all_bf16_pairs(tmp_path):
     p = subprocess.run([exe], capture_output=True, text=True, timeout=600)
     assert p.returncode == 0, p.stdout
     assert "bad 0" in p.stdout
+
+
+def test_division_free_coding_is_exact_on_all_bf16_pairs(tmp_path):
+    """The quantizer codes each element without a division: the cell from an
+    approximate quotient, the decision from the sign of w - m u (plus
+    m delta when needed).  Checked against the code of the IEEE quotient for
+    every pair of bf16 values with |w| <= m in the fast path's range, with the
+    reciprocal perturbed up to two ulps either way (exhaustive, ~2.5e9
+    cases), on the NF4 codebook of the oracle."""
+    from oracle import nf4
+    src = os.path.join(ROOT, "tests", "native", "coding_check.c")
+    exe = str(tmp_path / "coding_check")
+    subprocess.run(["gcc", "-O2", "-mfma", "-ffp-contract=off", "-fopenmp", "-o", exe, src, "-lm"], check=True)
+    levels = [float(v).hex() for v in nf4.nf4_levels()]
+    p = subprocess.run([exe, *levels], capture_output=True, text=True, timeout=900)
+    assert p.returncode == 0, p.stdout
+    assert "bad 0" in p.stdout
+    assert "one_fma 1" in p.stdout  # the NF4 table takes the one-FMA decision
+
+
+def test_merge_rejects_bad_arguments_on_host(ql):
+    _fake_pointers_only_without_gpu()
+    lib, E = ql.lib, ql
+    p, odd = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x10002)
+    s = ql.NF4Struct(256, 512, 64, 256, p, None, p, p, p)
+    assert lib.qlora_merge(ctypes.byref(s), None, p, 16, 1.0, p, None) == E.QL_ERR_INVALID
+    assert lib.qlora_merge(ctypes.byref(s), p, p, 16, 1.0, odd, None) == E.QL_ERR_MISALIGNED
+    assert lib.qlora_merge(ctypes.byref(s), p, p, 12, 1.0, p, None) == E.QL_ERR_UNSUPPORTED
+    assert "rank 12" in lib.ql_last_error().decode()
+    bad = ql.NF4Struct(100, 512, 64, 256, p, None, p, p, p)
+    assert lib.qlora_merge(ctypes.byref(bad), p, p, 16, 1.0, p, None) == E.QL_ERR_UNSUPPORTED
+
+
+def test_fp4_table_matches_oracle_bit_for_bit(ql):
+    lib_levels = np.array(ql.codebook(ql.QL_FP4), dtype=np.float32)
+    assert np.array_equal(lib_levels.view(np.uint32), nf4.fp4_levels().view(np.uint32))
+    with pytest.raises(ql.QLError):
+        ql.codebook(7)
+
+
+def test_division_free_coding_is_exact_on_the_fp4_table(tmp_path):
+    """The same exhaustive check as for NF4, on the FP4 comparison table."""
+    src = os.path.join(ROOT, "tests", "native", "coding_check.c")
+    exe = str(tmp_path / "coding_check")
+    subprocess.run(["gcc", "-O2", "-mfma", "-ffp-contract=off", "-fopenmp", "-o", exe, src, "-lm"], check=True)
+    p = subprocess.run([exe, *[float(v).hex() for v in nf4.fp4_levels()]], capture_output=True, text=True,
+                       timeout=900)
+    assert p.returncode == 0, p.stdout
+    assert "bad 0" in p.stdout
+
+
+def test_unknown_quant_type_is_rejected_on_host(ql):
+    _fake_pointers_only_without_gpu()
+    p = ctypes.c_void_p(0x10000)
+    s = ql.NF4Struct(256, 512, 64, 256, p, None, p, p, p, 5)
+    assert ql.lib.nf4_dequantize(ctypes.byref(s), p, None) == ql.QL_ERR_UNSUPPORTED
+    assert "quant_type 5" in ql.lib.ql_last_error().decode()

@@ -219,3 +219,69 @@ def test_chained_calls_read_the_previous_calls_output(ql):
     assert_close("dX of layer 1", f64(dX), dXr)
     assert_close("dA of layer 1", f64(dA1), dA1r)
     assert_close("dB of layer 1", f64(dB1), dB1r)
+
+
+def test_back_to_back_independent_calls_equal_synchronised_calls(ql):
+    """Independent linears issued back to back on one stream overlap: a GEMM
+    whose inputs the previous call does not write starts its main loop in the
+    previous GEMM's last wave and waits only before its LoRA steps.  Results
+    must equal the same calls made one at a time with a synchronisation in
+    between, bit for bit, over repeated rounds on one workspace."""
+    from bit_nf4_quantized_38_b300.workloads import normal_bf16, normal_with_outliers_bf16
+    dev = torch.device("cuda")
+    shapes = [(1032, 576, 1100, 64), (4096, 1024, 2048, 16), (520, 4160, 600, 32), (2048, 2048, 1500, 64),
+              (1032, 576, 300, 128)]
+    layers = []
+    for i, (N, K, M, r) in enumerate(shapes):
+        q = ql.nf4_quantize(normal_with_outliers_bf16((N, K), 0.02, 0.001, 20.0, 90 + i).to(dev))
+        X, A = normal_bf16((M, K), 1.0, 100 + i).to(dev), normal_bf16((K, r), 0.125, 110 + i).to(dev)
+        B, dY = normal_bf16((r, N), 0.01, 120 + i).to(dev), normal_bf16((M, N), 1.0, 130 + i).to(dev)
+        layers.append((q, X, A, B, dY, 16.0 / r))
+    ws = torch.empty(max(max(ql.workspace_size(ql.OP_LINEAR_FWD, M, N, K, r),
+                             ql.workspace_size(ql.OP_LINEAR_BWD, M, N, K, r)) for N, K, M, r in shapes),
+                     dtype=torch.uint8, device=dev)
+
+    def run(sync):
+        outs = []
+        for q, X, A, B, dY, s in layers:
+            Y, XA = ql.qlora_linear_fwd(X, q, A, B, s, ws=ws)
+            outs.append([Y, XA])
+            if sync:
+                torch.cuda.synchronize()
+        for (q, X, A, B, dY, s), o in zip(reversed(layers), reversed(outs)):
+            o.extend(ql.qlora_linear_bwd(dY, X, o[1], q, A, B, s, ws=ws))
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        ql.device_status()
+        return outs
+
+    ref = run(True)
+    for _ in range(3):
+        got = run(False)
+        for a, b in zip(ref, got):
+            for x, y in zip(a, b):
+                assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("N,K,M,r", [(1032, 576, 1100, 32), (264, 640, 17, 64), (520, 1088, 9, 16)])
+def test_fp4_weights_forward_backward(ql, N, K, M, r):
+    """The same layer with FP4-coded weights (tensor-core path and, for
+    M <= 16, the decode path): within tolerance of the oracle on the FP4
+    dequantized weight."""
+    W, X, A, B, dY, s = make_case(N, K, M, r, seed=N + M + 3)
+    dev = torch.device("cuda")
+    q = ql.nf4_quantize(W.to(dev), quant_type=ql.QL_FP4)
+    Xd, Ad, Bd, dYd = X.to(dev), A.to(dev), B.to(dev), dY.to(dev)
+    Y, XA = ql.qlora_linear_fwd(Xd, q, Ad, Bd, s)
+    dX, dA, dB = ql.qlora_linear_bwd(dYd, Xd, XA, q, Ad, Bd, s)
+    torch.cuda.synchronize()
+    ql.device_status()
+    Wh = nf4.dequantize(nf4.quantize(bits(W), quant_type=nf4.QT_FP4))
+    Yr, _ = linear.lora_forward(bits(X), Wh, bits(A), bits(B), s)
+    dXr, dAr, dBr, _ = linear.lora_backward(bits(dY), bits(X), Wh, bits(A), bits(B), s)
+    tag = f"fp4 {N}x{K} M={M} r={r}"
+    assert_close(f"Y {tag}", f64(Y), Yr)
+    assert_close(f"dX {tag}", f64(dX), dXr)
+    assert_close(f"dA {tag}", f64(dA), dAr)
+    assert_close(f"dB {tag}", f64(dB), dBr)

@@ -294,3 +294,50 @@ def test_quantized_arrays_have_the_counted_sizes():
     assert qt["code"].size == n // 64 and qt["step"].size == (n // 64 + 255) // 256
     bits = (qt["code"].nbytes * 8 + qt["step"].nbytes * 8 + 32) / n
     assert bits == nf4.constant_bits_per_param(8, 4096)
+
+
+# --------------------------------------------------------------------------- FP4 comparison table
+
+def test_fp4_table_is_the_e2m1_value_set_scaled_to_unit_range():
+    """E2M1 has 16 encodings, 15 distinct values: +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}
+    (the format's definition, written out); scaled by 1/6 and ascending, with
+    the 16th entry repeating +1 and the zero (+0) at index 7."""
+    v = nf4.e2m1_values()
+    assert v.size == 16 and np.unique(v).size == 15
+    spec = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert sorted(set(np.abs(v).tolist())) == spec
+    q = nf4.fp4_levels()
+    assert q.dtype == np.float32 and q.shape == (16,)
+    want = np.array([-x / 6 for x in reversed(spec[1:])] + [x / 6 for x in spec] + [1.0], dtype=np.float32)
+    assert np.array_equal(q.view(np.uint32), want.view(np.uint32))
+    assert q[nf4.ZERO_CODE].view(np.uint32) == 0  # +0
+    assert np.all(np.diff(q[:15].astype(np.float64)) > 0) and q[14] == q[15] == 1.0
+    assert np.array_equal(q[:15], -q[14::-1])  # symmetric
+
+
+def test_fp4_nearest_code_is_brute_force_argmin():
+    q = nf4.fp4_levels().astype(np.float64)
+    x = np.linspace(-1.0, 1.0, 200_001).astype(np.float32)
+    mids = ((q[:-1] + q[1:]) / 2).astype(np.float32)
+    x = np.concatenate([x, mids, np.nextafter(mids, np.float32(2)), np.nextafter(mids, np.float32(-2))])
+    x = x[np.abs(x) <= 1.0]  # quotients w / absmax never leave [-1, 1]
+    d = np.abs(x.astype(np.float64)[:, None] - q[None, :])
+    brute = np.argmin(d, axis=1)  # first minimum: ties to the lower index
+    got = nf4.nearest_code(x, nf4.fp4_levels())
+    assert np.array_equal(got, brute)
+    assert got.max() == 14  # the repeated +1 is never chosen
+
+
+def test_fp4_round_trip_error_bound():
+    """|w - w_hat| <= m g/2 + 2^-8 |w_hat| with g the largest FP4 level gap
+    (1/3, between 2/3 and 1), without double quantization."""
+    from bit_nf4_quantized_38_b300.workloads import bf16_bits, normal_with_outliers_bf16
+    W = bf16_bits(normal_with_outliers_bf16((64, 1024), 0.02, 0.001, 20.0, 3))
+    qt = nf4.quantize(W, dq_blocksize=0, quant_type=nf4.QT_FP4)
+    wh = bf16_bits_to_f32(nf4.dequantize(qt)).astype(np.float64)
+    w = bf16_bits_to_f32(W).astype(np.float64)
+    m = np.repeat(qt["absmax"].reshape(64, 16), 64, axis=1).astype(np.float64)
+    q = nf4.fp4_levels().astype(np.float64)
+    g = np.max(np.diff(q[:15]))
+    assert abs(g - 1 / 3) < 1e-7
+    assert np.all(np.abs(w - wh) <= m * g / 2 * (1 + 1e-6) + 2.0 ** -8 * np.abs(wh))

@@ -131,3 +131,54 @@ def test_llama65b_layer_weights_full_size(ql, idx):
     Wd = ql.nf4_dequantize(q)
     torch.cuda.synchronize()
     assert np.array_equal(_bits(Wd)[rows], nf4.dequantize(ref, rows=rows))
+
+
+@pytest.mark.parametrize("offset_elems", [0, 8])
+def test_weight_only_16_byte_aligned(ql, offset_elems):
+    """The quantizer reads whole 32-byte sectors when W is 32-byte aligned and
+    16-byte pieces otherwise (the interface asks only for 16): both give the
+    oracle's codes bit for bit."""
+    from bit_nf4_quantized_38_b300.workloads import normal_with_outliers_bf16
+    rows, cols = 520, 1088
+    W = normal_with_outliers_bf16((rows, cols), 0.02, 0.001, 20.0, seed=61)
+    buf = torch.empty(rows * cols + 64, dtype=torch.bfloat16, device="cuda")
+    Wd = buf[offset_elems:offset_elems + rows * cols].view(rows, cols)
+    Wd.copy_(W.cuda())
+    assert (Wd.data_ptr() % 32 == 0) == (offset_elems == 0)
+    ref = nf4.quantize(_bits(W), dq_blocksize=256)
+    _compare_quant(_gpu_quant(ql, Wd, 256), ref)
+
+
+@pytest.mark.parametrize("rows,cols,dq", [(1024, 1024, 256), (37, 4160, 256), (129, 1088, 0)])
+def test_fp4_quantize_and_dequantize_bit_exact(ql, rows, cols, dq):
+    """The FP4 comparison table behind the same interface (quant_type = FP4):
+    codes, constants and dequantized weights equal the oracle's bit for bit."""
+    from bit_nf4_quantized_38_b300.workloads import normal_with_outliers_bf16
+    W = normal_with_outliers_bf16((rows, cols), 0.02, 0.001, 20.0, seed=rows + cols + 5)
+    ref = nf4.quantize(_bits(W), dq_blocksize=dq, quant_type=nf4.QT_FP4)
+    q = ql.nf4_quantize(W.cuda(), dq_blocksize=dq, quant_type=ql.QL_FP4)
+    torch.cuda.synchronize()
+    ql.device_status()
+    _compare_quant(q, ref)
+    assert np.array_equal(_bits(ql.nf4_dequantize(q)), nf4.dequantize(ref))
+    # the same weight under NF4 codes differently
+    assert not np.array_equal(ref["packed"], nf4.quantize(_bits(W), dq_blocksize=dq)["packed"])
+
+
+def test_fp4_every_bf16_value(ql):
+    b = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = (b.astype(np.uint32) << 16).view(np.float32)
+    keep = b[np.isfinite(vals) & (np.abs(vals) <= 1.0)]
+    mb = f32_to_bf16_bits(np.float32(1.0))[0]
+    n = -(-keep.size // 63) * 63
+    blk = np.zeros(n, np.uint16)
+    blk[:keep.size] = keep
+    blk = np.concatenate([np.full((n // 63, 1), mb, np.uint16), blk.reshape(-1, 63)], axis=1).reshape(-1)
+    cols = 1024
+    data = np.concatenate([blk, np.zeros((-blk.size) % cols, np.uint16)]).reshape(-1, cols)
+    W = torch.from_numpy(data.view(np.int16)).view(torch.bfloat16).cuda()
+    ref = nf4.quantize(data, dq_blocksize=0, quant_type=nf4.QT_FP4)
+    q = ql.nf4_quantize(W, dq_blocksize=0, quant_type=ql.QL_FP4)
+    torch.cuda.synchronize()
+    assert np.array_equal(q.packed.cpu().numpy(), ref["packed"])
+    assert np.array_equal(_bits(ql.nf4_dequantize(q)), nf4.dequantize(ref))
