@@ -10,6 +10,8 @@
 // quantizer: 2 lanes per block, 64 B of bf16 in and 16 B of nibbles out per
 // lane; the dequantizer: 8 lanes per block, 4 B of nibbles in and 16 B of
 // bf16 out per lane).
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace ql {
@@ -204,33 +206,39 @@ __global__ void __launch_bounds__(256)
 k_double_quant(const float *__restrict__ absmax, int64_t n_b, int64_t total_blocks, const double *__restrict__ sum,
                int8_t *__restrict__ code, float *__restrict__ step, float *__restrict__ mean) {
   __shared__ float red[8];
-  const float mu = __double2float_rn(__ddiv_rn(*sum, (double)total_blocks));
-  const int64_t g = blockIdx.x;
-  const int64_t i = g * 256 + threadIdx.x;
-  const bool valid = i < n_b;
-  const float c = valid ? __fsub_rn(absmax[i], mu) : 0.0f;
-  float a = fabsf(c);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __shared__ float mu_s;
+  // mu once per CTA (an fp64 division is slow; every thread taking one was
+  // most of this kernel's time)
+  if (threadIdx.x == 0) mu_s = __double2float_rn(__ddiv_rn(*sum, (double)total_blocks));
   __syncthreads();
-  float a2 = red[0];
+  const float mu = mu_s;
+  const int64_t n_2 = (n_b + 255) / 256;
+  for (int64_t g = blockIdx.x; g < n_2; g += gridDim.x) {
+    const int64_t i = g * 256 + threadIdx.x;
+    const bool valid = i < n_b;
+    const float c = valid ? __fsub_rn(absmax[i], mu) : 0.0f;
+    float a = fabsf(c);
 #pragma unroll
-  for (int k = 1; k < 8; ++k) a2 = fmaxf(a2, red[k]);
-  const float st = __fdiv_rn(a2, 127.0f);
-  if (valid) {
-    int k = 0;
-    if (st != 0.0f) {
-      float t = rintf(__fdiv_rn(c, st));
-      t = fminf(fmaxf(t, -127.0f), 127.0f);
-      k = (int)t;
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+    __syncthreads();
+    float a2 = red[0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) a2 = fmaxf(a2, red[k]);
+    __syncthreads();  // red is rewritten by the next group
+    const float st = __fdiv_rn(a2, 127.0f);
+    if (valid) {
+      int k = 0;
+      if (st != 0.0f) {
+        float t = rintf(__fdiv_rn(c, st));
+        t = fminf(fmaxf(t, -127.0f), 127.0f);
+        k = (int)t;
+      }
+      code[i] = (int8_t)k;
     }
-    code[i] = (int8_t)k;
+    if (threadIdx.x == 0) step[g] = st;
   }
-  if (threadIdx.x == 0) {
-    step[g] = st;
-    if (g == 0) *mean = mu;
-  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *mean = mu;
 }
 
 template <bool kDQ>
@@ -342,7 +350,15 @@ cudaError_t launch_double_quant(const float *absmax, int64_t n_b, int64_t total_
                                 const double *sum, int8_t *code, float *step, float *mean, cudaStream_t st) {
   (void)dq_bs;  // 256, checked by the caller
   const int64_t n_2 = (n_b + 255) / 256;
-  k_double_quant<<<(unsigned)n_2, 256, 0, st>>>(absmax, n_b, total_blocks, sum, code, step, mean);
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  const int64_t grid = std::min<int64_t>(n_2, (int64_t)sms * 8);
+  k_double_quant<<<(unsigned)grid, 256, 0, st>>>(absmax, n_b, total_blocks, sum, code, step, mean);
   count_launch();
   return cudaGetLastError();
 }
