@@ -3,6 +3,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 
 #include "common.cuh"
 #include "linear.cuh"
@@ -70,6 +71,16 @@ int check_tensor(const ql_nf4_tensor *q, const char *fn, bool need_absmax_dq_off
 // quantize workspace: [fp64 sum | pad to 256][fp32 absmax n_b (double quant only)]
 size_t quantize_ws(int64_t N, int64_t K) { return 256 + round_up((size_t)(N * K / 64) * 4, 256); }
 
+// quantize-on-load: rows per staging chunk (about 16 MB of bf16) and the
+// workspace, [quantize workspace][chunk 0][chunk 1]
+int64_t host_chunk_rows(int64_t N, int64_t K) {
+  const int64_t rows = std::max<int64_t>(1, ((int64_t)8 << 20) / std::max<int64_t>(K, 1));
+  return std::min(rows, std::max<int64_t>(N, 1));
+}
+size_t quantize_host_ws(int64_t N, int64_t K) {
+  return quantize_ws(N, K) + 2 * round_up((size_t)(host_chunk_rows(N, K) * K * 2), 256);
+}
+
 }  // namespace
 }  // namespace ql
 
@@ -81,6 +92,7 @@ extern "C" size_t ql_workspace_size(int op, int64_t M, int64_t N, int64_t K, int
     case QL_OP_DEQUANTIZE: return 0;
     case QL_OP_LINEAR_FWD: return linear_fwd_ws(M, N, K, r);
     case QL_OP_LINEAR_BWD: return linear_bwd_ws(M, N, K, r);
+    case QL_OP_QUANTIZE_HOST: return quantize_host_ws(N, K);
     default: return (size_t)-1;
   }
 }
@@ -233,4 +245,60 @@ extern "C" int qlora_merge(const ql_nf4_tensor *W, const uint16_t *A, const uint
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   note_other_call(st);
   return launch_merge(*W, A, B, r, scale, W_out, st);
+}
+
+extern "C" int nf4_quantize_host(const uint16_t *W_host, const ql_nf4_tensor *q, void *ws, size_t ws_bytes,
+                                 ql_stream_t copy_stream, ql_stream_t stream) {
+  g_msg[0] = 0;
+  const char *fn = "nf4_quantize_host";
+  int rc = check_tensor(q, fn, true);
+  if (rc) return rc;
+  if (!W_host) return set_error(QL_ERR_INVALID, "%s: null W_host", fn);
+  if (!ws) return set_error(QL_ERR_INVALID, "%s: null workspace", fn);
+  if (!aligned(ws, 256)) return set_error(QL_ERR_MISALIGNED, "%s: workspace not 256-byte aligned", fn);
+  const int64_t N = q->rows, K = q->cols;
+  if (ws_bytes < quantize_host_ws(N, K))
+    return set_error(QL_ERR_UNSUPPORTED, "%s: workspace %zu < %zu bytes", fn, ws_bytes, quantize_host_ws(N, K));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t cst = reinterpret_cast<cudaStream_t>(copy_stream);
+  note_other_call(st);
+  char *base = static_cast<char *>(ws);
+  double *sum = reinterpret_cast<double *>(base);
+  float *absmax = q->dq_blocksize ? reinterpret_cast<float *>(base + 256) : q->absmax;
+  const int64_t crows = host_chunk_rows(N, K);
+  const size_t cbytes = round_up((size_t)(crows * K * 2), 256);
+  uint16_t *stage[2] = {reinterpret_cast<uint16_t *>(base + quantize_ws(N, K)),
+                        reinterpret_cast<uint16_t *>(base + quantize_ws(N, K) + cbytes)};
+  cudaEvent_t ev[5] = {};
+  for (auto &e : ev) {
+    rc = check_cuda(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "nf4_quantize_host: event");
+    if (rc) break;
+  }
+  // ev[0]: work queued on `stream` before this call (it may still use ws);
+  // ev[1 + h]: chunk in staging buffer h copied; ev[3 + h]: chunk in h coded
+  if (!rc) rc = check_cuda(cudaMemsetAsync(sum, 0, sizeof(double), st), "nf4_quantize_host: clear sum");
+  if (!rc) rc = check_cuda(cudaEventRecord(ev[0], st), "nf4_quantize_host: record");
+  if (!rc) rc = check_cuda(cudaStreamWaitEvent(cst, ev[0], 0), "nf4_quantize_host: wait");
+  for (int64_t r0 = 0, c = 0; !rc && r0 < N; r0 += crows, ++c) {
+    const int h = (int)(c & 1);
+    const int64_t rows = std::min(crows, N - r0);
+    if (c >= 2) rc = check_cuda(cudaStreamWaitEvent(cst, ev[3 + h], 0), "nf4_quantize_host: wait");
+    if (!rc)
+      rc = check_cuda(cudaMemcpyAsync(stage[h], W_host + r0 * K, (size_t)(rows * K * 2), cudaMemcpyHostToDevice, cst),
+                      "nf4_quantize_host: copy");
+    if (!rc) rc = check_cuda(cudaEventRecord(ev[1 + h], cst), "nf4_quantize_host: record");
+    if (!rc) rc = check_cuda(cudaStreamWaitEvent(st, ev[1 + h], 0), "nf4_quantize_host: wait");
+    if (!rc)
+      rc = check_cuda(launch_quantize(stage[h], rows, K, q->quant_type, q->packed + r0 * (K / 2),
+                                      absmax + r0 * (K / 64), sum, st),
+                      "nf4_quantize_host: launch");
+    if (!rc) rc = check_cuda(cudaEventRecord(ev[3 + h], st), "nf4_quantize_host: record");
+  }
+  if (!rc && q->dq_blocksize)
+    rc = check_cuda(launch_double_quant(absmax, N * K / 64, N * K / 64, q->dq_blocksize, sum, q->absmax_code,
+                                        q->dq_step, q->dq_mean, st),
+                    "nf4_quantize_host: double-quant launch");
+  for (auto &e : ev)
+    if (e) cudaEventDestroy(e);  // released once recorded work completes
+  return rc;
 }

@@ -29,13 +29,22 @@ size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 bool rank_ok(int r) { return r == 8 || r == 16 || r == 32 || r == 64 || r == 128; }
 bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-// forward workspace: XAs [M][r] bf16; backward: Gs [M][r] + recomputed XA [M][r]
-// Training workspaces have two halves; successive calls on a stream alternate
-// between them (see next_ws_half).
-size_t fwd_half(int64_t M, int r) { return up256((size_t)M * r * 2); }      // s XA, bf16 [M][r]
-size_t bwd_half(int64_t M, int r) { return 2 * up256((size_t)M * r * 2); }  // s G, XA: bf16 [M][r] each
-size_t fwd_ws(int64_t M, int r) { return 2 * fwd_half(M, r); }
-size_t bwd_ws(int64_t M, int r) { return 2 * bwd_half(M, r); }
+// forward workspace: XAs [M][r] bf16; backward: Gs [M][r] + recomputed XA [M][r];
+// with M <= 128 tokens either also holds the fp32 partials of the GEMM split
+// over its reduction.  Training workspaces have two halves; successive calls
+// on a stream alternate between them (see next_ws_half).
+size_t part_bytes(int64_t M, int64_t Nout, int64_t Kred) {
+  const int s = gemm_splits(M, Nout, Kred);
+  return s > 1 ? up256((size_t)s * M * Nout * 4) : 0;
+}
+size_t fwd_half(int64_t M, int64_t N, int64_t K, int r) {  // s XA bf16 [M][r], partials
+  return up256((size_t)M * r * 2) + part_bytes(M, N, K);
+}
+size_t bwd_half(int64_t M, int64_t N, int64_t K, int r) {  // s G, XA: bf16 [M][r] each, partials
+  return 2 * up256((size_t)M * r * 2) + part_bytes(M, K, N);
+}
+size_t fwd_ws(int64_t M, int64_t N, int64_t K, int r) { return 2 * fwd_half(M, N, K, r); }
+size_t bwd_ws(int64_t M, int64_t N, int64_t K, int r) { return 2 * bwd_half(M, N, K, r); }
 
 int check_common(const LinearArgs &a, const char *fn, size_t need) {
   if (a.M <= 0) return set_error(QL_ERR_INVALID, "%s: M = %lld", fn, (long long)a.M);
@@ -182,12 +191,12 @@ void note_other_call(cudaStream_t st) { note_call(st, false, {}); }
 size_t linear_fwd_ws(int64_t M, int64_t N, int64_t K, int32_t r) {
   if (M <= 0 || N <= 0 || K <= 0 || !rank_ok(r)) return 0;
   if (M <= kDecodeMaxM) return decode_ws(N, K, r);
-  return fwd_ws(M, r);
+  return fwd_ws(M, N, K, r);
 }
 
 size_t linear_bwd_ws(int64_t M, int64_t N, int64_t K, int32_t r) {
   if (M <= 0 || N <= 0 || K <= 0 || !rank_ok(r)) return 0;
-  return bwd_ws(M, r);
+  return bwd_ws(M, N, K, r);
 }
 
 int linear_fwd(const LinearArgs &a) {
@@ -222,11 +231,12 @@ int linear_fwd(const LinearArgs &a) {
     note_call(a.stream, rc == QL_OK, std::move(outs), std::move(reads), early_dependents);
     return rc;
   }
-  QL_TRY(check_common(a, fn, fwd_ws(M, r)));
+  QL_TRY(check_common(a, fn, fwd_ws(M, N, K, r)));
   cudaStream_t st = a.stream;
-  const size_t half = fwd_half(M, r);
+  const size_t half = fwd_half(M, N, K, r);
   char *wsh = static_cast<char *>(a.ws) + (next_ws_half(st) ? half : 0);
   uint16_t *xas = reinterpret_cast<uint16_t *>(wsh);
+  float *part = part_bytes(M, N, K) ? reinterpret_cast<float *>(wsh + up256((size_t)M * r * 2)) : nullptr;
 
   const std::vector<Range> xa_reads = {range(a.X, (size_t)(M * K * 2)), range(a.A, (size_t)(K * r * 2))};
   std::vector<Range> xa_writes = {range(wsh, half)};
@@ -256,6 +266,7 @@ int linear_fwd(const LinearArgs &a) {
   g.w = nf4_view(a.W);
   g.out = a.Y; g.Nout = N;
   g.early_main = gemm_early;
+  g.part = part;
   return launch_nf4_gemm(g, st);
 }
 
@@ -268,12 +279,13 @@ int linear_bwd(const LinearArgs &a) {
     return set_error(QL_ERR_MISALIGNED, "%s: operand not 16-byte aligned", fn);
   const int64_t M = a.M, N = a.W.rows, K = a.W.cols;
   const int r = a.r;
-  QL_TRY(check_common(a, fn, bwd_ws(M, r)));
+  QL_TRY(check_common(a, fn, bwd_ws(M, N, K, r)));
   cudaStream_t st = a.stream;
-  const size_t half = bwd_half(M, r);
+  const size_t half = bwd_half(M, N, K, r);
   char *ws = static_cast<char *>(a.ws) + (next_ws_half(st) ? half : 0);
   uint16_t *gs = reinterpret_cast<uint16_t *>(ws);
   uint16_t *xa_tmp = reinterpret_cast<uint16_t *>(ws + up256((size_t)M * r * 2));
+  float *part = part_bytes(M, K, N) ? reinterpret_cast<float *>(ws + 2 * up256((size_t)M * r * 2)) : nullptr;
 
   std::vector<Range> reads = {range(a.dY, (size_t)(M * N * 2)), range(a.X, (size_t)(M * K * 2)),
                              range(a.A, (size_t)(K * r * 2)), range(a.B, (size_t)(r * N * 2))};
@@ -323,6 +335,7 @@ int linear_bwd(const LinearArgs &a) {
     g.w = nf4_view(a.W);
     g.out = a.dX; g.Nout = K;
     g.early_main = gemm_early;
+    g.part = part;
     QL_TRY(launch_nf4_gemm(g, st));
   }
   // 3. dA = X^T Gs (X [M][K] and Gs [M][r] read MN-major) and 4. dB = s XA^T dY,

@@ -19,6 +19,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -54,6 +55,7 @@ struct GemmArgs {
   // that may still run: start the main loop at once and wait for the
   // previous kernel only before the LoRA steps (pair kernel; see there).
   int early_main;
+  float *part;  // single-CTA kernel split over K (gridDim.z > 1): fp32 partials [splits][M][ldo]
   float q[16];
 };
 
@@ -172,7 +174,13 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
-  const int nsteps = p.ksteps_main + p.ksteps_lora;
+  // Split over the reduction (few output tiles, M <= 128): CTA z takes main
+  // K-steps [kq0, kq0 + nmain) and the last one also the LoRA steps; each
+  // stores its fp32 partial tile, and k_splitk_sum adds them in split order.
+  const int sp = blockIdx.z, nsplit = gridDim.z;
+  const int kq0 = (int)((int64_t)sp * p.ksteps_main / nsplit);
+  const int nmain = (int)((int64_t)(sp + 1) * p.ksteps_main / nsplit) - kq0;
+  const int nsteps = nmain + (sp == nsplit - 1 ? p.ksteps_lora : 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -211,11 +219,11 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         const uint32_t ph = (ks / STAGES) & 1;
         if (!ptx::mbar_wait(empty(s), ph ^ 1, abort, p.status)) break;
         const uint32_t a_dst = sbase + s * STAGE_BYTES;
-        if (ks < p.ksteps_main) {
+        if (ks < nmain) {
           ptx::mbar_arrive_expect_tx(full(s), A_BYTES);
-          ptx::tma_load_2d(a_dst, &tmA, full(s), ks * BK, m0);
+          ptx::tma_load_2d(a_dst, &tmA, full(s), (kq0 + ks) * BK, m0);
         } else {
-          const int kl = ks - p.ksteps_main;
+          const int kl = ks - nmain;
           ptx::mbar_arrive_expect_tx(full(s), A_BYTES + B_BYTES);
           ptx::tma_load_2d(a_dst, &tmA2, full(s), kl * BK, m0);
           if (kTrans) {  // LoRA A stored [k][j]: K-major rows of the output columns
@@ -241,7 +249,7 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         ptx::tc_fence_after();
         const uint32_t a_addr = sbase + s * STAGE_BYTES;
         const uint32_t b_addr = a_addr + A_BYTES;
-        const bool lora = ks >= p.ksteps_main;
+        const bool lora = ks >= nmain;
         const uint64_t a_desc = ptx::desc_sw128(a_addr, 16, 1024);
         // K-major B: rows of 128 B, 8-row atoms 1024 B apart.  MN-major B
         // (W_hat^T for dX, the LoRA B for the forward): atoms of 64 output
@@ -299,12 +307,12 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
       }
     };
     RowBlockSrc cur[2], nxt[2];
-    if (p.ksteps_main > 0) fetch(0, cur);
+    if (nmain > 0) fetch(kq0, cur);
     for (int ks = 0; ks < nsteps; ++ks) {
       const int s = ks % STAGES;
       const uint32_t ph = (ks / STAGES) & 1;
-      const bool main_step = ks < p.ksteps_main;
-      if (ks + 1 < p.ksteps_main) fetch(ks + 1, nxt);
+      const bool main_step = ks < nmain;
+      if (ks + 1 < nmain) fetch(kq0 + ks + 1, nxt);
       if (!ptx::mbar_wait(empty(s), ph ^ 1, abort, p.status)) break;
       if (main_step) {
         const uint32_t b_addr = sbase + s * STAGE_BYTES + A_BYTES;
@@ -316,7 +324,7 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         ptx::fence_proxy_async_smem();
       }
       ptx::mbar_arrive(full(s));
-      if (ks + 1 < p.ksteps_main) {
+      if (ks + 1 < nmain) {
         cur[0] = nxt[0];
         cur[1] = nxt[1];
       }
@@ -327,6 +335,7 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
       const int qd = warp & 3;  // TMEM lane quarter this warp may access
       const int row = m0 + qd * 32 + lane;
       uint16_t *orow = p.out + (int64_t)row * p.ldo;
+      float *prow = nsplit > 1 ? p.part + ((int64_t)sp * p.M + row) * p.ldo : nullptr;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -337,12 +346,20 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           for (int j = 0; j < 4; ++j) {
             const int col = n0 + c * 32 + j * 8;
             if (col + 8 <= p.Nout) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
-              v.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
-              v.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
-              v.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
-              *reinterpret_cast<uint4 *>(orow + col) = v;
+              if (prow) {  // fp32 partial of this split
+                float4 *dst = reinterpret_cast<float4 *>(prow + col);
+                dst[0] = make_float4(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]),
+                                     __uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
+                dst[1] = make_float4(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]),
+                                     __uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
+              } else {
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
+                v.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
+                v.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
+                v.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
+                *reinterpret_cast<uint4 *>(orow + col) = v;
+              }
             }
           }
         }
@@ -355,6 +372,28 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
   __syncthreads();
   if (p.span && threadIdx.x == 0) atomicMax(p.span + 1, (unsigned long long)ptx::globaltimer());
   if (warp == 1) ptx::tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// out = bf16(sum over the splits of part[s]) in split order (fixed, so the
+// result is deterministic); 8 outputs per thread.  A programmatic dependent
+// of the split GEMM: waits for it before reading.
+__global__ void __launch_bounds__(256) k_splitk_sum(const float *__restrict__ part, int nsplit, int64_t n8,
+                                                    uint16_t *__restrict__ out) {
+  ptx::griddep_wait();
+  ptx::griddep_launch();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    float4 a = __ldcg(reinterpret_cast<const float4 *>(part) + 2 * i);
+    float4 b = __ldcg(reinterpret_cast<const float4 *>(part) + 2 * i + 1);
+    for (int s = 1; s < nsplit; ++s) {
+      const float4 *ps = reinterpret_cast<const float4 *>(part + (int64_t)s * n8 * 8) + 2 * i;
+      const float4 x = __ldcg(ps), y = __ldcg(ps + 1);
+      a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+      b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+    }
+    reinterpret_cast<uint4 *>(out)[i] =
+        make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+  }
 }
 
 // ---------------------------------------------------------------------------- CTA-pair kernel
@@ -652,6 +691,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
+int gemm_splits(int64_t M, int64_t Nout, int64_t Kred) {
+  if (M > 128) return 1;
+  const int64_t tiles = (Nout + BN - 1) / BN, ks = (Kred + BK - 1) / BK;
+  int64_t s = (kSplitTarget + tiles - 1) / tiles;
+  s = std::min<int64_t>(s, 16);
+  s = std::min<int64_t>(s, ks);
+  return (int)std::max<int64_t>(s, 1);
+}
+
 int make_tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
   auto fn = encode_fn();
   if (!fn) return set_error(QL_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
@@ -748,7 +796,9 @@ int launch(const GemmProblem &g, unsigned long long *span, cudaStream_t st) {
   a.span = span;
   const Codebook &cb = codebook(g.w.qt);
   for (int i = 0; i < 16; ++i) a.q[i] = cb.q[i];
-  dim3 grid((unsigned)((g.Nout + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM));
+  const int nsplit = g.part ? gemm_splits(g.M, g.Nout, g.Kred) : 1;
+  a.part = nsplit > 1 ? g.part : nullptr;
+  dim3 grid((unsigned)((g.Nout + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM), (unsigned)nsplit);
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(THREADS);
@@ -761,7 +811,18 @@ int launch(const GemmProblem &g, unsigned long long *span, cudaStream_t st) {
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, k_nf4_gemm<kTrans>, tA, tA2, tB2, a);
   count_launch();
-  return check_cuda(e, "tensor-core GEMM launch");
+  rc = check_cuda(e, "tensor-core GEMM launch");
+  if (rc || nsplit == 1) return rc;
+  const int64_t n8 = g.M * g.Nout / 8;
+  cudaLaunchConfig_t sc{};
+  sc.gridDim = dim3((unsigned)std::min<int64_t>((n8 + 255) / 256, 148 * 8));
+  sc.blockDim = dim3(256);
+  sc.stream = st;
+  sc.attrs = attr;
+  sc.numAttrs = 1;
+  e = cudaLaunchKernelEx(&sc, k_splitk_sum, (const float *)g.part, nsplit, n8, g.out);
+  count_launch();
+  return check_cuda(e, "split-K sum launch");
 }
 
 struct Timing {

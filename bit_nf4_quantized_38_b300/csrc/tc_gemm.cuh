@@ -44,8 +44,16 @@ struct GemmProblem {
   // (the previous library call writes neither): the CTA-pair kernel then
   // starts its main loop before its predecessor completes.
   bool early_main = false;
+  // fp32 partial buffer for the single-CTA kernel split over the reduction
+  // (M <= 128: gemm_splits(M, Nout, Kred) x M x Nout floats), or null (no split)
+  float *part = nullptr;
 };
 int launch_nf4_gemm(const GemmProblem &g, cudaStream_t st);
+// Splits over the reduction of a GEMM with M <= 128 tokens (1 otherwise): as
+// many as make the tiles x splits about one CTA per SM of a 148-SM GPU, at
+// most 16 and at most one per 64-wide K-step.
+constexpr int kSplitTarget = 148;
+int gemm_splits(int64_t M, int64_t Nout, int64_t Kred);
 
 // 2-D bf16 tensor map [outer][inner] (inner contiguous), box [box_outer][64],
 // 128-byte swizzle, zero fill outside the tensor.

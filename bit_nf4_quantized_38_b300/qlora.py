@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libq
 
 QL_OK, QL_ERR_INVALID, QL_ERR_UNSUPPORTED, QL_ERR_MISALIGNED, QL_ERR_CUDA, QL_ERR_TIMEOUT = range(6)
 QL_NF4, QL_FP4 = 0, 1
-OP_QUANTIZE, OP_DEQUANTIZE, OP_LINEAR_FWD, OP_LINEAR_BWD = range(4)
+OP_QUANTIZE, OP_DEQUANTIZE, OP_LINEAR_FWD, OP_LINEAR_BWD, OP_QUANTIZE_HOST = range(5)
 
 _c_i64, _c_i32, _c_f32, _c_p, _c_sz = (ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
                                        ctypes.c_void_p, ctypes.c_size_t)
@@ -33,6 +33,7 @@ _SIGNATURES = {
     "ql_codebook": (ctypes.c_int, [_c_i32, ctypes.POINTER(ctypes.c_float)]),
     "nf4_quantize": (ctypes.c_int, [_c_p, ctypes.POINTER(NF4Struct), _c_p, _c_sz, _c_p]),
     "nf4_quantize_noalloc": (ctypes.c_int, [_c_p, ctypes.POINTER(NF4Struct), _c_p]),
+    "nf4_quantize_host": (ctypes.c_int, [_c_p, ctypes.POINTER(NF4Struct), _c_p, _c_sz, _c_p, _c_p]),
     "nf4_quantize_shard_begin": (ctypes.c_int, [_c_p, ctypes.POINTER(NF4Struct), _c_p, _c_sz, _c_p]),
     "nf4_quantize_shard_end": (ctypes.c_int, [ctypes.POINTER(NF4Struct), _c_p, _c_sz, _c_i64, _c_p]),
     "nf4_dequantize": (ctypes.c_int, [ctypes.POINTER(NF4Struct), _c_p, _c_p]),
@@ -230,6 +231,25 @@ def nf4_quantize_noalloc(W, dq_blocksize=256, blocksize=64, out=None, stream=Non
     q = out if out is not None else NF4Tensor.empty(rows, cols, W.device, dq_blocksize, blocksize)
     s = q.struct()
     _check(lib.nf4_quantize_noalloc(_ptr(W), ctypes.byref(s), _stream(stream)))
+    return q
+
+
+def nf4_quantize_host(W_host, device, dq_blocksize=256, blocksize=64, out=None, ws=None, stream=None,
+                      copy_stream=None, quant_type=QL_NF4):
+    """Quantize a bf16 (rows x cols) CPU tensor into NF4 on `device` while it
+    streams to the GPU (quantize-on-load; see include/qlora.h).  Pinned
+    memory lets the copies overlap the kernels.  Keep W_host alive and
+    unchanged until `stream` has passed the call."""
+    if W_host.is_cuda or W_host.dtype != torch.bfloat16 or not W_host.is_contiguous():
+        raise ValueError("W_host must be a contiguous bf16 CPU tensor")
+    rows, cols = W_host.shape
+    device = torch.device(device)
+    q = out if out is not None else NF4Tensor.empty(rows, cols, device, dq_blocksize, blocksize, quant_type)
+    ws, nbytes = _workspace(workspace_size(OP_QUANTIZE_HOST, 0, rows, cols, 0), device, ws)
+    s = q.struct()
+    st = _stream(stream)
+    cst = st if copy_stream is None else ctypes.c_void_p(copy_stream.cuda_stream)
+    _check(lib.nf4_quantize_host(ctypes.c_void_p(W_host.data_ptr()), ctypes.byref(s), _ptr(ws), nbytes, cst, st))
     return q
 
 

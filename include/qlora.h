@@ -59,7 +59,8 @@ enum ql_op {
   QL_OP_QUANTIZE = 0,
   QL_OP_DEQUANTIZE = 1,
   QL_OP_LINEAR_FWD = 2,
-  QL_OP_LINEAR_BWD = 3
+  QL_OP_LINEAR_BWD = 3,
+  QL_OP_QUANTIZE_HOST = 4
 };
 
 /*
@@ -169,6 +170,30 @@ QL_API int nf4_quantize(const uint16_t *W, const ql_nf4_tensor *q, void *ws,
  * -- race and must be ordered by the caller.
  */
 QL_API int nf4_quantize_noalloc(const uint16_t *W, const ql_nf4_tensor *q, ql_stream_t stream);
+
+/*
+ * Quantize-on-load: nf4_quantize of a weight that is still in HOST memory, so
+ * that loading a model in 4 bit (the QLoRA project page's load_in_4bit)
+ * never needs the bf16 copy in device memory.  The weight streams through
+ * two device staging chunks: chunk c is copied host -> device on
+ * `copy_stream` while chunk c - 1 is coded on `stream`; the double-quant
+ * constants follow once every chunk is coded.  The result equals
+ * nf4_quantize of the same weight bit for bit.
+ *   W_host      : rows x cols bf16 in HOST memory (page-locked memory lets the
+ *                 copies overlap the kernels; pageable memory works too).
+ *   q           : as for nf4_quantize (device outputs).
+ *   ws          : ql_workspace_size(QL_OP_QUANTIZE_HOST, 0, rows, cols, 0)
+ *                 bytes (the quantize scratch plus two staging chunks of about
+ *                 16 MB), 256-byte aligned.
+ *   copy_stream : the stream for the copies (may equal `stream`, then nothing
+ *                 overlaps); it first waits for the work already queued on
+ *                 `stream`, and `stream` waits for each chunk's copy.
+ * When the call returns the work is queued; the caller keeps W_host unchanged
+ * until `stream` has passed it.  The call creates and releases a few CUDA
+ * events (no device memory).
+ */
+QL_API int nf4_quantize_host(const uint16_t *W_host, const ql_nf4_tensor *q, void *ws, size_t ws_bytes,
+                             ql_stream_t copy_stream, ql_stream_t stream);
 
 /*
  * Row-sharded quantization for data-parallel training (the QLoRA project

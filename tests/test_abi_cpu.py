@@ -213,3 +213,16 @@ def test_unknown_quant_type_is_rejected_on_host(ql):
     s = ql.NF4Struct(256, 512, 64, 256, p, None, p, p, p, 5)
     assert ql.lib.nf4_dequantize(ctypes.byref(s), p, None) == ql.QL_ERR_UNSUPPORTED
     assert "quant_type 5" in ql.lib.ql_last_error().decode()
+
+
+def test_quantize_host_rejects_bad_arguments_on_host(ql):
+    _fake_pointers_only_without_gpu()
+    lib, E = ql.lib, ql
+    p = ctypes.c_void_p(0x10000)
+    s = ql.NF4Struct(256, 512, 64, 256, p, None, p, p, p)
+    need = ql.workspace_size(ql.OP_QUANTIZE_HOST, 0, 256, 512, 0)
+    assert need > ql.workspace_size(ql.OP_QUANTIZE, 0, 256, 512, 0)
+    assert lib.nf4_quantize_host(None, ctypes.byref(s), p, need, None, None) == E.QL_ERR_INVALID
+    assert lib.nf4_quantize_host(p, ctypes.byref(s), p, need - 1, None, None) == E.QL_ERR_UNSUPPORTED
+    assert lib.nf4_quantize_host(p, ctypes.byref(s), ctypes.c_void_p(0x10010), need, None, None) == \
+        E.QL_ERR_MISALIGNED

@@ -182,3 +182,28 @@ def test_fp4_every_bf16_value(ql):
     torch.cuda.synchronize()
     assert np.array_equal(q.packed.cpu().numpy(), ref["packed"])
     assert np.array_equal(_bits(ql.nf4_dequantize(q)), nf4.dequantize(ref))
+
+
+@pytest.mark.parametrize("rows,cols,pinned,dq", [(4096, 4096, True, 256), (1000, 11008, True, 256),
+                                                 (37, 4160, False, 256), (3000, 2048, False, 0)])
+def test_quantize_on_load_equals_device_quantize(ql, rows, cols, pinned, dq):
+    """nf4_quantize_host streams a host weight through two staging chunks
+    (copies on their own stream overlapping the coding): the result equals
+    quantizing the same weight already on the device, bit for bit, and the
+    oracle's codes."""
+    from bit_nf4_quantized_38_b300.workloads import normal_with_outliers_bf16
+    W = normal_with_outliers_bf16((rows, cols), 0.02, 0.001, 20.0, seed=rows + cols)
+    Wh = W.pin_memory() if pinned else W.clone()
+    dev = torch.device("cuda")
+    copy = torch.cuda.Stream()
+    got = ql.nf4_quantize_host(Wh, dev, dq_blocksize=dq, copy_stream=copy)
+    want = ql.nf4_quantize(W.to(dev), dq_blocksize=dq)
+    torch.cuda.synchronize()
+    ql.device_status()
+    for f in ("packed", "absmax", "absmax_code", "dq_step", "dq_mean"):
+        a, b = getattr(got, f), getattr(want, f)
+        assert (a is None) == (b is None), f
+        if a is not None:
+            assert torch.equal(a, b), f
+    if rows * cols <= 4096 * 4096:
+        _compare_quant(got, nf4.quantize(_bits(W), dq_blocksize=dq))
