@@ -1,0 +1,115 @@
+// Device helpers shared by the tensor-core GEMM kernels (internal): the
+// in-shared-memory dequantizer of one 64-element row-block and the bounded
+// waits used after an abort.
+#pragma once
+#include <cstdint>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace ql {
+
+// 8 bf16 values of one 16-byte smem chunk from 8 packed nibbles, through the
+// 16-entry table held as low-byte (TL) and high-byte (TH) planes.  Byte j of
+// `w` holds element 2j in its high nibble and element 2j+1 in its low nibble.
+__device__ __forceinline__ void lookup8(uint32_t w, const uint32_t (&TL)[4], const uint32_t (&TH)[4],
+                                        uint32_t &o0, uint32_t &o1, uint32_t &o2, uint32_t &o3) {
+  using ptx::prmt;
+  // selector: the low 3 bits of every nibble pick a byte among 8 entries
+  const uint32_t s = w & 0x77777777u;
+  // second-level selector: byte i from the first (entries 0-7) or second
+  // (entries 8-15) half, by bit 3 of nibble i
+  const uint32_t s2 = ((w >> 1) & 0x44444444u) | 0x32103210u;
+  {
+    uint32_t L = prmt(prmt(TL[0], TL[1], s), prmt(TL[2], TL[3], s), s2);
+    uint32_t H = prmt(prmt(TH[0], TH[1], s), prmt(TH[2], TH[3], s), s2);
+    // L, H bytes hold elements (1, 0, 3, 2); interleave to bf16 pairs (0,1), (2,3)
+    o0 = prmt(L, H, 0x4051u);
+    o1 = prmt(L, H, 0x6273u);
+  }
+  {
+    const uint32_t sh = s >> 16, s2h = s2 >> 16;
+    uint32_t L = prmt(prmt(TL[0], TL[1], sh), prmt(TL[2], TL[3], sh), s2h);
+    uint32_t H = prmt(prmt(TH[0], TH[1], sh), prmt(TH[2], TH[3], sh), s2h);
+    o2 = prmt(L, H, 0x4051u);
+    o3 = prmt(L, H, 0x6273u);
+  }
+}
+
+// One 64-element row-block: 32 packed bytes and the block constant -> one
+// 128-byte row of a 128B-swizzled tile at `dst` (chunk j stored at j ^ swz).
+__device__ __forceinline__ void convert_rowblock(const uint4 &p0, const uint4 &p1, float mhat,
+                                                 const float (&q)[16], uint32_t dst, uint32_t swz) {
+  uint32_t P[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) P[k] = pack_bf16x2(__fmul_rn(q[2 * k], mhat), __fmul_rn(q[2 * k + 1], mhat));
+  uint32_t TL[4], TH[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    TL[i] = ptx::prmt(P[2 * i], P[2 * i + 1], 0x6420u);
+    TH[i] = ptx::prmt(P[2 * i], P[2 * i + 1], 0x7531u);
+  }
+  const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t o0, o1, o2, o3;
+    lookup8(words[j], TL, TH, o0, o1, o2, o3);
+    ptx::sts128(dst + (((uint32_t)j ^ swz) << 4), o0, o1, o2, o3);
+  }
+}
+
+// Two row-blocks at once (independent instruction streams interleaved, for
+// latency hiding); both rows have the same swizzle phase `swz`.
+__device__ __forceinline__ void convert_rowblock2(const uint4 &a0, const uint4 &a1, float ma, const uint4 &b0,
+                                                  const uint4 &b1, float mb, const float (&q)[16], uint32_t dst_a,
+                                                  uint32_t dst_b, uint32_t swz) {
+  uint32_t TLa[4], THa[4], TLb[4], THb[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t pa0 = pack_bf16x2(__fmul_rn(q[4 * i], ma), __fmul_rn(q[4 * i + 1], ma));
+    const uint32_t pa1 = pack_bf16x2(__fmul_rn(q[4 * i + 2], ma), __fmul_rn(q[4 * i + 3], ma));
+    const uint32_t pb0 = pack_bf16x2(__fmul_rn(q[4 * i], mb), __fmul_rn(q[4 * i + 1], mb));
+    const uint32_t pb1 = pack_bf16x2(__fmul_rn(q[4 * i + 2], mb), __fmul_rn(q[4 * i + 3], mb));
+    TLa[i] = ptx::prmt(pa0, pa1, 0x6420u);
+    THa[i] = ptx::prmt(pa0, pa1, 0x7531u);
+    TLb[i] = ptx::prmt(pb0, pb1, 0x6420u);
+    THb[i] = ptx::prmt(pb0, pb1, 0x7531u);
+  }
+  const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+  const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t o0, o1, o2, o3, e0, e1, e2, e3;
+    lookup8(wa[j], TLa, THa, o0, o1, o2, o3);
+    lookup8(wb[j], TLb, THb, e0, e1, e2, e3);
+    const uint32_t off = ((uint32_t)j ^ swz) << 4;
+    ptx::sts128(dst_a + off, o0, o1, o2, o3);
+    ptx::sts128(dst_b + off, e0, e1, e2, e3);
+  }
+}
+
+// Wait for phase `parity` of a barrier for at most `limit_ns`, ignoring the
+// abort flag (used only after an abort, for work already in flight).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 100000000ull) {
+  const uint64_t t0 = ptx::globaltimer();
+#pragma unroll 1
+  while (!ptx::mbar_try_wait(bar, parity) && ptx::globaltimer() - t0 < limit_ns) {
+  }
+}
+
+// After an abort: a fixed 50 us pause so that tensor copies already issued
+// into shared memory land before the CTA exits (their barriers may never
+// complete, since the other roles stopped arriving on them).
+__device__ __forceinline__ void settle() {
+  const uint64_t t0 = ptx::globaltimer();
+#pragma unroll 1
+  while (ptx::globaltimer() - t0 < 50000ull) {
+  }
+}
+
+__device__ __forceinline__ void zero_row(uint32_t dst) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) ptx::sts128(dst + (j << 4), 0, 0, 0, 0);
+}
+
+}  // namespace ql

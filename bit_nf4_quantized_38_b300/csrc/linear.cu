@@ -1,10 +1,11 @@
 // Forward and backward of the frozen-NF4 linear with a LoRA adapter:
 // argument checks, workspace layout and the launch sequence on one stream.
 //
-// forward, M > 16 tokens (2 launches):
+// forward, M > 16 tokens (2 launches; 3 for M <= 128):
 //   1. XA = X A  -> XA_out (bf16) and XAs = bf16(s XA)     LoRA kernel
 //   2. Y  = X W_hat^T + XAs B                             tensor-core GEMM,
 //                                                          LoRA as extra K-steps
+//      (M <= 128: the few-token kernel, skinny.cu, and its fixup kernel)
 // forward, M <= 16: the decode path (decode.cu).
 // backward (4 launches, 5 when XA must be recomputed):
 //   0. XA = X A                                            (only without XA)
@@ -30,15 +31,17 @@ bool rank_ok(int r) { return r == 8 || r == 16 || r == 32 || r == 64 || r == 128
 bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 // forward workspace: XAs [M][r] bf16; backward: Gs [M][r] + recomputed XA [M][r];
-// with M <= 128 tokens either also holds the fp32 partials of the GEMM split
-// over its reduction.  Training workspaces have two halves; successive calls
-// on a stream alternate between them (see next_ws_half).
+// with M <= 128 tokens either also holds the fp32 partials of the GEMM (the
+// forward's few-token kernel, the backward's split over the reduction).
+// Training workspaces have two halves; successive calls on a stream
+// alternate between them (see next_ws_half).
 size_t part_bytes(int64_t M, int64_t Nout, int64_t Kred) {
   const int s = gemm_splits(M, Nout, Kred);
   return s > 1 ? up256((size_t)s * M * Nout * 4) : 0;
 }
+size_t fwd_part_bytes(int64_t M, int64_t N, int64_t K, int r) { return up256(skinny_part_bytes(M, N, K, r)); }
 size_t fwd_half(int64_t M, int64_t N, int64_t K, int r) {  // s XA bf16 [M][r], partials
-  return up256((size_t)M * r * 2) + part_bytes(M, N, K);
+  return up256((size_t)M * r * 2) + fwd_part_bytes(M, N, K, r);
 }
 size_t bwd_half(int64_t M, int64_t N, int64_t K, int r) {  // s G, XA: bf16 [M][r] each, partials
   return 2 * up256((size_t)M * r * 2) + part_bytes(M, K, N);
@@ -236,7 +239,7 @@ int linear_fwd(const LinearArgs &a) {
   const size_t half = fwd_half(M, N, K, r);
   char *wsh = static_cast<char *>(a.ws) + (next_ws_half(st) ? half : 0);
   uint16_t *xas = reinterpret_cast<uint16_t *>(wsh);
-  float *part = part_bytes(M, N, K) ? reinterpret_cast<float *>(wsh + up256((size_t)M * r * 2)) : nullptr;
+  float *part = fwd_part_bytes(M, N, K, r) ? reinterpret_cast<float *>(wsh + up256((size_t)M * r * 2)) : nullptr;
 
   const std::vector<Range> xa_reads = {range(a.X, (size_t)(M * K * 2)), range(a.A, (size_t)(K * r * 2))};
   std::vector<Range> xa_writes = {range(wsh, half)};

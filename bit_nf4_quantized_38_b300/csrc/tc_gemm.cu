@@ -26,6 +26,7 @@
 #include "common.cuh"
 #include "ptx.cuh"
 #include "tc_gemm.cuh"
+#include "convert.cuh"
 
 namespace ql {
 namespace {
@@ -58,79 +59,6 @@ struct GemmArgs {
   float *part;  // single-CTA kernel split over K (gridDim.z > 1): fp32 partials [splits][M][ldo]
   float q[16];
 };
-
-// 8 bf16 values of one 16-byte smem chunk from 8 packed nibbles, through the
-// 16-entry table held as low-byte (TL) and high-byte (TH) planes.  Byte j of
-// `w` holds element 2j in its high nibble and element 2j+1 in its low nibble.
-__device__ __forceinline__ void lookup8(uint32_t w, const uint32_t (&TL)[4], const uint32_t (&TH)[4],
-                                        uint32_t &o0, uint32_t &o1, uint32_t &o2, uint32_t &o3) {
-  using ptx::prmt;
-  // selector: the low 3 bits of every nibble pick a byte among 8 entries
-  const uint32_t s = w & 0x77777777u;
-  // second-level selector: byte i from the first (entries 0-7) or second
-  // (entries 8-15) half, by bit 3 of nibble i
-  const uint32_t s2 = ((w >> 1) & 0x44444444u) | 0x32103210u;
-  {
-    uint32_t L = prmt(prmt(TL[0], TL[1], s), prmt(TL[2], TL[3], s), s2);
-    uint32_t H = prmt(prmt(TH[0], TH[1], s), prmt(TH[2], TH[3], s), s2);
-    // L, H bytes hold elements (1, 0, 3, 2); interleave to bf16 pairs (0,1), (2,3)
-    o0 = prmt(L, H, 0x4051u);
-    o1 = prmt(L, H, 0x6273u);
-  }
-  {
-    const uint32_t sh = s >> 16, s2h = s2 >> 16;
-    uint32_t L = prmt(prmt(TL[0], TL[1], sh), prmt(TL[2], TL[3], sh), s2h);
-    uint32_t H = prmt(prmt(TH[0], TH[1], sh), prmt(TH[2], TH[3], sh), s2h);
-    o2 = prmt(L, H, 0x4051u);
-    o3 = prmt(L, H, 0x6273u);
-  }
-}
-
-// One 64-element row-block: 32 packed bytes and the block constant -> one
-// 128-byte row of a 128B-swizzled tile at `dst` (chunk j stored at j ^ swz).
-__device__ __forceinline__ void convert_rowblock(const uint4 &p0, const uint4 &p1, float mhat,
-                                                 const float (&q)[16], uint32_t dst, uint32_t swz) {
-  uint32_t P[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) P[k] = pack_bf16x2(__fmul_rn(q[2 * k], mhat), __fmul_rn(q[2 * k + 1], mhat));
-  uint32_t TL[4], TH[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    TL[i] = ptx::prmt(P[2 * i], P[2 * i + 1], 0x6420u);
-    TH[i] = ptx::prmt(P[2 * i], P[2 * i + 1], 0x7531u);
-  }
-  const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    uint32_t o0, o1, o2, o3;
-    lookup8(words[j], TL, TH, o0, o1, o2, o3);
-    ptx::sts128(dst + (((uint32_t)j ^ swz) << 4), o0, o1, o2, o3);
-  }
-}
-
-// Wait for phase `parity` of a barrier for at most `limit_ns`, ignoring the
-// abort flag (used only after an abort, for work already in flight).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 100000000ull) {
-  const uint64_t t0 = ptx::globaltimer();
-#pragma unroll 1
-  while (!ptx::mbar_try_wait(bar, parity) && ptx::globaltimer() - t0 < limit_ns) {
-  }
-}
-
-// After an abort: a fixed 50 us pause so that tensor copies already issued
-// into shared memory land before the CTA exits (their barriers may never
-// complete, since the other roles stopped arriving on them).
-__device__ __forceinline__ void settle() {
-  const uint64_t t0 = ptx::globaltimer();
-#pragma unroll 1
-  while (ptx::globaltimer() - t0 < 50000ull) {
-  }
-}
-
-__device__ __forceinline__ void zero_row(uint32_t dst) {
-#pragma unroll
-  for (int j = 0; j < 8; ++j) ptx::sts128(dst + (j << 4), 0, 0, 0, 0);
-}
 
 struct RowBlockSrc {
   uint4 p0, p1;
@@ -714,6 +642,20 @@ int make_tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer, 
   return QL_OK;
 }
 
+int make_tmap_packed(CUtensorMap *tm, const uint8_t *ptr, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return set_error(QL_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(QL_ERR_CUDA, "cuTensorMapEncodeTiled (packed) failed (%d)", (int)r);
+  return QL_OK;
+}
+
 namespace {
 
 template <bool kTrans, int NACC>
@@ -851,7 +793,8 @@ int launch_nf4_gemm(const GemmProblem &g, cudaStream_t st) {
   Spans &sp = g_spans;
   unsigned long long *span = (sp.on && sp.used < sp.capacity) ? sp.buf + 2 * sp.used : nullptr;
   int rc;
-  if (g.M <= 128) rc = g.trans ? launch<true>(g, span, st) : launch<false>(g, span, st);
+  if (!g.trans && g.M <= kSkinnyMaxM && g.part) rc = launch_nf4_skinny(g, span, st);
+  else if (g.M <= 128) rc = g.trans ? launch<true>(g, span, st) : launch<false>(g, span, st);
   else if (g.M <= 256) rc = g.trans ? launch_pair<true, 1>(g, span, st) : launch_pair<false, 1>(g, span, st);
   else rc = g.trans ? launch_pair<true, 2>(g, span, st) : launch_pair<false, 2>(g, span, st);
   const double flops = 2.0 * (double)g.M * (double)g.Nout * (double)(g.Kred + g.r);

@@ -44,8 +44,10 @@ struct GemmProblem {
   // (the previous library call writes neither): the CTA-pair kernel then
   // starts its main loop before its predecessor completes.
   bool early_main = false;
-  // fp32 partial buffer for the single-CTA kernel split over the reduction
-  // (M <= 128: gemm_splits(M, Nout, Kred) x M x Nout floats), or null (no split)
+  // fp32 partial buffer, or null: for the forward form with M <= 128 the
+  // few-token kernel's shares (skinny_part_bytes); for the transposed form
+  // the single-CTA kernel split over the reduction (M <= 128:
+  // gemm_splits(M, Nout, Kred) x M x Nout floats)
   float *part = nullptr;
 };
 int launch_nf4_gemm(const GemmProblem &g, cudaStream_t st);
@@ -58,6 +60,20 @@ int gemm_splits(int64_t M, int64_t Nout, int64_t Kred);
 // 2-D bf16 tensor map [outer][inner] (inner contiguous), box [box_outer][64],
 // 128-byte swizzle, zero fill outside the tensor.
 int make_tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_outer);
+
+// 2-D tensor map over packed NF4 bytes [rows][row_bytes], box [box_rows][128
+// bytes] (four 64-element blocks of each row), 128-byte swizzle (16-byte
+// piece j of row i stored at j xor (i mod 8)), zero fill.
+int make_tmap_packed(CUtensorMap *tm, const uint8_t *ptr, uint64_t row_bytes, uint64_t rows, uint32_t box_rows);
+
+// Few-token forward (16 < M <= 128): the transposed product on the tensor
+// cores, weight rows as the MMA M dimension and tokens as N, split over all
+// SMs by a stream-K partition of (128-row tile, K-step) units; fp32 partials
+// of tiles that several CTAs share are summed in a fixed order by a second
+// kernel.  `g.part` holds skinny_part_bytes(...) bytes.  Forward form only.
+constexpr int64_t kSkinnyMaxM = 128;
+size_t skinny_part_bytes(int64_t M, int64_t Nout, int64_t Kred, int r);
+int launch_nf4_skinny(const GemmProblem &g, unsigned long long *span, cudaStream_t st);
 
 // ---------------------------------------------------------------- LoRA side (tensor cores)
 // out = scale * (A op . B op^T) over a reduction index t:
