@@ -27,7 +27,9 @@
 //               K-steps by cp.async into 4 staging buffers, runs ahead
 //   warp 1      TMEM allocation (two accumulators of Mp columns, so the next
 //               segment's MMAs overlap the previous segment's epilogue) and
-//               the single MMA-issuing thread
+//               the single MMA-issuing thread, which waits on one barrier per
+//               step (a wait costs far more than an MMA issue once MMAs are in
+//               flight, and these MMAs are small)
 //   warp 2      TMA of the X tile (or the LoRA tiles) of each step
 //   warps 3-10  four converter groups of 2 warps taking K-steps in turn:
 //               each thread computes the m_hat of two row-blocks (rows r and
@@ -311,8 +313,8 @@ k_nf4_skinny(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CU
           if (!ptx::mbar_wait(tfree(acc), ((j - 2) >> 1) & 1, abort, p.status)) { ok = false; break; }
           ptx::tc_fence_after();
         }
+        // afull(s) also implies xfull: the group arrives after the X tile landed
         if (!ptx::mbar_wait(afull(sa.s), sa.ph, abort, p.status)) { ok = false; break; }
-        if (!ptx::mbar_wait(xfull(sx.s), sx.ph, abort, p.status)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t a_addr = sbase + sa.s * A_BYTES, x_addr = xbase + sx.s * p.x_bytes;
         const uint32_t d = tmem + (uint32_t)(acc * p.Mp);
@@ -355,7 +357,7 @@ k_nf4_skinny(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CU
     const float mean = p.w.dq ? __ldg(p.w.mean) : 0.0f;
     bool stores_ok = !p.early_main;
     Cursor c{t0, k0};
-    Slot sa{0, 0}, ps{0, 0};
+    Slot sa{0, 0}, ps{0, 0}, sx{0, 0};
     // the run of block constants the current main step belongs to
     RunCursor rc{0, Cursor{t0, k0}};
     Run run = rc.next(nsteps, p.ksm, p.upt);
@@ -373,7 +375,7 @@ k_nf4_skinny(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CU
       return __uint_as_float(ptx::lds32(sb + 4u * (uint32_t)rj));
     };
 #pragma unroll 1
-    for (int gs = 0; gs < nsteps; ++gs, c.next(p.upt), sa.next(ASTAGES)) {
+    for (int gs = 0; gs < nsteps; ++gs, c.next(p.upt), sa.next(ASTAGES), sx.next(xstages)) {
       const bool main_step = c.k < p.ksm;
       const uint32_t sb = stage_base + (uint32_t)(rn % SBUF) * SBUF_BYTES + (uint32_t)row * 64u;
       if (main_step && rj == 0) {
@@ -413,11 +415,13 @@ k_nf4_skinny(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CU
           const int kfirst = max(cq * PCHUNK, c.t == t0 ? k0 : 0);
           const int klast = min(cq * PCHUNK + PCHUNK, c.t == tl ? kl_end : p.ksm) - 1;
           ptx::mbar_arrive_cnt(pempty(ps.s), c.k == klast ? 1u + (uint32_t)(PCHUNK - (klast - kfirst + 1)) : 1u);
+          if (!ptx::mbar_wait(xfull(sx.s), sx.ph, abort, p.status)) break;
           ptx::mbar_arrive(afull(sa.s));
         } else {
           // LoRA step: A = B^T, B stored [r][N]: two MN-major atoms of 64
           // weight rows x 64 ranks, loaded by one thread of the group
           if (!ptx::mbar_wait(aempty(sa.s), sa.ph ^ 1, abort, p.status)) break;
+          if (!ptx::mbar_wait(xfull(sx.s), sx.ph, abort, p.status)) break;
           if ((cw & 1) == 0 && lane == 0) {
             const uint32_t a_dst = sbase + sa.s * A_BYTES;
             const int l = c.k - p.ksm;
@@ -481,9 +485,11 @@ k_nf4_skinny(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CU
 }
 
 // Y[m][n] = bf16(sum of the fp32 shares of tile n / 128 in CTA order), for
-// the tiles that more than one CTA shares; 8 outputs per thread.  A
-// programmatic dependent of k_nf4_skinny: waits for it before reading.
-__global__ void __launch_bounds__(256) k_skinny_fixup(const float *__restrict__ part, int64_t U, int G, int upt,
+// the tiles that more than one CTA shares; 8 outputs per thread.  The shares
+// are loaded 8 at a time before they are added (in CTA order), so the loads
+// overlap.  A programmatic dependent of k_nf4_skinny: waits for it before
+// reading.
+__global__ void __launch_bounds__(128) k_skinny_fixup(const float *__restrict__ part, int64_t U, int G, int upt,
                                                       int tiles, int M, int Mp, int Nout, uint16_t *__restrict__ out) {
   ptx::griddep_wait();
   ptx::griddep_launch();
@@ -498,13 +504,27 @@ __global__ void __launch_bounds__(256) k_skinny_fixup(const float *__restrict__ 
     const int64_t ua = (int64_t)t * upt;
     const int cf = owner_of(ua, U, G), cl = owner_of(ua + upt - 1, U, G);
     if (cf == cl) continue;
-    const float *src = part + ((int64_t)(cf + t) * Mp + m) * TBM + i8 * 8;
-    float4 a = __ldcg(reinterpret_cast<const float4 *>(src)), b = __ldcg(reinterpret_cast<const float4 *>(src) + 1);
-    for (int c = cf + 1; c <= cl; ++c) {
-      const float4 *ps = reinterpret_cast<const float4 *>(part + ((int64_t)(c + t) * Mp + m) * TBM + i8 * 8);
-      const float4 x = __ldcg(ps), y = __ldcg(ps + 1);
-      a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
-      b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+    for (int c0 = cf; c0 <= cl; c0 += 8) {
+      float4 x[8], y[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (c0 + i <= cl) {
+          const float4 *ps = reinterpret_cast<const float4 *>(part + ((int64_t)(c0 + i + t) * Mp + m) * TBM + i8 * 8);
+          x[i] = __ldcg(ps);
+          y[i] = __ldcg(ps + 1);
+        }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (c0 + i <= cl) {
+          if (c0 + i == cf) {
+            a = x[i];
+            b = y[i];
+          } else {
+            a.x += x[i].x; a.y += x[i].y; a.z += x[i].z; a.w += x[i].w;
+            b.x += y[i].x; b.y += y[i].y; b.z += y[i].z; b.w += y[i].w;
+          }
+        }
     }
     *reinterpret_cast<uint4 *>(out + (int64_t)m * Nout + n) =
         make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
@@ -515,7 +535,8 @@ struct Geometry {
   int Mp, ksm, ksl, upt, tiles, G;
   int64_t U;
 };
-Geometry geometry(int64_t M, int64_t Nout, int64_t Kred, int r) {
+// cta_cap: CTAs the split may use (at most kCtas)
+Geometry geometry(int64_t M, int64_t Nout, int64_t Kred, int r, int cta_cap = kCtas) {
   Geometry g{};
   g.Mp = (int)((M + 31) / 32 * 32);
   g.ksm = (int)((Kred + TBK - 1) / TBK);
@@ -523,7 +544,7 @@ Geometry geometry(int64_t M, int64_t Nout, int64_t Kred, int r) {
   g.upt = g.ksm + g.ksl;
   g.tiles = (int)((Nout + TBM - 1) / TBM);
   g.U = (int64_t)g.tiles * g.upt;
-  g.G = (int)std::min<int64_t>(g.U, kCtas);
+  g.G = (int)std::min<int64_t>(g.U, std::min(cta_cap, kCtas));
   return g;
 }
 
@@ -547,7 +568,12 @@ int launch_nf4_skinny(const GemmProblem &gp, unsigned long long *span, cudaStrea
     if (rc) return rc;
     attr_done[dev] = true;
   }
-  const Geometry geo = geometry(gp.M, gp.Nout, gp.Kred, gp.r);
+  // With early_main this kernel runs alongside the LoRA kernel that makes XAs
+  // (one CTA per split of its reduction): leave it those SMs, so that no CTA
+  // of this kernel (which fills an SM) waits for it to finish.  The partial
+  // buffer, sized for kCtas CTAs, has room for any smaller split.
+  const int cap = gp.early_main ? kCtas - lora_splits(gp.M, gp.Kred) * (int)((gp.M + 127) / 128) : kCtas;
+  const Geometry geo = geometry(gp.M, gp.Nout, gp.Kred, gp.r, cap);
   CUtensorMap tP, tX, tB, tXA;
   int rc = make_tmap_packed(&tP, gp.w.packed, (uint64_t)gp.Kred / 2, (uint64_t)gp.Nout, TBM);
   if (!rc) rc = make_tmap(&tX, gp.A, (uint64_t)gp.Kred, (uint64_t)gp.M, (uint32_t)geo.Mp);
@@ -594,8 +620,8 @@ int launch_nf4_skinny(const GemmProblem &gp, unsigned long long *span, cudaStrea
   if (rc) return rc;
   const int64_t items = (int64_t)geo.tiles * gp.M * (TBM / 8);
   cudaLaunchConfig_t fc{};
-  fc.gridDim = dim3((unsigned)std::min<int64_t>((items + 255) / 256, 148 * 8));
-  fc.blockDim = dim3(256);
+  fc.gridDim = dim3((unsigned)std::min<int64_t>((items + 127) / 128, 148 * 16));
+  fc.blockDim = dim3(128);
   fc.stream = st;
   fc.attrs = attr;
   fc.numAttrs = 1;
