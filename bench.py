@@ -370,7 +370,8 @@ def run_reference(args):
 
 def clone_nf4(ql, q):
     import torch
-    t = ql.NF4Tensor(q.rows, q.cols, q.packed.clone(), blocksize=q.blocksize, dq_blocksize=q.dq_blocksize)
+    t = ql.NF4Tensor(q.rows, q.cols, q.packed.clone(), blocksize=q.blocksize, dq_blocksize=q.dq_blocksize,
+                     quant_type=q.quant_type, dq_type=q.dq_type)
     for f in ("absmax", "absmax_code", "dq_step", "dq_mean"):
         v = getattr(q, f)
         setattr(t, f, None if v is None else v.clone())

@@ -57,6 +57,8 @@ int check_tensor(const ql_nf4_tensor *q, const char *fn, bool need_absmax_dq_off
   if (!q->packed) return set_error(QL_ERR_INVALID, "%s: null packed", fn);
   if (!aligned(q->packed, 16)) return set_error(QL_ERR_MISALIGNED, "%s: packed not 16-byte aligned", fn);
   if (q->dq_blocksize) {
+    if (q->dq_type != QL_DQ_INT8 && q->dq_type != QL_DQ_E4M3)
+      return set_error(QL_ERR_UNSUPPORTED, "%s: dq_type %d (0 = int8, 1 = E4M3)", fn, q->dq_type);
     if (!q->absmax_code || !q->dq_step || !q->dq_mean)
       return set_error(QL_ERR_INVALID, "%s: null double-quant array", fn);
     if (!aligned(q->absmax_code, 16) || !aligned(q->dq_step, 16) || !aligned(q->dq_mean, 4))
@@ -151,7 +153,7 @@ int quantize_second(const ql_nf4_tensor *q, void *ws, int64_t total_blocks, cuda
   if (!q->dq_blocksize) return QL_OK;
   const int64_t n_b = q->rows * q->cols / 64;
   float *absmax = reinterpret_cast<float *>(static_cast<char *>(ws) + 256);
-  return check_cuda(launch_double_quant(absmax, n_b, total_blocks, q->dq_blocksize, static_cast<double *>(ws),
+  return check_cuda(launch_double_quant(absmax, n_b, total_blocks, q->dq_blocksize, q->dq_type, static_cast<double *>(ws),
                                         q->absmax_code, q->dq_step, q->dq_mean, st),
                     "quantize: double-quant launch");
 }
@@ -295,7 +297,7 @@ extern "C" int nf4_quantize_host(const uint16_t *W_host, const ql_nf4_tensor *q,
     if (!rc) rc = check_cuda(cudaEventRecord(ev[3 + h], st), "nf4_quantize_host: record");
   }
   if (!rc && q->dq_blocksize)
-    rc = check_cuda(launch_double_quant(absmax, N * K / 64, N * K / 64, q->dq_blocksize, sum, q->absmax_code,
+    rc = check_cuda(launch_double_quant(absmax, N * K / 64, N * K / 64, q->dq_blocksize, q->dq_type, sum, q->absmax_code,
                                         q->dq_step, q->dq_mean, st),
                     "nf4_quantize_host: double-quant launch");
   for (auto &e : ev)

@@ -66,13 +66,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// E4M3 (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent
+// 0 holds the subnormals m * 2^-9; largest finite 448 = 0x7E) from its
+// definition.  Value of a code byte:
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  const uint32_t e = (code >> 3) & 15u, m = code & 7u;
+  const float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;
+  return (code & 0x80u) ? -v : v;
+}
+// Code of a finite fp32 x: round to nearest, ties to the even code,
+// saturating at +-448 (the sign of x is kept, so -0 and negative values that
+// round to 0 give 0x80).
+__device__ __forceinline__ uint32_t e4m3_code(float x) {
+  const uint32_t b = __float_as_uint(x), s = (b >> 24) & 0x80u;
+  const float a = fabsf(x);
+  if (!(a < 448.0f)) return s | 0x7Eu;
+  if (a < 0.015625f) return s | (uint32_t)rintf(a * 512.0f);  // subnormal grid; 8 is 2^-6 (code 0x08)
+  const uint32_t e = (b >> 23) & 0xFFu, mant = b & 0x7FFFFFu;
+  uint32_t q = mant >> 20;
+  const uint32_t rem = mant & 0xFFFFFu;
+  if (rem > 0x80000u || (rem == 0x80000u && (q & 1u))) ++q;  // a carry into the exponent is right
+  return s | (((e - 120u) << 3) + q);
+}
+// Value of a second-level code byte (ql_nf4_tensor.dq_type).
+__device__ __forceinline__ float dq_code_value(int8_t raw, int dq_type) {
+  return dq_type == QL_DQ_E4M3 ? e4m3_value((uint8_t)raw) : (float)raw;
+}
+
 // ---------------------------------------------------------------------------
 // launchers (quant.cu)
 
 cudaError_t launch_quantize(const uint16_t *W, int64_t rows, int64_t cols, int quant_type, uint8_t *packed,
                             float *absmax, double *sum_acc, cudaStream_t st);
 // mu = fl32(sum / total_blocks); codes and steps of the n_b blocks given.
-cudaError_t launch_double_quant(const float *absmax, int64_t n_b, int64_t total_blocks, int dq_bs,
+cudaError_t launch_double_quant(const float *absmax, int64_t n_b, int64_t total_blocks, int dq_bs, int dq_type,
                                 const double *sum, int8_t *code, float *step, float *mean, cudaStream_t st);
 cudaError_t launch_dequantize(const ql_nf4_tensor &q, uint16_t *W_out, cudaStream_t st);
 

@@ -150,6 +150,7 @@ struct StreamArgs {  // N K / 64 < 2^31 and units < 2^31 (checked on the host)
   int nbox;        // ceil(K / 256)
   int W;           // units = row groups x nbox
   int dq;          // block constants by double quantization (else fp32 absmax)
+  int dqt;         // second-level code (QL_DQ_INT8 or QL_DQ_E4M3)
   int w_early;     // the weight may be read before the previous grid completes
   int x_early;     // so may X and A
   int ws_early;    // and this call's workspace half may be written
@@ -363,7 +364,7 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
       if (row < a.N) {
         const int bi = row * nb_row + kb;
         if (a.dq) {
-          p.a[k] = (float)__ldg(a.code + bi);
+          p.a[k] = dq_code_value(__ldg(a.code + bi), a.dqt);
           p.b[k] = __ldg(a.step + (bi >> 8));
         } else {
           p.a[k] = __ldg(a.absmax + bi);
@@ -862,6 +863,7 @@ int launch_decode(const DecodeProblem &p, cudaStream_t st, bool *early_dependent
   a.nbox = (int)((p.K + UNIT_K - 1) / UNIT_K);
   a.W = (int)(groups * a.nbox);
   a.dq = p.w.dq ? 1 : 0;
+  a.dqt = p.w.dqt;
   a.w_early = p.w_early ? 1 : 0;
   a.x_early = (p.w_early && p.x_early) ? 1 : 0;
   a.ws_early = p.ws_early ? 1 : 0;

@@ -33,6 +33,7 @@ struct MergeArgs {
   const float *mean;
   const float *absmax;
   int dq;
+  int dqt;  // second-level code (QL_DQ_INT8 or QL_DQ_E4M3)
   int N, K, r, rp;  // rp = r rounded up to 16
   const uint16_t *A;  // [K][r]
   const uint16_t *B;  // [r][N]
@@ -112,7 +113,7 @@ __global__ void __launch_bounds__(MTHREADS) k_merge(const __grid_constant__ Merg
     float m = 0.0f;
     if (nr < nrows && kb * 64 < kcols) {
       const int64_t b = (int64_t)(n0 + nr) * (a.K / 64) + k0 / 64 + kb;
-      m = a.dq ? __fadd_rn(__fmul_rn((float)__ldg(a.code + b), __ldg(a.step + (b >> 8))), __ldg(a.mean))
+      m = a.dq ? __fadd_rn(__fmul_rn(dq_code_value(__ldg(a.code + b), a.dqt), __ldg(a.step + (b >> 8))), __ldg(a.mean))
                : __ldg(a.absmax + b);
     }
     sM[i] = m;
@@ -188,6 +189,7 @@ int launch_merge(const ql_nf4_tensor &W, const uint16_t *A, const uint16_t *B, i
   MergeArgs a{};
   a.packed = W.packed; a.code = W.absmax_code; a.step = W.dq_step; a.mean = W.dq_mean; a.absmax = W.absmax;
   a.dq = W.dq_blocksize ? 1 : 0;
+  a.dqt = W.dq_type;
   a.N = (int)W.rows; a.K = (int)W.cols; a.r = r; a.rp = rp;
   a.A = A; a.B = B; a.scale = scale; a.out = out;
   const Codebook &cb = codebook(W.quant_type);

@@ -204,7 +204,7 @@ k_quantize(const uint4 *__restrict__ W, int64_t n_blocks, Codebook cb, uint4 *__
 
 __global__ void __launch_bounds__(256)
 k_double_quant(const float *__restrict__ absmax, int64_t n_b, int64_t total_blocks, const double *__restrict__ sum,
-               int8_t *__restrict__ code, float *__restrict__ step, float *__restrict__ mean) {
+               int dq_type, int8_t *__restrict__ code, float *__restrict__ step, float *__restrict__ mean) {
   __shared__ float red[8];
   __shared__ float mu_s;
   // mu once per CTA (an fp64 division is slow; every thread taking one was
@@ -226,13 +226,18 @@ k_double_quant(const float *__restrict__ absmax, int64_t n_b, int64_t total_bloc
 #pragma unroll
     for (int k = 1; k < 8; ++k) a2 = fmaxf(a2, red[k]);
     __syncthreads();  // red is rewritten by the next group
-    const float st = __fdiv_rn(a2, 127.0f);
+    const bool e4m3 = dq_type == QL_DQ_E4M3;
+    const float st = __fdiv_rn(a2, e4m3 ? 448.0f : 127.0f);
     if (valid) {
       int k = 0;
       if (st != 0.0f) {
-        float t = rintf(__fdiv_rn(c, st));
-        t = fminf(fmaxf(t, -127.0f), 127.0f);
-        k = (int)t;
+        const float x = __fdiv_rn(c, st);
+        if (e4m3) {
+          k = (int)(int8_t)(uint8_t)e4m3_code(x);
+        } else {
+          const float t = fminf(fmaxf(rintf(x), -127.0f), 127.0f);
+          k = (int)t;
+        }
       }
       code[i] = (int8_t)k;
     }
@@ -243,7 +248,7 @@ k_double_quant(const float *__restrict__ absmax, int64_t n_b, int64_t total_bloc
 
 template <bool kDQ>
 __global__ void __launch_bounds__(kThreads)
-k_dequantize(const uint32_t *__restrict__ packed, int64_t n_blocks, const int8_t *__restrict__ code,
+k_dequantize(const uint32_t *__restrict__ packed, int64_t n_blocks, const int8_t *__restrict__ code, int dq_type,
              const float *__restrict__ step, const float *__restrict__ mean,
              const float *__restrict__ absmax, Codebook cb, uint4 *__restrict__ out) {
   __shared__ float qtab[16 * 32];  // one copy of the levels per lane
@@ -265,7 +270,7 @@ k_dequantize(const uint32_t *__restrict__ packed, int64_t n_blocks, const int8_t
       mh[u] = 0.0f;
       if (b < n_blocks) {
         wd[u] = __ldg(packed + b * 8 + sub);
-        if (kDQ) mh[u] = __fadd_rn(__fmul_rn((float)__ldg(code + b), __ldg(step + (b >> 8))), mu);
+        if (kDQ) mh[u] = __fadd_rn(__fmul_rn(dq_code_value(__ldg(code + b), dq_type), __ldg(step + (b >> 8))), mu);
         else mh[u] = __ldg(absmax + b);
       }
     }
@@ -346,7 +351,7 @@ cudaError_t launch_quantize(const uint16_t *W, int64_t rows, int64_t cols, int q
   return cudaGetLastError();
 }
 
-cudaError_t launch_double_quant(const float *absmax, int64_t n_b, int64_t total_blocks, int dq_bs,
+cudaError_t launch_double_quant(const float *absmax, int64_t n_b, int64_t total_blocks, int dq_bs, int dq_type,
                                 const double *sum, int8_t *code, float *step, float *mean, cudaStream_t st) {
   (void)dq_bs;  // 256, checked by the caller
   const int64_t n_2 = (n_b + 255) / 256;
@@ -358,7 +363,7 @@ cudaError_t launch_double_quant(const float *absmax, int64_t n_b, int64_t total_
     if (sms <= 0) sms = 148;
   }
   const int64_t grid = std::min<int64_t>(n_2, (int64_t)sms * 8);
-  k_double_quant<<<(unsigned)grid, 256, 0, st>>>(absmax, n_b, total_blocks, sum, code, step, mean);
+  k_double_quant<<<(unsigned)grid, 256, 0, st>>>(absmax, n_b, total_blocks, sum, dq_type, code, step, mean);
   count_launch();
   return cudaGetLastError();
 }
@@ -369,10 +374,10 @@ cudaError_t launch_dequantize(const ql_nf4_tensor &q, uint16_t *W_out, cudaStrea
   const uint32_t *p = reinterpret_cast<const uint32_t *>(q.packed);
   uint4 *o = reinterpret_cast<uint4 *>(W_out);
   if (q.dq_blocksize)
-    k_dequantize<true><<<g, kThreads, 0, st>>>(p, n_blocks, q.absmax_code, q.dq_step, q.dq_mean,
+    k_dequantize<true><<<g, kThreads, 0, st>>>(p, n_blocks, q.absmax_code, q.dq_type, q.dq_step, q.dq_mean,
                                                nullptr, codebook(q.quant_type), o);
   else
-    k_dequantize<false><<<g, kThreads, 0, st>>>(p, n_blocks, nullptr, nullptr, nullptr, q.absmax,
+    k_dequantize<false><<<g, kThreads, 0, st>>>(p, n_blocks, nullptr, 0, nullptr, nullptr, q.absmax,
                                                 codebook(q.quant_type), o);
   count_launch();
   return cudaGetLastError();

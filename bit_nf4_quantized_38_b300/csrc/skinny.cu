@@ -368,7 +368,7 @@ k_nf4_skinny(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CU
       if (p.w.dq) {
         const int off = (int)(b0 & 3) + rj;  // byte of the staged code words
         const uint32_t word = ptx::lds32(sb + 4u * (uint32_t)(off >> 2));
-        const float code = (float)(int8_t)(word >> (8 * (off & 3)));
+        const float code = dq_code_value((int8_t)(word >> (8 * (off & 3))), p.w.dqt);
         const bool second = ((b0 + rj) >> 8) != (b0 >> 8);
         return __fadd_rn(__fmul_rn(code, __uint_as_float(ptx::lds32(sb + (second ? 28u : 24u)))), mean);
       }

@@ -75,7 +75,7 @@ __device__ __forceinline__ RowBlockSrc load_rowblock(const NF4View &w, int64_t n
     r.p1 = ptx::ldg_nc_v4(src + 16);
     const int64_t b = n * (w.cols >> 6) + kb;
     if (w.dq)
-      r.mhat = __fadd_rn(__fmul_rn((float)__ldg(w.code + b), __ldg(w.step + (b >> 8))), __ldg(w.mean));
+      r.mhat = __fadd_rn(__fmul_rn(dq_code_value(__ldg(w.code + b), w.dqt), __ldg(w.step + (b >> 8))), __ldg(w.mean));
     else
       r.mhat = __ldg(w.absmax + b);
   } else {

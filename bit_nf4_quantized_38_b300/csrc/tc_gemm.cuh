@@ -15,12 +15,13 @@ struct NF4View {
   const float *absmax;
   int64_t rows, cols;
   int dq;
-  int qt;  // quant type: the code table the codes index
+  int qt;   // quant type: the code table the codes index
+  int dqt;  // second-level code (QL_DQ_INT8 or QL_DQ_E4M3)
 };
 
 inline NF4View nf4_view(const ql_nf4_tensor &t) {
   return NF4View{t.packed, t.absmax_code, t.dq_step, t.dq_mean, t.absmax, t.rows, t.cols, t.dq_blocksize != 0,
-                 t.quant_type};
+                 t.quant_type, t.dq_type};
 }
 
 // out[M][Nout] = A[M][Kred] . op(W_hat) + A2[M][r] . op2(B2)

@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libq
 
 QL_OK, QL_ERR_INVALID, QL_ERR_UNSUPPORTED, QL_ERR_MISALIGNED, QL_ERR_CUDA, QL_ERR_TIMEOUT = range(6)
 QL_NF4, QL_FP4 = 0, 1
+QL_DQ_INT8, QL_DQ_E4M3 = 0, 1  # second-level codes (ql_nf4_tensor.dq_type)
 OP_QUANTIZE, OP_DEQUANTIZE, OP_LINEAR_FWD, OP_LINEAR_BWD, OP_QUANTIZE_HOST = range(5)
 
 _c_i64, _c_i32, _c_f32, _c_p, _c_sz = (ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
@@ -24,7 +25,7 @@ _c_i64, _c_i32, _c_f32, _c_p, _c_sz = (ctypes.c_int64, ctypes.c_int32, ctypes.c_
 class NF4Struct(ctypes.Structure):
     _fields_ = [("rows", _c_i64), ("cols", _c_i64), ("blocksize", _c_i32), ("dq_blocksize", _c_i32),
                 ("packed", _c_p), ("absmax", _c_p), ("absmax_code", _c_p), ("dq_step", _c_p),
-                ("dq_mean", _c_p), ("quant_type", _c_i32)]
+                ("dq_mean", _c_p), ("quant_type", _c_i32), ("dq_type", _c_i32)]
 
 
 _SIGNATURES = {
@@ -186,12 +187,13 @@ class NF4Tensor:
     blocksize: int = 64
     dq_blocksize: int = 256
     quant_type: int = QL_NF4
+    dq_type: int = QL_DQ_INT8
 
     @classmethod
-    def empty(cls, rows, cols, device, dq_blocksize=256, blocksize=64, quant_type=QL_NF4):
+    def empty(cls, rows, cols, device, dq_blocksize=256, blocksize=64, quant_type=QL_NF4, dq_type=QL_DQ_INT8):
         n_b = rows * cols // blocksize
         t = cls(rows, cols, torch.empty(rows * cols // 2, dtype=torch.uint8, device=device),
-                blocksize=blocksize, dq_blocksize=dq_blocksize, quant_type=quant_type)
+                blocksize=blocksize, dq_blocksize=dq_blocksize, quant_type=quant_type, dq_type=dq_type)
         if dq_blocksize:
             t.absmax_code = torch.empty(n_b, dtype=torch.int8, device=device)
             t.dq_step = torch.empty((n_b + dq_blocksize - 1) // dq_blocksize, dtype=torch.float32,
@@ -204,7 +206,7 @@ class NF4Tensor:
     def struct(self):
         return NF4Struct(self.rows, self.cols, self.blocksize, self.dq_blocksize,
                          _ptr(self.packed), _ptr(self.absmax), _ptr(self.absmax_code),
-                         _ptr(self.dq_step), _ptr(self.dq_mean), self.quant_type)
+                         _ptr(self.dq_step), _ptr(self.dq_mean), self.quant_type, self.dq_type)
 
     def nbytes(self):
         return sum(t.numel() * t.element_size() for t in
@@ -212,11 +214,14 @@ class NF4Tensor:
                    if t is not None)
 
 
-def nf4_quantize(W, dq_blocksize=256, blocksize=64, out=None, ws=None, stream=None, quant_type=QL_NF4):
-    """Quantize a bf16 (rows x cols) CUDA tensor to NF4 (or FP4) codes (+ double quant)."""
+def nf4_quantize(W, dq_blocksize=256, blocksize=64, out=None, ws=None, stream=None, quant_type=QL_NF4,
+                 dq_type=QL_DQ_INT8):
+    """Quantize a bf16 (rows x cols) CUDA tensor to NF4 (or FP4) codes (+ double
+    quant with int8 or E4M3 second-level codes)."""
     _need(W, torch.bfloat16, "W")
     rows, cols = W.shape
-    q = out if out is not None else NF4Tensor.empty(rows, cols, W.device, dq_blocksize, blocksize, quant_type)
+    q = out if out is not None else NF4Tensor.empty(rows, cols, W.device, dq_blocksize, blocksize, quant_type,
+                                                    dq_type)
     ws, nbytes = _workspace(workspace_size(OP_QUANTIZE, 0, rows, cols, 0), W.device, ws)
     s = q.struct()
     _check(lib.nf4_quantize(_ptr(W), ctypes.byref(s), _ptr(ws), nbytes, _stream(stream)))
@@ -235,7 +240,7 @@ def nf4_quantize_noalloc(W, dq_blocksize=256, blocksize=64, out=None, stream=Non
 
 
 def nf4_quantize_host(W_host, device, dq_blocksize=256, blocksize=64, out=None, ws=None, stream=None,
-                      copy_stream=None, quant_type=QL_NF4):
+                      copy_stream=None, quant_type=QL_NF4, dq_type=QL_DQ_INT8):
     """Quantize a bf16 (rows x cols) CPU tensor into NF4 on `device` while it
     streams to the GPU (quantize-on-load; see include/qlora.h).  Pinned
     memory lets the copies overlap the kernels.  Keep W_host alive and
@@ -244,7 +249,7 @@ def nf4_quantize_host(W_host, device, dq_blocksize=256, blocksize=64, out=None, 
         raise ValueError("W_host must be a contiguous bf16 CPU tensor")
     rows, cols = W_host.shape
     device = torch.device(device)
-    q = out if out is not None else NF4Tensor.empty(rows, cols, device, dq_blocksize, blocksize, quant_type)
+    q = out if out is not None else NF4Tensor.empty(rows, cols, device, dq_blocksize, blocksize, quant_type, dq_type)
     ws, nbytes = _workspace(workspace_size(OP_QUANTIZE_HOST, 0, rows, cols, 0), device, ws)
     s = q.struct()
     st = _stream(stream)

@@ -74,14 +74,28 @@ enum ql_op {
  *                    the HIGH nibble of byte j, element 2j+1 the low nibble.
  *   absmax         : n_b = rows*cols/64 floats, the block absmax values.
  *                    Required when dq_blocksize == 0; ignored otherwise.
- *   absmax_code    : n_b int8 second-level codes   (dq_blocksize != 0)
+ *   absmax_code    : n_b 8-bit second-level codes  (dq_blocksize != 0):
+ *                    int8 or E4M3 bytes, as dq_type says
  *   dq_step        : n_2 = ceil(n_b/256) floats     (dq_blocksize != 0)
  *   dq_mean        : 1 float                         (dq_blocksize != 0)
  *   quant_type     : QL_NF4 (0, the default) or QL_FP4 (1): which 16-level
  *                    code table the 4-bit codes index (see ql_codebook).
+ *   dq_type        : QL_DQ_INT8 (0, the default) or QL_DQ_E4M3 (1): the
+ *                    8-bit code of the second level (see below).
  * Block b = row*(cols/64) + j covers row `row`, columns [64j, 64j+64).
  * Decoded block constant: dq off: absmax[b];
- *   dq on: fl32(fl32(absmax_code[b] * dq_step[b/256]) + dq_mean[0]).
+ *   dq on: fl32(fl32(v(absmax_code[b]) * dq_step[b/256]) + dq_mean[0]), where
+ *   v is the code's value: the int8 itself (QL_DQ_INT8), or the E4M3 number
+ *   the byte encodes (QL_DQ_E4M3: sign, 4-bit exponent with bias 7, 3-bit
+ *   mantissa, subnormals at exponent 0, largest finite 448, byte 0x7F/0xFF
+ *   never written).
+ * Second-level quantization (QLoRA abstract, innovation (b): the
+ *   quantization constants are themselves quantized; group of 256): c_b =
+ *   fl32(absmax_b - mu), a2 = max |c_b| over the group, dq_step =
+ *   fl32(a2 / L) with L = 127 (int8) or 448 (E4M3), code = the nearest code
+ *   value to fl32(c_b / dq_step) (int8: round half to even, clamped to
+ *   +-127; E4M3: round to nearest, ties to the even code, saturating at
+ *   +-448); a group with a2 = 0 gets step 0 and codes 0.
  * Dequantized weight: bf16_rne(fl32(q[code] * constant)), q = the code table.
  */
 typedef struct {
@@ -95,7 +109,14 @@ typedef struct {
   float *dq_step;
   float *dq_mean;
   int32_t quant_type;
+  int32_t dq_type;
 } ql_nf4_tensor;
+
+/* Second-level codes (ql_nf4_tensor.dq_type). */
+enum ql_dq_type {
+  QL_DQ_INT8 = 0, /* linear int8, step = a2 / 127 */
+  QL_DQ_E4M3 = 1  /* 8-bit float E4M3, step = a2 / 448 */
+};
 
 /* Code tables (ql_nf4_tensor.quant_type). */
 enum ql_quant_type {

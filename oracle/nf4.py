@@ -37,6 +37,16 @@ Readings taken where the pages are silent:
      -127, 127) (0 when step is 0).  Decode: fl32(fl32(code * step) + mu),
      with no fused multiply-add.
   R6 Dequantized weight: w_hat = bf16_rne(fl32(q[code] * absmax_hat)).
+  R21 The second-level code may instead be an 8-bit float (the pages only
+     say the constants are quantized): E4M3, the plainest 8-bit float that
+     keeps 3 mantissa bits (1 sign bit, 4 exponent bits with bias 7,
+     subnormals m * 2^-9 at exponent 0, largest finite 448, no infinities;
+     bytes 0x7F/0xFF are NaN and never produced).  Same groups and mu as R5;
+     step = fl32(max|c| / 448); code = the E4M3 value nearest to
+     fl32(c / step), ties to the even code (mantissa bit 0 clear), magnitudes
+     above 448 saturating to 448, the sign of the quotient kept (a negative
+     quotient that rounds to zero is byte 0x80); decode
+     fl32(fl32(value(code) * step) + mu).
   R17 FP4 (the 4-bit float the pages say NF4 beats; its format is not on the
      pages): the plainest 4-bit float, E2M1 (values 0, 0.5, 1, 1.5, 2, 3, 4, 6
      and negatives), scaled by 1/6 to [-1, 1]; codes index the ascending
@@ -59,6 +69,7 @@ from .bf16 import bf16_bits_to_f32, f32_to_bf16_bits
 
 BLOCKSIZE = 64
 DQ_BLOCKSIZE = 256
+DQ_INT8, DQ_E4M3 = 0, 1  # second-level codes (R5, R21)
 ZERO_CODE = 7
 
 # R1: outer probability of the asymmetric quantile grid.
@@ -221,8 +232,41 @@ def exact_sum_f64(values_f32):
         math.fsum(nz.tolist())), exact
 
 
-def double_quantize(absmax, dq_blocksize=DQ_BLOCKSIZE):
-    """Second-level int8 code of the mean-subtracted block absmax values (R5).
+def e4m3_values():
+    """Values of the 256 E4M3 bytes (R21), fp64: sign * 2^(e-7) * (1 + m/8) for
+    exponent field e > 0, sign * m * 2^-9 for e = 0; NaN for 0x7F and 0xFF."""
+    v = np.empty(256, dtype=np.float64)
+    for b in range(256):
+        s, e, m = b >> 7, (b >> 3) & 15, b & 7
+        mag = math.ldexp(1.0 + m / 8.0, e - 7) if e else math.ldexp(float(m), -9)
+        v[b] = math.nan if (e == 15 and m == 7) else (-mag if s else mag)
+    return v
+
+
+def e4m3_codes(x):
+    """E4M3 byte of each fp32 x (R21): nearest value, ties to the even code,
+    saturating at 448, sign of x kept."""
+    x = np.asarray(x, dtype=np.float32).reshape(-1)
+    pos = e4m3_values()[:0x7F]  # 0x00 .. 0x7E: 0 .. 448, strictly increasing
+    a = np.abs(x.astype(np.float64))
+    hi = np.clip(np.searchsorted(pos, a, side="left"), 0, 0x7E)  # first value >= a (or the top)
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = a - pos[lo], pos[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(a >= pos[0x7E], 0x7E, np.where(pick_hi, hi, lo)).astype(np.uint8)
+    return np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)
+
+
+def dq_code_values(code, dq_type=DQ_INT8):
+    """Values of second-level code bytes (int8 storage): the int8 itself, or the E4M3 value."""
+    code = np.asarray(code, dtype=np.int8).reshape(-1)
+    if dq_type == DQ_E4M3:
+        return e4m3_values()[code.view(np.uint8)].astype(np.float32)
+    return code.astype(np.float32)
+
+
+def double_quantize(absmax, dq_blocksize=DQ_BLOCKSIZE, dq_type=DQ_INT8):
+    """Second-level code of the mean-subtracted block absmax values (R5, or R21 for E4M3).
 
     absmax: float32 vector of n_b block absmax values in block order
     (row-major over (row, block-in-row)).
@@ -232,7 +276,7 @@ def double_quantize(absmax, dq_blocksize=DQ_BLOCKSIZE):
     n_b = a.size
     S, exact = exact_sum_f64(a)
     mean = dq_mean_from_sum(S, n_b)
-    code, step = double_quantize_codes(a, mean, dq_blocksize)
+    code, step = double_quantize_codes(a, mean, dq_blocksize, dq_type)
     return code, step, mean, exact
 
 
@@ -241,10 +285,11 @@ def dq_mean_from_sum(S, n_b):
     return np.float32(float(S) / float(n_b))
 
 
-def double_quantize_codes(absmax, mean, dq_blocksize=DQ_BLOCKSIZE):
+def double_quantize_codes(absmax, mean, dq_blocksize=DQ_BLOCKSIZE, dq_type=DQ_INT8):
     """The second-level codes and steps of consecutive block absmax values,
-    given the mean mu (R5): groups of dq_blocksize start at the first value.
-    Returns (code int8[n], step float32[ceil(n / dq_blocksize)])."""
+    given the mean mu (R5; R21 for E4M3): groups of dq_blocksize start at the
+    first value.  Returns (code int8[n] -- E4M3 bytes viewed as int8 --,
+    step float32[ceil(n / dq_blocksize)])."""
     a = np.asarray(absmax, dtype=np.float32).reshape(-1)
     n_b = a.size
     mean = np.float32(mean)
@@ -255,20 +300,23 @@ def double_quantize_codes(absmax, mean, dq_blocksize=DQ_BLOCKSIZE):
     for g in range(n_2):
         cg = c[g * dq_blocksize:(g + 1) * dq_blocksize]
         a2 = np.float32(np.abs(cg).max())
-        st = np.float32(a2 / np.float32(127.0))
+        st = np.float32(a2 / np.float32(448.0 if dq_type == DQ_E4M3 else 127.0))
         step[g] = st
         if st == 0:
             continue
-        r = np.rint((cg / st).astype(np.float32))
-        code[g * dq_blocksize:(g + 1) * dq_blocksize] = np.clip(r, -127, 127).astype(np.int8)
+        x = (cg / st).astype(np.float32)
+        if dq_type == DQ_E4M3:
+            code[g * dq_blocksize:(g + 1) * dq_blocksize] = e4m3_codes(x).view(np.int8)
+        else:
+            code[g * dq_blocksize:(g + 1) * dq_blocksize] = np.clip(np.rint(x), -127, 127).astype(np.int8)
     return code, step
 
 
-def double_dequantize(code, step, mean, dq_blocksize=DQ_BLOCKSIZE):
-    """absmax_hat = fl32(fl32(code * step) + mean), no FMA (R5)."""
+def double_dequantize(code, step, mean, dq_blocksize=DQ_BLOCKSIZE, dq_type=DQ_INT8):
+    """absmax_hat = fl32(fl32(value(code) * step) + mean), no FMA (R5, R21)."""
     code = np.asarray(code, dtype=np.int8).reshape(-1)
     st = np.repeat(np.asarray(step, dtype=np.float32), dq_blocksize)[:code.size]
-    prod = (code.astype(np.float32) * st).astype(np.float32)
+    prod = (dq_code_values(code, dq_type) * st).astype(np.float32)
     return (prod + np.float32(mean)).astype(np.float32)
 
 
@@ -281,14 +329,14 @@ def dequantize_codes(codes, absmax_hat, blocksize=BLOCKSIZE, levels=None):
     return f32_to_bf16_bits(prod.reshape(rows, cols))
 
 
-def quantize(w_bits, blocksize=BLOCKSIZE, dq_blocksize=DQ_BLOCKSIZE, quant_type=QT_NF4):
+def quantize(w_bits, blocksize=BLOCKSIZE, dq_blocksize=DQ_BLOCKSIZE, quant_type=QT_NF4, dq_type=DQ_INT8):
     """Quantize a bf16 (rows, cols) weight matrix given as uint16 bit patterns.
 
     Returns a dict with: rows, cols, blocksize, dq_blocksize, quant_type,
     packed (uint8, rows*cols/2), absmax (float32, n_b), and, when
     dq_blocksize > 0, code (int8, n_b), step (float32, n_2), mean (float32),
-    mean_exact (bool).  quant_type selects the code table (NF4, or FP4 for
-    comparison).
+    mean_exact (bool), dq_type.  quant_type selects the code table (NF4, or FP4
+    for comparison); dq_type the second-level code (int8, or E4M3).
     """
     w_bits = np.asarray(w_bits, dtype=np.uint16)
     rows, cols = w_bits.shape
@@ -298,15 +346,16 @@ def quantize(w_bits, blocksize=BLOCKSIZE, dq_blocksize=DQ_BLOCKSIZE, quant_type=
     out = dict(rows=rows, cols=cols, blocksize=blocksize, dq_blocksize=dq_blocksize, quant_type=quant_type,
                packed=pack_nibbles(codes), absmax=absmax.reshape(-1))
     if dq_blocksize:
-        code, step, mean, exact = double_quantize(absmax.reshape(-1), dq_blocksize)
-        out.update(code=code, step=step, mean=mean, mean_exact=exact)
+        code, step, mean, exact = double_quantize(absmax.reshape(-1), dq_blocksize, dq_type)
+        out.update(code=code, step=step, mean=mean, mean_exact=exact, dq_type=dq_type)
     return out
 
 
 def absmax_hat(qt):
     """The block constants the dequantizer uses: decoded DQ values, or the fp32 absmax."""
     if qt["dq_blocksize"]:
-        return double_dequantize(qt["code"], qt["step"], qt["mean"], qt["dq_blocksize"])
+        return double_dequantize(qt["code"], qt["step"], qt["mean"], qt["dq_blocksize"],
+                                 qt.get("dq_type", DQ_INT8))
     return np.asarray(qt["absmax"], dtype=np.float32)
 
 

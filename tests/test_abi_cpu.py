@@ -69,6 +69,11 @@ def test_quantize_rejects_bad_arguments_on_host(ql):
     s = ql.NF4Struct(64, 128, 64, 0, buf, None, None, None, None)  # dq off needs absmax
     assert lib.nf4_quantize(buf, ctypes.byref(s), buf, 1 << 20, None) == ql.QL_ERR_INVALID
     assert lib.nf4_quantize(buf, None, buf, 1 << 20, None) == ql.QL_ERR_INVALID
+    s = ql.NF4Struct(64, 128, 64, 256, buf, None, buf, buf, buf, ql.QL_NF4, 2)  # unknown second-level code
+    assert lib.nf4_quantize(buf, ctypes.byref(s), buf, 1 << 20, None) == ql.QL_ERR_UNSUPPORTED
+    assert "dq_type" in lib.ql_last_error().decode()
+    s = ql.NF4Struct(64, 128, 64, 0, buf, buf, None, None, None, ql.QL_NF4, 7)  # ignored without double quant
+    assert lib.nf4_dequantize(ctypes.byref(s), None, None) == ql.QL_ERR_INVALID  # fails on the null output instead
 
 
 def _fake_pointers_only_without_gpu():

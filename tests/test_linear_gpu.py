@@ -285,3 +285,49 @@ def test_fp4_weights_forward_backward(ql, N, K, M, r):
     assert_close(f"dX {tag}", f64(dX), dXr)
     assert_close(f"dA {tag}", f64(dA), dAr)
     assert_close(f"dB {tag}", f64(dB), dBr)
+
+
+@pytest.mark.parametrize("N,K,M,r", [(1032, 576, 1100, 32), (520, 1088, 300, 16), (264, 640, 33, 64),
+                                     (520, 1088, 9, 16)])
+def test_e4m3_second_level_forward_backward(ql, N, K, M, r):
+    """Weights double-quantized with E4M3 second-level codes through every
+    forward path (CTA-pair and single-CTA tensor-core GEMMs, the few-token
+    kernel, the decode path) and the backward, against the oracle on the same
+    dequantized weights."""
+    W, X, A, B, dY, s = make_case(N, K, M, r, seed=N + K + M + r + 5)
+    dev = torch.device("cuda")
+    q = ql.nf4_quantize(W.to(dev), dq_type=ql.QL_DQ_E4M3)
+    Xd, Ad, Bd, dYd = X.to(dev), A.to(dev), B.to(dev), dY.to(dev)
+    Y, XA = ql.qlora_linear_fwd(Xd, q, Ad, Bd, s)
+    dX, dA, dB = ql.qlora_linear_bwd(dYd, Xd, XA, q, Ad, Bd, s)
+    torch.cuda.synchronize()
+    ql.device_status()
+    Wh = nf4.dequantize(nf4.quantize(bits(W), dq_type=nf4.DQ_E4M3))
+    tag = f"e4m3 dq {N}x{K} M={M} r={r}"
+    if M > 16:  # the decode path computes with bf16(q) * m_hat (see test_decode_gpu)
+        Yr, _ = linear.lora_forward(bits(X), Wh, bits(A), bits(B), s)
+        assert_close(f"Y {tag}", f64(Y), Yr)
+    dXr, dAr, dBr, _ = linear.lora_backward(bits(dY), bits(X), Wh, bits(A), bits(B), s)
+    assert_close(f"dX {tag}", f64(dX), dXr)
+    assert_close(f"dA {tag}", f64(dA), dAr)
+    assert_close(f"dB {tag}", f64(dB), dBr)
+
+
+def test_e4m3_second_level_in_gemm_dequant_is_bit_exact(ql):
+    """One-hot tokens through the CTA-pair GEMM and the few-token kernel with
+    E4M3 second-level codes: Y[m, n] = W_hat[n, k_m] bit for bit."""
+    from bit_nf4_quantized_38_b300.workloads import normal_with_outliers_bf16
+    N, K = 296, 320
+    W = normal_with_outliers_bf16((N, K), 0.02, 0.001, 20.0, seed=17)
+    Wh = nf4.dequantize(nf4.quantize(bits(W), dq_type=nf4.DQ_E4M3))
+    dev = torch.device("cuda")
+    q = ql.nf4_quantize(W.to(dev), dq_type=ql.QL_DQ_E4M3)
+    A = torch.randn(K, 8).to(torch.bfloat16).to(dev)
+    Bz = torch.zeros(8, N, dtype=torch.bfloat16, device=dev)
+    for k0, k1 in ((0, K), (0, 100), (100, 217)):  # all tokens at once; few-token batches
+        ks = np.arange(k0, k1)
+        X = torch.zeros(len(ks), K, dtype=torch.bfloat16)
+        X[torch.arange(len(ks)), torch.from_numpy(ks)] = 1.0
+        Y, _ = ql.qlora_linear_fwd(X.to(dev), q, A, Bz, 2.0)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(Y), Wh.T[ks])

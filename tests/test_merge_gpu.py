@@ -89,3 +89,12 @@ def test_merge_fp4_weight(ql):
     torch.cuda.synchronize()
     Wh = nf4.dequantize(nf4.quantize(bits(W), quant_type=nf4.QT_FP4))
     assert_close("merge fp4", linear.as_f64(bits(Wm)), linear.merged_weight(Wh, bits(A), bits(B), 0.25))
+
+
+def test_merge_e4m3_second_level_weight(ql):
+    W, A, B = _case(520, 1088, 64, 78)
+    q = ql.nf4_quantize(W.cuda(), dq_type=ql.QL_DQ_E4M3)
+    Wm = ql.qlora_merge(q, A.cuda(), B.cuda(), 0.25)
+    torch.cuda.synchronize()
+    Wh = nf4.dequantize(nf4.quantize(bits(W), dq_type=nf4.DQ_E4M3))
+    assert_close("merge e4m3 dq", linear.as_f64(bits(Wm)), linear.merged_weight(Wh, bits(A), bits(B), 0.25))

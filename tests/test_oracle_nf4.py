@@ -341,3 +341,86 @@ def test_fp4_round_trip_error_bound():
     g = np.max(np.diff(q[:15]))
     assert abs(g - 1 / 3) < 1e-7
     assert np.all(np.abs(w - wh) <= m * g / 2 * (1 + 1e-6) + 2.0 ** -8 * np.abs(wh))
+
+
+# --------------------------------------------------------------------------- E4M3 second level (R21)
+
+def test_e4m3_table_is_the_format_definition():
+    """Closed-form facts of E4M3 (sign, 4-bit exponent with bias 7, 3-bit
+    mantissa, subnormals at exponent 0, no infinities, one NaN per sign)."""
+    v = nf4.e4m3_values()
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF]) and np.isfinite(v).sum() == 254
+    pos = v[:0x7F]
+    assert np.all(np.diff(pos) > 0)                          # 0x00 .. 0x7E strictly increasing
+    assert pos[0] == 0.0 and pos[0x7E] == 448.0 and pos[0x08] == 2.0 ** -6
+    assert np.array_equal(pos[:8], np.arange(8) * 2.0 ** -9)  # subnormals
+    assert pos[0x38] == 1.0 and pos[0x30] == 0.5 and pos[0x7D] == 416.0
+    assert np.array_equal(-v[0x80:0xFF], pos)                 # sign bit
+    # 3 mantissa bits: within every binade the 8 values are evenly spaced
+    for e in range(1, 16):
+        seg = pos[8 * e:8 * e + 8] if e < 15 else pos[0x78:0x7F]
+        assert np.allclose(np.diff(seg), 2.0 ** (e - 7) / 8)
+
+
+def test_e4m3_coding_is_brute_force_nearest_with_even_ties():
+    """Every code is the nearest E4M3 value (argmin over all finite values),
+    an exact tie going to the even byte; checked on random values, all the
+    exact midpoints between neighbours and their fp32 neighbours, and the
+    saturating range."""
+    pos = nf4.e4m3_values()[:0x7F]
+    mids = (pos[1:] + pos[:-1]) / 2
+    rng = np.random.default_rng(21)
+    x = np.concatenate([
+        rng.uniform(-460, 460, 4000), rng.uniform(-1, 1, 4000) * 2.0 ** rng.integers(-12, 9, 4000),
+        mids, -mids, np.nextafter(mids.astype(np.float32), 0), np.nextafter(mids.astype(np.float32), 1000),
+        [0.0, 448.0, 449.0, 463.9, 464.0, 1e30, -1e30]]).astype(np.float32)
+    got = nf4.e4m3_codes(x)
+    a = np.abs(x.astype(np.float64))
+    d = np.abs(a[:, None] - pos[None, :])
+    best = d.min(axis=1, keepdims=True)
+    cand = d == best
+    # tie rule: the even byte among the nearest ones
+    expect = np.array([np.flatnonzero(c)[np.argmin(np.flatnonzero(c) % 2)] if c.sum() > 1 else np.flatnonzero(c)[0]
+                       for c in cand])
+    expect = np.where(a >= 448.0, 0x7E, expect)  # saturation (fp64 distances to 1e30 all round alike)
+    expect = np.where(np.signbit(x), expect | 0x80, expect)
+    assert np.array_equal(got, expect.astype(np.uint8))
+    # hand cases from the definition
+    assert list(nf4.e4m3_codes(np.array([1.0625, 1.1875, 432.0, 7.5 * 2 ** -9, 1.5 * 2 ** -9, -0.0], np.float32))) == \
+        [0x38, 0x3A, 0x7E, 0x08, 0x02, 0x80]
+
+
+def test_e4m3_double_quant_round_trip_bound():
+    """|m - m_hat| <= half an E4M3 spacing of the quotient times the step, plus
+    the fp32 roundings; the group maximum codes to 448 exactly."""
+    rng = np.random.default_rng(22)
+    a = (rng.random(1000) * 0.05 + 0.02).astype(np.float32)
+    code, step, mean, _ = nf4.double_quantize(a, 256, nf4.DQ_E4M3)
+    assert not np.any(code.view(np.uint8) & 0x7F == 0x7F)
+    vals = nf4.dq_code_values(code, nf4.DQ_E4M3)
+    assert np.abs(vals).max() <= 448.0
+    c = (a - mean).astype(np.float32).astype(np.float64)
+    st = np.repeat(step, 256)[:a.size].astype(np.float64)
+    for g in range(4):
+        i = g * 256 + int(np.argmax(np.abs(c[g * 256:(g + 1) * 256])))
+        assert abs(vals[i]) == 448.0
+    q = c / st
+    spacing = np.where(np.abs(q) < 2.0 ** -6, 2.0 ** -9, 2.0 ** (np.floor(np.log2(np.maximum(np.abs(q), 2.0 ** -6))) - 3))
+    mh = nf4.double_dequantize(code, step, mean, 256, nf4.DQ_E4M3).astype(np.float64)
+    ulp = np.spacing(np.abs(mh).astype(np.float32) + np.float32(step.max())).astype(np.float64)
+    assert np.all(np.abs(a - mh) <= st * (spacing / 2 + 2.0 ** -20) + 2 * ulp)
+
+
+def test_e4m3_double_quant_exact_on_grid_and_zero_step():
+    mean = np.float32(0.25)
+    stv = np.float32(2.0 ** -12)
+    pos = nf4.e4m3_values()[:0x7F]
+    ks = np.concatenate([-pos[::-1], pos])[::2]  # E4M3 values, -448 .. 448
+    a = (mean + (ks * stv).astype(np.float32)).astype(np.float32)
+    a = np.concatenate([a, np.full(256 - a.size, mean)]).astype(np.float32)
+    code, step, m, _ = nf4.double_quantize_codes(a, mean, 256, nf4.DQ_E4M3) + (mean, None)
+    assert step[0] == np.float32(np.float32(448 * stv) / np.float32(448))
+    assert np.array_equal(nf4.double_dequantize(code, step, mean, 256, nf4.DQ_E4M3), a)
+    z = np.full(300, 0.5, dtype=np.float32)
+    code, step, mean, _ = nf4.double_quantize(z, 256, nf4.DQ_E4M3)
+    assert np.all(step == 0) and np.all(code == 0)

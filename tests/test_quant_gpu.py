@@ -207,3 +207,21 @@ def test_quantize_on_load_equals_device_quantize(ql, rows, cols, pinned, dq):
             assert torch.equal(a, b), f
     if rows * cols <= 4096 * 4096:
         _compare_quant(got, nf4.quantize(_bits(W), dq_blocksize=dq))
+
+
+@pytest.mark.parametrize("rows,cols", [(1024, 1024), (37, 4160), (3, 64), (8192, 2752)])
+def test_e4m3_second_level_bit_exact(ql, rows, cols):
+    """Double quantization with E4M3 second-level codes: packed codes, the
+    E4M3 bytes, steps and mean bit-exact against the oracle, and the
+    dequantized weight too (ragged groups, and a LLaMA-65B-sized slab)."""
+    from bit_nf4_quantized_38_b300.workloads import normal_with_outliers_bf16
+    W = normal_with_outliers_bf16((rows, cols), 0.015, 0.001, 20.0, seed=rows + 3 * cols)
+    ref = nf4.quantize(_bits(W), dq_blocksize=256, dq_type=nf4.DQ_E4M3)
+    q = ql.nf4_quantize(W.cuda(), dq_type=ql.QL_DQ_E4M3)
+    torch.cuda.synchronize()
+    ql.device_status()
+    _compare_quant(q, ref)
+    assert not np.any((q.absmax_code.cpu().numpy().view(np.uint8) & 0x7F) == 0x7F)  # no NaN bytes
+    Wd = ql.nf4_dequantize(q)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(Wd), nf4.dequantize(ref))
