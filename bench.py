@@ -64,7 +64,7 @@ def parse_args():
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-extras", action="store_true", help="skip the decode and quantizer sub-results")
     p.add_argument("--linears", default="", help="comma-separated subset of the 7 linears (profiling runs)")
-    p.add_argument("--only", choices=["all", "decode", "quantize", "single"], default="all",
+    p.add_argument("--only", choices=["all", "decode", "quantize", "single", "fp8"], default="all",
                    help="run only one sub-benchmark (profiling runs)")
     p.add_argument("--decode-m", default="1,4,16", help="decode token counts")
     p.add_argument("--decode-shapes", default="0,1,2", help="indices of the LLaMA-13B decode shapes")
@@ -523,9 +523,48 @@ def run_only(args):
                            tuple(int(i) for i in args.decode_shapes.split(",")))
     elif args.only == "single":
         res = bench_single_linear(ql, dev)
+    elif args.only == "fp8":
+        res = bench_forward_fp8(ql, dev, peaks)
     else:
         res = bench_quantize(ql, dev, peaks["hbm_gbs"])
     print(json.dumps({"only": args.only, "results": res}), flush=True)
+
+
+def bench_forward_fp8(ql, dev, peaks, steps=20, warmup=5):
+    """The LLaMA-7B linears (M = 4096 tokens, r = 64), forward only: the bf16
+    forward and the E4M3 forward (main product on E4M3 operands), each timed
+    over `steps` passes of the 7 calls with CUDA events; flops counted as
+    2 M N K + 2 M r (N + K) per linear for both."""
+    import torch
+    wl = workload_of("llama7b")
+    layers = build_layers(ql, dev, wl)
+    ws_bytes = max(max(ql.workspace_size(ql.OP_LINEAR_FWD, c.M, c.N, c.K, c.r),
+                       ql.workspace_size(ql.OP_LINEAR_FWD_FP8, c.M, c.N, c.K, c.r)) for c in wl.cases)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flops = sum(2.0 * c.M * c.N * c.K + 2.0 * c.M * c.r * (c.N + c.K) for c in wl.cases)
+    out = {"workload": wl.name + " forward", "flops_per_pass": flops}
+    for name, fn in (("bf16", ql.qlora_linear_fwd), ("e4m3", ql.qlora_linear_fwd_fp8)):
+        def one_pass():
+            for L in layers:
+                c = L["case"]
+                fn(L["X"], L["q"], L["A"], L["B"], c.scale, Y=L["Y"], XA=L["XA"], ws=ws)
+        for _ in range(warmup):
+            one_pass()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            one_pass()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        out[name] = {"ms_per_pass": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12}
+    out["speedup_e4m3_over_bf16"] = out["bf16"]["ms_per_pass"] / out["e4m3"]["ms_per_pass"]
+    out["peak_e4m3_tflops"] = 2.0 * peaks["bf16_tflops"]
+    out["peak_note"] = "E4M3 dense peak taken as 2x the measured bf16 burst peak (nominal ratio)"
+    del layers
+    torch.cuda.empty_cache()
+    return out
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -803,12 +842,13 @@ def main():
                          "results": bench_decode(ql, dev, peaks["hbm_gbs"], args.decode_calls,
                                                  tuple(int(m) for m in args.decode_m.split(",")),
                                                  tuple(int(i) for i in args.decode_shapes.split(",")))}
-        out["prefill"] = {"workload": "llama13b shapes, M in {32,64,128} tokens (the tensor-core path split over "
-                                      "the reduction), r=64, fwd, CUDA graph over weight copies > 3x L2",
+        out["prefill"] = {"workload": "llama13b shapes, M in {32,64,128} tokens (the few-token tensor-core "
+                                      "kernel), r=64, fwd, CUDA graph over weight copies > 3x L2",
                           "peak_hbm_gbs": peaks["hbm_gbs"],
                           "results": bench_decode(ql, dev, peaks["hbm_gbs"], 120, (32, 64, 128), (0, 1, 2))}
         out["quantize"] = bench_quantize(ql, dev, peaks["hbm_gbs"])
         out["single_linear"] = bench_single_linear(ql, dev)
+        out["forward_e4m3"] = bench_forward_fp8(ql, dev, peaks)
     sampler.stop()
     if rank == 0 and world == 1 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline(args.workload, step_flops(wl))

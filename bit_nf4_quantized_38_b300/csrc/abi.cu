@@ -95,6 +95,7 @@ extern "C" size_t ql_workspace_size(int op, int64_t M, int64_t N, int64_t K, int
     case QL_OP_LINEAR_FWD: return linear_fwd_ws(M, N, K, r);
     case QL_OP_LINEAR_BWD: return linear_bwd_ws(M, N, K, r);
     case QL_OP_QUANTIZE_HOST: return quantize_host_ws(N, K);
+    case QL_OP_LINEAR_FWD_FP8: return linear_fwd_fp8_ws(M, N, K, r);
     default: return (size_t)-1;
   }
 }
@@ -214,6 +215,19 @@ extern "C" int qlora_linear_fwd(const uint16_t *X, int64_t M, const ql_nf4_tenso
   a.Y = Y; a.XA = XA_out; a.ws = ws; a.ws_bytes = ws_bytes;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   return linear_fwd(a);
+}
+
+extern "C" int qlora_linear_fwd_fp8(const uint16_t *X, int64_t M, const ql_nf4_tensor *W, const uint16_t *A,
+                                    const uint16_t *B, int32_t r, float scale, uint16_t *Y, uint16_t *XA_out,
+                                    void *ws, size_t ws_bytes, ql_stream_t stream) {
+  g_msg[0] = 0;
+  int rc = check_tensor(W, "qlora_linear_fwd_fp8", true);
+  if (rc) return rc;
+  LinearArgs a{};
+  a.X = X; a.M = M; a.W = *W; a.A = A; a.B = B; a.r = r; a.scale = scale;
+  a.Y = Y; a.XA = XA_out; a.ws = ws; a.ws_bytes = ws_bytes;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  return linear_fwd_fp8(a);
 }
 
 extern "C" int qlora_linear_bwd(const uint16_t *dY, const uint16_t *X, const uint16_t *XA, int64_t M,

@@ -1,6 +1,7 @@
 // Shared declarations of libqlora's CUDA sources (internal; the public ABI is
 // include/qlora.h).
 #pragma once
+#include <cstring>
 
 #include <cstdint>
 #include <cstddef>
@@ -88,6 +89,24 @@ __device__ __forceinline__ uint32_t e4m3_code(float x) {
   if (rem > 0x80000u || (rem == 0x80000u && (q & 1u))) ++q;  // a carry into the exponent is right
   return s | (((e - 120u) << 3) + q);
 }
+// The weight's power-of-two scale for E4M3 main steps: the largest 2^E with
+// maxm * 2^E <= 448 (maxm = f 2^e, f in [1, 2): E = 8 - e if f <= 1.75, else
+// 7 - e), E clamped to [-60, 60]; 1 when maxm is 0.
+__host__ __device__ __forceinline__ int e4m3_weight_exponent(float maxm) {
+  if (!(maxm > 0.0f)) return 0;
+  uint32_t b;
+  memcpy(&b, &maxm, 4);
+  const int e = (int)((b >> 23) & 0xFFu) - 127;
+  uint32_t fb = (b & 0x7FFFFFu) | 0x3F800000u;
+  float f;
+  memcpy(&f, &fb, 4);
+  int E = (f <= 1.75f ? 8 : 7) - e;
+  return E < -60 ? -60 : (E > 60 ? 60 : E);
+}
+__device__ __forceinline__ float e4m3_weight_scale(float maxm) {
+  return __uint_as_float((uint32_t)(e4m3_weight_exponent(maxm) + 127) << 23);
+}
+
 // Value of a second-level code byte (ql_nf4_tensor.dq_type).
 __device__ __forceinline__ float dq_code_value(int8_t raw, int dq_type) {
   return dq_type == QL_DQ_E4M3 ? e4m3_value((uint8_t)raw) : (float)raw;

@@ -88,6 +88,45 @@ __device__ __forceinline__ void convert_rowblock2(const uint4 &a0, const uint4 &
   }
 }
 
+// 4 E4M3 bytes (elements i = 0..3 in bytes 0..3) from the 4 codes in
+// nibbles 0..3 of `s`, through the 16-byte table T (entry c in byte c % 4 of
+// T[c / 4]): bits 0-2 of a code pick a byte among 8, bit 3 the table half.
+__device__ __forceinline__ uint32_t lut4_e4m3(uint32_t s, const uint32_t (&T)[4]) {
+  using ptx::prmt;
+  const uint32_t sel = s & 0x7777u;
+  return prmt(prmt(T[0], T[1], sel), prmt(T[2], T[3], sel), ((s >> 1) & 0x4444u) | 0x3210u);
+}
+
+// One 64-element row-block to E4M3: the block's table holds
+// e4m3(fl32(q[c] * mE)) with mE = m_hat * 2^E (exact scaling), so an element
+// becomes e4m3(fl32(q[c] * m_hat) * 2^E); its 64 bytes are 16-byte pieces
+// 4h .. 4h + 3 of the 128-byte swizzled row at `row_addr` (piece j stored at
+// j ^ swz): h = 0 for the first 64 K-elements of a 128-wide step, 1 for the
+// second.
+__device__ __forceinline__ void convert_rowblock_e4m3(const uint4 &p0, const uint4 &p1, float mE,
+                                                      const float (&q)[16], uint32_t row_addr, int h, uint32_t swz) {
+  uint32_t T[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    T[i] = ptx::cvt_e4m3x2(__fmul_rn(q[4 * i], mE), __fmul_rn(q[4 * i + 1], mE)) |
+           (ptx::cvt_e4m3x2(__fmul_rn(q[4 * i + 2], mE), __fmul_rn(q[4 * i + 3], mE)) << 16);
+  const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    uint32_t o[4];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const uint32_t w = words[2 * jj + t];
+      // byte j of w holds element 2j (high nibble) and 2j + 1 (low): swap so
+      // that nibble i holds element i
+      const uint32_t sw = ((w >> 4) & 0x0F0F0F0Fu) | ((w << 4) & 0xF0F0F0F0u);
+      o[2 * t] = lut4_e4m3(sw, T);
+      o[2 * t + 1] = lut4_e4m3(sw >> 16, T);
+    }
+    ptx::sts128(row_addr + ((((uint32_t)(4 * h + jj)) ^ swz) << 4), o[0], o[1], o[2], o[3]);
+  }
+}
+
 // Wait for phase `parity` of a barrier for at most `limit_ns`, ignoring the
 // abort flag (used only after an abort, for work already in flight).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 100000000ull) {

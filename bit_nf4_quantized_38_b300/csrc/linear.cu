@@ -20,6 +20,7 @@
 #include <vector>
 
 #include "decode.cuh"
+#include "fp8.cuh"
 #include "linear.cuh"
 #include "tc_gemm.cuh"
 
@@ -270,6 +271,54 @@ int linear_fwd(const LinearArgs &a) {
   g.out = a.Y; g.Nout = N;
   g.early_main = gemm_early;
   g.part = part;
+  return launch_nf4_gemm(g, st);
+}
+
+// E4M3 forward workspace: [max |m_hat| | pad][row exponents M int32][X codes
+// M x K bytes][XAs M x r bf16]
+size_t linear_fwd_fp8_ws(int64_t M, int64_t N, int64_t K, int32_t r) {
+  if (M <= 0 || N <= 0 || K <= 0 || !rank_ok(r)) return 0;
+  return 256 + up256((size_t)M * 4) + up256((size_t)M * K) + up256((size_t)M * r * 2);
+}
+
+// Forward with E4M3 main steps (3 launches, in stream order):
+//   1. X codes e4m3(x 2^E_m) with the row exponents, and max |m_hat|  (k_prep_e4m3)
+//   2. XA = X A -> XA_out, and XAs = bf16(fl32(s XA) 2^(E_m + E))    LoRA kernel
+//   3. Y = 2^(-E_m - E) (X_e4m3 . W_e4m3^T + XAs B)                  CTA-pair GEMM
+int linear_fwd_fp8(const LinearArgs &a) {
+  const char *fn = "qlora_linear_fwd_fp8";
+  if (!a.X || !a.A || !a.B || !a.Y) return set_error(QL_ERR_INVALID, "%s: null X, A, B or Y", fn);
+  if (!al16(a.X) || !al16(a.A) || !al16(a.B) || !al16(a.Y) || (a.XA && !al16(a.XA)))
+    return set_error(QL_ERR_MISALIGNED, "%s: operand not 16-byte aligned", fn);
+  const int64_t M = a.M, N = a.W.rows, K = a.W.cols;
+  const int r = a.r;
+  QL_TRY(check_common(a, fn, linear_fwd_fp8_ws(M, N, K, r)));
+  cudaStream_t st = a.stream;
+  note_other_call(st);  // the next call waits for this one in full
+  char *ws = static_cast<char *>(a.ws);
+  float *wmax = reinterpret_cast<float *>(ws);
+  int *rows = reinterpret_cast<int *>(ws + 256);
+  uint8_t *xq = reinterpret_cast<uint8_t *>(ws + 256 + up256((size_t)M * 4));
+  uint16_t *xas = reinterpret_cast<uint16_t *>(ws + 256 + up256((size_t)M * 4) + up256((size_t)M * K));
+  const NF4View w = nf4_view(a.W);
+  QL_TRY(check_cuda(launch_prep_e4m3(a.X, M, K, w, xq, rows, wmax, st), "qlora_linear_fwd_fp8: operand codes"));
+  LoraProblem L{};
+  L.A = a.X; L.a_mn = false; L.B = a.A; L.b_mn = true;  // X [M][K], A [K][r]
+  L.P = M; L.Q = r; L.T = K; L.mode = 0; L.scale = a.scale;
+  L.out = xas; L.ldo = r; L.out2 = a.XA; L.ldo2 = r;
+  L.row_exp = rows;
+  L.wmax = wmax;
+  L.dep = kDepStart;
+  QL_TRY(launch_lora(L, st));
+  GemmProblem g{};
+  g.trans = false;
+  g.A = reinterpret_cast<const uint16_t *>(xq); g.M = M; g.Kred = K;
+  g.A2 = xas; g.B2 = a.B; g.r = r;
+  g.w = w;
+  g.out = a.Y; g.Nout = N;
+  g.fp8 = true;
+  g.row_exp = rows;
+  g.wmax = wmax;
   return launch_nf4_gemm(g, st);
 }
 

@@ -34,6 +34,8 @@ struct LoraTcArgs {
   int64_t ldo;
   uint16_t *out2;
   int64_t ldo2;
+  const int *row_exp;  // mode 0: out[p][q] = bf16(fl32(scale v) 2^(row_exp[p] + E)) when set
+  const float *wmax;   // E = e4m3_weight_exponent(*wmax)
   int dep;  // kDepStart, kDepStores or kDepExit (see LoraProblem)
   int *status;
 };
@@ -215,8 +217,10 @@ k_lora_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
     for (int e = 0; e < 4; ++e) {
       const int64_t q = 4 * c4 + e;
       if (q >= a.Q) break;
-      const float sv = __fmul_rn(vals[e], a.scale);
+      float sv = __fmul_rn(vals[e], a.scale);
       if (a.mode == 0) {
+        if (a.row_exp) sv = __fmul_rn(sv, __uint_as_float((uint32_t)(__ldg(a.row_exp + p) +
+                                                             e4m3_weight_exponent(__ldg(a.wmax)) + 127) << 23));
         static_cast<uint16_t *>(a.out)[p * a.ldo + q] = (uint16_t)(pack_bf16x2(sv, 0.f) & 0xFFFFu);
         if (a.out2) a.out2[p * a.ldo2 + q] = (uint16_t)(pack_bf16x2(vals[e], 0.f) & 0xFFFFu);
       } else if (a.mode == 1) {
@@ -248,6 +252,8 @@ int prepare(const LoraProblem &L, CUtensorMap *tA, CUtensorMap *tB, LoraTcArgs *
   *a = LoraTcArgs{};
   a->P = L.P; a->Q = L.Q; a->T = L.T; a->mode = L.mode; a->scale = L.scale;
   a->out = L.out; a->ldo = L.ldo; a->out2 = L.out2; a->ldo2 = L.ldo2;
+  a->row_exp = L.row_exp;
+  a->wmax = L.wmax;
   a->dep = L.dep;
   a->status = device_status_ptr();
   return QL_OK;

@@ -27,6 +27,7 @@
 #include "ptx.cuh"
 #include "tc_gemm.cuh"
 #include "convert.cuh"
+#include "fp8.cuh"
 
 namespace ql {
 namespace {
@@ -57,6 +58,11 @@ struct GemmArgs {
   // previous kernel only before the LoRA steps (pair kernel; see there).
   int early_main;
   float *part;  // single-CTA kernel split over K (gridDim.z > 1): fp32 partials [splits][M][ldo]
+  // E4M3 main steps (CTA-pair kernel, kFp8): per X row its exponent E_m; the
+  // largest |m_hat| of the weight, from which the converters take the
+  // weight's exponent E; the epilogue multiplies row m by 2^(-E_m - E)
+  const int *row_exp;
+  const float *wmax;
   float q[16];
 };
 
@@ -355,10 +361,18 @@ struct Geo {
 };
 }  // namespace pairk
 
-template <bool kTrans, int NACC>
+// With kFp8 (forward form only) the main steps are E4M3 x E4M3 products on
+// kind::f8f6f4: A = X quantized per row to E4M3 (the same 128-byte smem rows
+// now hold 128 reduction elements, so a step covers K = 128 with the same four
+// MMA instructions of K = 32), B = the weight converted to E4M3 with a
+// power-of-two scale 2^E; the LoRA steps stay bf16 into the same accumulator
+// with XAs already multiplied by 2^(E_m + E), and the epilogue multiplies
+// each row by 2^(-E_m - E) (exact).
+template <bool kTrans, int NACC, bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pairk::THREADS, 1)
 k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                 const __grid_constant__ CUtensorMap tmB2, const GemmArgs p) {
+  static_assert(!(kFp8 && kTrans), "E4M3 main steps: forward form only");
   using G = pairk::Geo<NACC>;
   constexpr int PSTAGES = pairk::STAGES, PBK = pairk::BK, BMH = pairk::BMH, BNH = pairk::BNH,
                 GROUP_WARPS = pairk::GROUP_WARPS;
@@ -462,7 +476,8 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
         poll_trigger();
         ptx::mbar_arrive_expect_tx_cluster(lead_full, G::A_BYTES + (lora ? G::B_BYTES : 0));
-        const int x = (lora ? ks - p.ksteps_main : ks) * PBK;
+        // x in elements of the operand: bf16 (64 per step) or E4M3 bytes (128)
+        const int x = lora ? (ks - p.ksteps_main) * PBK : ks * (kFp8 ? 2 * PBK : PBK);
 #pragma unroll
         for (int a = 0; a < NACC; ++a)
           ptx::tma_load_2d_pair(a_dst + a * G::A_ONE, lora ? &tmA2 : &tmA, lead_full, x,
@@ -498,14 +513,20 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         // the LoRA B in the forward): 2 MN-atoms of 64 output columns, 8 KB
         // apart, each 8 K-atoms of 8 reduction rows, 1 KB apart.
         const uint64_t b_desc = bmn ? ptx::desc_sw128(b_addr, 8192, 1024) : ptx::desc_sw128(b_addr, 16, 1024);
+        const bool e4m3 = kFp8 && ks < p.ksteps_main;
 #pragma unroll
         for (int kk = 0; kk < PBK / 16; ++kk) {
+          // 32 bytes per instruction either way: 16 bf16 or 32 E4M3 elements
           const uint64_t bd = b_desc + (uint64_t)(bmn ? kk * 128 : kk * 2);
 #pragma unroll
           for (int a = 0; a < NACC; ++a) {
             const uint64_t ad = ptx::desc_sw128(a_addr + a * G::A_ONE, 16, 1024) + (uint64_t)(kk * 2);
-            ptx::mma_bf16_pair(tmem + a * 256, ad, bd, bmn ? idesc_mn : idesc_kmaj,
-                               (ks > 0 || kk > 0) ? 1u : 0u);
+            if (e4m3)
+              ptx::mma_e4m3_pair(tmem + a * 256, ad, bd, ptx::idesc_e4m3(256, 256, false),
+                                 (ks > 0 || kk > 0) ? 1u : 0u);
+            else
+              ptx::mma_bf16_pair(tmem + a * 256, ad, bd, bmn ? idesc_mn : idesc_kmaj,
+                                 (ks > 0 || kk > 0) ? 1u : 0u);
           }
         }
         ptx::mma_commit_pair(empty(s));
@@ -538,27 +559,43 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       rb_dst = (uint32_t)((kbl * 8 + (nl >> 3)) * 1024 + (nl & 7) * 128);
       rb_swz = (uint32_t)(nl & 7);
     }
-    auto fetch = [&](int ks) {
-      return kTrans ? load_rowblock(p.w, rb_n + (int64_t)ks * 64, rb_kb0) : load_rowblock(p.w, rb_n, rb_kb0 + ks);
+    // E4M3: the weight's power-of-two scale 2^E (the largest with
+    // max |m_hat| 2^E <= 448), applied exactly to every block constant
+    const float s2e = kFp8 ? e4m3_weight_scale(__ldg(p.wmax)) : 1.0f;
+    constexpr int RB = kFp8 ? 2 : 1;  // row-blocks per thread per step (K = 128 per E4M3 step)
+    auto fetch = [&](int ks, RowBlockSrc (&r)[RB]) {
+#pragma unroll
+      for (int h = 0; h < RB; ++h)
+        r[h] = kTrans ? load_rowblock(p.w, rb_n + (int64_t)ks * 64, rb_kb0)
+                      : load_rowblock(p.w, rb_n, rb_kb0 + RB * ks + h);
     };
     // The row-blocks of stage ks + 2 are loaded while stage ks is converted.
-    RowBlockSrc cur, nxt;
-    if (grp < p.ksteps_main) cur = fetch(grp);
+    RowBlockSrc cur[RB], nxt[RB];
+    if (grp < p.ksteps_main) fetch(grp, cur);
     for (int ks = grp; ks < nsteps; ks += 2) {
       const int s = ks % PSTAGES;
       const uint32_t ph = (ks / PSTAGES) & 1;
-      if (ks + 2 < p.ksteps_main) nxt = fetch(ks + 2);
+      if (ks + 2 < p.ksteps_main) fetch(ks + 2, nxt);
       poll_trigger();
       if (!ptx::mbar_wait_cluster(empty(s), ph ^ 1, abort, p.status)) break;
       if (ks < p.ksteps_main) {
         const uint32_t b_addr = sbase + s * G::STAGE_BYTES + G::A_BYTES;
-        if (cur.valid) convert_rowblock(cur.p0, cur.p1, cur.mhat, q, b_addr + rb_dst, rb_swz);
-        else zero_row(b_addr + rb_dst);
+        if (kFp8) {
+#pragma unroll
+          for (int h = 0; h < RB; ++h)  // an invalid row-block has zero codes and constant: zero bytes
+            convert_rowblock_e4m3(cur[h].p0, cur[h].p1, __fmul_rn(cur[h].mhat, s2e), q, b_addr + rb_dst, h, rb_swz);
+        } else {
+          if (cur[0].valid) convert_rowblock(cur[0].p0, cur[0].p1, cur[0].mhat, q, b_addr + rb_dst, rb_swz);
+          else zero_row(b_addr + rb_dst);
+        }
         ptx::fence_proxy_async_smem();
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(full(s), 0));
-      if (ks + 2 < p.ksteps_main) cur = nxt;
+      if (ks + 2 < p.ksteps_main) {
+#pragma unroll
+        for (int h = 0; h < RB; ++h) cur[h] = nxt[h];
+      }
     }
     // ---------------------------------------------------------------- epilogue
     if (!*abort && ptx::mbar_wait_cluster(accf, 0, abort, p.status)) {
@@ -568,6 +605,7 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       const int c_begin = NACC == 2 ? 0 : grp * 4, c_end = NACC == 2 ? 8 : grp * 4 + 4;
       const int row = mrow0 + acc * 256 + (int)crank * BMH + qd * 32 + lane;
       uint16_t *orow = p.out + (int64_t)row * p.ldo;
+      const float rs = kFp8 && row < p.M ? e4m3_row_factor(__ldg(p.row_exp + row), __ldg(p.wmax)) : 1.0f;
 #pragma unroll 1
       for (int c = c_begin; c < c_end; ++c) {
         uint32_t r[32];
@@ -578,11 +616,15 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           for (int j = 0; j < 4; ++j) {
             const int col = n0 + c * 32 + j * 8;
             if (col + 8 <= p.Nout) {
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] = kFp8 ? __fmul_rn(__uint_as_float(r[8 * j + e]), rs)
+                                                      : __uint_as_float(r[8 * j + e]);
               uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
-              v.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
-              v.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
-              v.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
+              v.x = pack_bf16x2(f[0], f[1]);
+              v.y = pack_bf16x2(f[2], f[3]);
+              v.z = pack_bf16x2(f[4], f[5]);
+              v.w = pack_bf16x2(f[6], f[7]);
               *reinterpret_cast<uint4 *>(orow + col) = v;
             }
           }
@@ -658,21 +700,24 @@ int make_tmap_packed(CUtensorMap *tm, const uint8_t *ptr, uint64_t row_bytes, ui
 
 namespace {
 
-template <bool kTrans, int NACC>
+template <bool kTrans, int NACC, bool kFp8>
 int launch_pair(const GemmProblem &g, unsigned long long *span, cudaStream_t st) {
   using Gm = pairk::Geo<NACC>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
-    int rc = check_cuda(cudaFuncSetAttribute(k_nf4_gemm_pair<kTrans, NACC>,
+    int rc = check_cuda(cudaFuncSetAttribute(k_nf4_gemm_pair<kTrans, NACC, kFp8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Gm::SMEM),
                         "tensor-core pair GEMM: shared-memory attribute");
     if (rc) return rc;
     attr_done[dev] = true;
   }
   CUtensorMap tA, tA2, tB2;
-  int rc = make_tmap(&tA, g.A, (uint64_t)g.Kred, (uint64_t)g.M, pairk::BMH);
+  // E4M3 A: the per-row codes [M][K] bytes, 128-byte rows of the box
+  int rc = kFp8 ? make_tmap_packed(&tA, reinterpret_cast<const uint8_t *>(g.A), (uint64_t)g.Kred, (uint64_t)g.M,
+                                   pairk::BMH)
+                : make_tmap(&tA, g.A, (uint64_t)g.Kred, (uint64_t)g.M, pairk::BMH);
   if (!rc) rc = make_tmap(&tA2, g.A2, (uint64_t)g.r, (uint64_t)g.M, pairk::BMH);
   if (!rc)
     rc = kTrans ? make_tmap(&tB2, g.B2, (uint64_t)g.r, (uint64_t)g.Nout, pairk::BNH)
@@ -681,7 +726,7 @@ int launch_pair(const GemmProblem &g, unsigned long long *span, cudaStream_t st)
   GemmArgs a{};
   a.M = (int)g.M;
   a.Nout = (int)g.Nout;
-  a.ksteps_main = (int)((g.Kred + BK - 1) / BK);
+  a.ksteps_main = (int)((g.Kred + (kFp8 ? 2 * BK : BK) - 1) / (kFp8 ? 2 * BK : BK));
   a.ksteps_lora = (g.r + BK - 1) / BK;
   a.w = g.w;
   a.out = g.out;
@@ -689,6 +734,8 @@ int launch_pair(const GemmProblem &g, unsigned long long *span, cudaStream_t st)
   a.status = device_status_ptr();
   a.span = span;
   a.early_main = g.early_main ? 1 : 0;
+  a.row_exp = g.row_exp;
+  a.wmax = g.wmax;
   const Codebook &cb = codebook(g.w.qt);
   for (int i = 0; i < 16; ++i) a.q[i] = cb.q[i];
   dim3 grid((unsigned)(2 * ((g.Nout + 255) / 256)), (unsigned)((g.M + NACC * 256 - 1) / (NACC * 256)));
@@ -702,7 +749,7 @@ int launch_pair(const GemmProblem &g, unsigned long long *span, cudaStream_t st)
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_nf4_gemm_pair<kTrans, NACC>, tA, tA2, tB2, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_nf4_gemm_pair<kTrans, NACC, kFp8>, tA, tA2, tB2, a);
   count_launch();
   return check_cuda(e, "tensor-core pair GEMM launch");
 }
@@ -793,10 +840,18 @@ int launch_nf4_gemm(const GemmProblem &g, cudaStream_t st) {
   Spans &sp = g_spans;
   unsigned long long *span = (sp.on && sp.used < sp.capacity) ? sp.buf + 2 * sp.used : nullptr;
   int rc;
-  if (!g.trans && g.M <= kSkinnyMaxM && g.part) rc = launch_nf4_skinny(g, span, st);
-  else if (g.M <= 128) rc = g.trans ? launch<true>(g, span, st) : launch<false>(g, span, st);
-  else if (g.M <= 256) rc = g.trans ? launch_pair<true, 1>(g, span, st) : launch_pair<false, 1>(g, span, st);
-  else rc = g.trans ? launch_pair<true, 2>(g, span, st) : launch_pair<false, 2>(g, span, st);
+  if (g.fp8) {
+    if (g.trans || !g.row_exp || !g.wmax) return set_error(QL_ERR_INVALID, "E4M3 GEMM: forward form with scales only");
+    rc = g.M <= 256 ? launch_pair<false, 1, true>(g, span, st) : launch_pair<false, 2, true>(g, span, st);
+  } else if (!g.trans && g.M <= kSkinnyMaxM && g.part) {
+    rc = launch_nf4_skinny(g, span, st);
+  } else if (g.M <= 128) {
+    rc = g.trans ? launch<true>(g, span, st) : launch<false>(g, span, st);
+  } else if (g.M <= 256) {
+    rc = g.trans ? launch_pair<true, 1, false>(g, span, st) : launch_pair<false, 1, false>(g, span, st);
+  } else {
+    rc = g.trans ? launch_pair<true, 2, false>(g, span, st) : launch_pair<false, 2, false>(g, span, st);
+  }
   const double flops = 2.0 * (double)g.M * (double)g.Nout * (double)(g.Kred + g.r);
   if (timed && rc == QL_OK) {
     cudaEventRecord(t.ev[2 * t.used + 1], st);

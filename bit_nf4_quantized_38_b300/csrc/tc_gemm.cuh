@@ -50,6 +50,14 @@ struct GemmProblem {
   // the single-CTA kernel split over the reduction (M <= 128:
   // gemm_splits(M, Nout, Kred) x M x Nout floats)
   float *part = nullptr;
+  // E4M3 main steps (forward form; CTA-pair kernel): A holds the E4M3 codes
+  // of X [M][Kred] bytes (row m scaled by 2^row_exp[m]), A2 the LoRA operand
+  // already multiplied by 2^(row_exp[m] + E), and the output row m is
+  // multiplied by 2^(-row_exp[m] - E); wmax points at the largest |m_hat| of
+  // the weight, E = e4m3_weight_exponent(*wmax).
+  bool fp8 = false;
+  const int *row_exp = nullptr;
+  const float *wmax = nullptr;
 };
 int launch_nf4_gemm(const GemmProblem &g, cudaStream_t st);
 // Splits over the reduction of a GEMM with M <= 128 tokens (1 otherwise): as
@@ -95,6 +103,10 @@ struct LoraProblem {
   int64_t ldo;
   uint16_t *out2;
   int64_t ldo2;
+  // mode 0 only: multiply row p of `out` by 2^(row_exp[p] + E), E =
+  // e4m3_weight_exponent(*wmax) (after the scale; exact)
+  const int *row_exp = nullptr;
+  const float *wmax = nullptr;
   // Ordering against the previous kernel in the stream (programmatic
   // dependent launch):
   //   kDepStart  wait for it before reading anything (the default);

@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libq
 QL_OK, QL_ERR_INVALID, QL_ERR_UNSUPPORTED, QL_ERR_MISALIGNED, QL_ERR_CUDA, QL_ERR_TIMEOUT = range(6)
 QL_NF4, QL_FP4 = 0, 1
 QL_DQ_INT8, QL_DQ_E4M3 = 0, 1  # second-level codes (ql_nf4_tensor.dq_type)
-OP_QUANTIZE, OP_DEQUANTIZE, OP_LINEAR_FWD, OP_LINEAR_BWD, OP_QUANTIZE_HOST = range(5)
+OP_QUANTIZE, OP_DEQUANTIZE, OP_LINEAR_FWD, OP_LINEAR_BWD, OP_QUANTIZE_HOST, OP_LINEAR_FWD_FP8 = range(6)
 
 _c_i64, _c_i32, _c_f32, _c_p, _c_sz = (ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
                                        ctypes.c_void_p, ctypes.c_size_t)
@@ -40,6 +40,8 @@ _SIGNATURES = {
     "nf4_dequantize": (ctypes.c_int, [ctypes.POINTER(NF4Struct), _c_p, _c_p]),
     "qlora_linear_fwd": (ctypes.c_int, [_c_p, _c_i64, ctypes.POINTER(NF4Struct), _c_p, _c_p, _c_i32,
                                         _c_f32, _c_p, _c_p, _c_p, _c_sz, _c_p]),
+    "qlora_linear_fwd_fp8": (ctypes.c_int, [_c_p, _c_i64, ctypes.POINTER(NF4Struct), _c_p, _c_p, _c_i32,
+                                            _c_f32, _c_p, _c_p, _c_p, _c_sz, _c_p]),
     "qlora_linear_bwd": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, ctypes.POINTER(NF4Struct), _c_p,
                                         _c_p, _c_i32, _c_f32, _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p]),
     "qlora_merge": (ctypes.c_int, [ctypes.POINTER(NF4Struct), _c_p, _c_p, _c_i32, _c_f32, _c_p, _c_p]),
@@ -307,6 +309,28 @@ def qlora_linear_fwd(X, q, A, B, scale, Y=None, XA=None, ws=None, stream=None, w
     s = q.struct()
     _check(lib.qlora_linear_fwd(_ptr(X), M, ctypes.byref(s), _ptr(A), _ptr(B), r, float(scale),
                                 _ptr(Y), _ptr(XA), _ptr(ws), nbytes, _stream(stream)))
+    return Y, XA
+
+
+def qlora_linear_fwd_fp8(X, q, A, B, scale, Y=None, XA=None, ws=None, stream=None, want_xa=True):
+    """qlora_linear_fwd with the main product on E4M3 operands (see
+    include/qlora.h); returns (Y, XA or None)."""
+    M, K = X.shape
+    r = A.shape[1]
+    _need(X, torch.bfloat16, "X", (M, q.cols))
+    _need(A, torch.bfloat16, "A", (q.cols, r))
+    _need(B, torch.bfloat16, "B", (r, q.rows))
+    if Y is None:
+        Y = torch.empty(M, q.rows, dtype=torch.bfloat16, device=X.device)
+    _need(Y, torch.bfloat16, "Y", (M, q.rows))
+    if XA is None and want_xa:
+        XA = torch.empty(M, r, dtype=torch.bfloat16, device=X.device)
+    if XA is not None:
+        _need(XA, torch.bfloat16, "XA", (M, r))
+    ws, nbytes = _workspace(workspace_size(OP_LINEAR_FWD_FP8, M, q.rows, q.cols, r), X.device, ws)
+    s = q.struct()
+    _check(lib.qlora_linear_fwd_fp8(_ptr(X), M, ctypes.byref(s), _ptr(A), _ptr(B), r, float(scale),
+                                    _ptr(Y), _ptr(XA), _ptr(ws), nbytes, _stream(stream)))
     return Y, XA
 
 

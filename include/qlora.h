@@ -60,7 +60,8 @@ enum ql_op {
   QL_OP_DEQUANTIZE = 1,
   QL_OP_LINEAR_FWD = 2,
   QL_OP_LINEAR_BWD = 3,
-  QL_OP_QUANTIZE_HOST = 4
+  QL_OP_QUANTIZE_HOST = 4,
+  QL_OP_LINEAR_FWD_FP8 = 5
 };
 
 /*
@@ -269,6 +270,30 @@ QL_API int qlora_linear_fwd(const uint16_t *X, int64_t M, const ql_nf4_tensor *W
                      const uint16_t *A, const uint16_t *B, int32_t r,
                      float scale, uint16_t *Y, uint16_t *XA_out, void *ws,
                      size_t ws_bytes, ql_stream_t stream);
+
+/*
+ * The same forward with the main product on 8-bit floats (E4M3: 1 sign, 4
+ * exponent bits with bias 7, 3 mantissa bits, largest finite 448) -- the FP8
+ * variant of the compute dtype the QLoRA project page's configuration example
+ * sets (bnb_4bit_compute_dtype); the LoRA term stays bf16:
+ *   maxm = max |m_hat| over the weight's blocks; 2^E the largest power of two
+ *          with maxm 2^E <= 448 (1 if maxm = 0)
+ *   Wq   = e4m3(fl32(q[code] * m_hat) * 2^E)      (the weight before its
+ *          bf16 rounding, scaled exactly)
+ *   per row m of X: sx = fl32(amax_m / 448) (1 for an all-zero row),
+ *          Xq = e4m3(fl32(x / sx))
+ *   Y[m] = bf16(fl32(sx 2^-E) * (Xq Wq^T + bf16(fl32(s XA) / fl32(sx 2^-E)) B))
+ * e4m3(x): nearest value, ties to the even code, saturating at +-448; the
+ * products accumulate in fp32.  Arguments, layouts and XA_out as for
+ * qlora_linear_fwd; K % 8 == 0 (always, as K % 64 == 0).
+ *   ws : ql_workspace_size(QL_OP_LINEAR_FWD_FP8, M, N, K, r) bytes.
+ * Every M takes the tensor-core path (tiles of 256 tokens).  The next call on
+ * the stream waits for this one to complete.
+ */
+QL_API int qlora_linear_fwd_fp8(const uint16_t *X, int64_t M, const ql_nf4_tensor *W,
+                         const uint16_t *A, const uint16_t *B, int32_t r,
+                         float scale, uint16_t *Y, uint16_t *XA_out, void *ws,
+                         size_t ws_bytes, ql_stream_t stream);
 
 /*
  * Backward of the same layer (QLoRA abstract: gradients back-propagate through

@@ -23,6 +23,7 @@ Modules:
   nf4     -- codebook, blockwise absmax, NF4 code + nibble pack, double
              quantization of the absmax constants, dequantization.
   linear  -- forward and backward of the frozen-NF4 linear with a LoRA adapter.
+  fp8     -- the same forward with the main product on E4M3 operands.
   bf16    -- IEEE round-to-nearest-even to bfloat16 and back.
 
 Parity status of each function is stated in its docstring; the readings taken

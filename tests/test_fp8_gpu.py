@@ -1,0 +1,108 @@
+"""GPU parity of the E4M3 forward (qlora_linear_fwd_fp8) against the oracle's
+E4M3 forward (oracle/fp8.py): same quantized operands, fp32 accumulation on
+the GPU vs fp64 -- the usual GEMM tolerance (relative Frobenius <= 5e-3,
+|err| <= 1e-2 (|ref| + rms(ref)) per element).  One-hot tokens pin the weight
+conversion, the row codes and the epilogue factor bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import fp8, linear, nf4
+from oracle.bf16 import f32_to_bf16_bits
+from parity import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ql():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_nf4_quantized_38_b300 import qlora
+    return qlora
+
+
+def bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def f64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def make(N, K, M, r, seed):
+    from bit_nf4_quantized_38_b300.workloads import normal_bf16, normal_with_outliers_bf16
+    W = normal_with_outliers_bf16((N, K), 0.02, 0.001, 20.0, seed)
+    X = normal_bf16((M, K), 1.0, seed + 1)
+    A = normal_bf16((K, r), 1.0 / np.sqrt(r), seed + 2)
+    B = normal_bf16((r, N), 0.01, seed + 3)
+    return W, X, A, B, 16.0 / r
+
+
+@pytest.mark.parametrize("N,K,M,r,dq,dqt", [
+    (520, 1088, 200, 16, 256, 0),    # one accumulator per CTA (M <= 256)
+    (1032, 576, 1100, 32, 256, 0),   # two accumulators, ragged in N and M
+    (264, 640, 17, 64, 256, 0),      # few tokens, mostly padding
+    (1024, 1024, 300, 128, 256, 1),  # rank 128; E4M3 second-level codes
+    (776, 1088, 513, 8, 0, 0),       # double quantization off
+])
+def test_forward_matches_the_e4m3_oracle(ql, N, K, M, r, dq, dqt):
+    W, X, A, B, s = make(N, K, M, r, seed=N + K + M + r)
+    dev = torch.device("cuda")
+    q = ql.nf4_quantize(W.to(dev), dq_blocksize=dq, dq_type=dqt)
+    Y, XA = ql.qlora_linear_fwd_fp8(X.to(dev), q, A.to(dev), B.to(dev), s)
+    torch.cuda.synchronize()
+    ql.device_status()
+    qt = nf4.quantize(bits(W), dq_blocksize=dq, dq_type=dqt)
+    Yr, _ = fp8.lora_forward_e4m3(bits(X), qt, bits(A), bits(B), s)
+    tag = f"{N}x{K} M={M} r={r} dq={dq} dqt={dqt}"
+    assert_close(f"Y e4m3 {tag}", f64(Y), Yr)
+    # XA_out is the same bf16 XA the bf16 forward hands to the backward
+    _, XA16 = ql.qlora_linear_fwd(X.to(dev), q, A.to(dev), B.to(dev), s)
+    torch.cuda.synchronize()
+    assert torch.equal(XA, XA16)
+    # and the E4M3 forward stays near the bf16 one (3 mantissa bits per operand)
+    Y16, _ = linear.lora_forward(bits(X), nf4.dequantize(qt), bits(A), bits(B), s)
+    assert np.linalg.norm(f64(Y) - Y16) / np.linalg.norm(Y16) < 0.06
+
+
+def test_one_hot_tokens_are_bit_exact(ql):
+    """X row m one-hot (1.0) at k_m, B = 0: the row exponent is 8, the row
+    code 256, so Y[m, n] = bf16(Wq[n, k_m] 2^-E) exactly -- the weight's E4M3
+    codes, read back bit for bit."""
+    from bit_nf4_quantized_38_b300.workloads import normal_with_outliers_bf16
+    N, K = 296, 320
+    W = normal_with_outliers_bf16((N, K), 0.02, 0.001, 20.0, seed=23)
+    qt = nf4.quantize(bits(W))
+    E, wq = fp8.weight_e4m3(qt)
+    dev = torch.device("cuda")
+    q = ql.nf4_quantize(W.to(dev))
+    A = torch.randn(K, 8).to(torch.bfloat16).to(dev)
+    Bz = torch.zeros(8, N, dtype=torch.bfloat16, device=dev)
+    ks = np.arange(K)
+    X = torch.zeros(K, K, dtype=torch.bfloat16)
+    X[torch.arange(K), torch.from_numpy(ks)] = 1.0
+    Y, _ = ql.qlora_linear_fwd_fp8(X.to(dev), q, A, Bz, 2.0)
+    torch.cuda.synchronize()
+    Em, xq = fp8.rows_e4m3(bits(X))
+    assert np.all(Em == 8) and np.all(xq[np.arange(K), ks] == 256.0)
+    expect = f32_to_bf16_bits(np.ldexp(wq.T[ks], -E).astype(np.float32))
+    assert np.array_equal(bits(Y), expect)
+
+
+def test_llama7b_q_proj_full_size_sampled(ql):
+    """LLaMA-7B q_proj (4096 x 4096) at 4096 tokens, r = 64: 64 sampled rows
+    against the oracle (the weight's E4M3 codes in full)."""
+    from bit_nf4_quantized_38_b300.workloads import case_inputs, case_weight, llama7b_linears
+    case = llama7b_linears().cases[0]
+    W = case_weight(case)
+    X, A, B, _ = case_inputs(case)
+    dev = torch.device("cuda")
+    q = ql.nf4_quantize(W.to(dev))
+    Y, _ = ql.qlora_linear_fwd_fp8(X.to(dev), q, A.to(dev), B.to(dev), case.scale)
+    torch.cuda.synchronize()
+    ql.device_status()
+    rows = np.sort(np.random.default_rng(7).choice(case.M, 64, replace=False))
+    qt = nf4.quantize(bits(W))
+    Yr, _ = fp8.lora_forward_e4m3(bits(X)[rows], qt, bits(A), bits(B), case.scale)
+    assert_close("Y e4m3 llama7b q_proj rows", f64(Y)[rows], Yr)
