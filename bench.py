@@ -769,7 +769,8 @@ def roofline_of(res, peaks, peak_src, wl):
     achieved = g["flops"] / (g["busy_ms"] / 1e3) / 1e12 if g["busy_ms"] > 0 else 0.0
     long_region = res["ms_total"] >= 1000.0
     peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
-    traffic = ncu_traffic("k_nf4_gemm_pair " + wl.name, ["bit_nf4_quantized_38_b300/csrc/tc_gemm.cu"])
+    traffic = ncu_traffic("k_nf4_gemm_pair " + wl.name, ["bit_nf4_quantized_38_b300/csrc/tc_gemm.cu",
+                                                         "bit_nf4_quantized_38_b300/csrc/convert.cuh"])
     return {"kernel": "k_nf4_gemm_pair (tcgen05 fused NF4-dequant GEMM, fwd Y and bwd dX)",
             "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "traffic": traffic,

@@ -66,29 +66,38 @@ struct GemmArgs {
   float q[16];
 };
 
+// The raw inputs of one 64-element row-block, loaded ahead of their use: no
+// value is computed from them at load time, so the loads stay in flight
+// until the conversion (a computation -- or a register copy -- would wait for
+// them there).
 struct RowBlockSrc {
   uint4 p0, p1;
-  float mhat;
+  float s;   // absmax (no double quantization) or the step of the block's group
+  int code;  // second-level code byte (double quantization)
   bool valid;
 };
 
-__device__ __forceinline__ RowBlockSrc load_rowblock(const NF4View &w, int64_t n, int64_t kb) {
-  RowBlockSrc r;
+__device__ __forceinline__ void load_rowblock(const NF4View &w, int64_t n, int64_t kb, RowBlockSrc &r) {
   r.valid = n < w.rows && kb < w.cols / 64;
   if (r.valid) {
     const uint8_t *src = w.packed + n * (w.cols >> 1) + kb * 32;
     r.p0 = ptx::ldg_nc_v4(src);
     r.p1 = ptx::ldg_nc_v4(src + 16);
     const int64_t b = n * (w.cols >> 6) + kb;
-    if (w.dq)
-      r.mhat = __fadd_rn(__fmul_rn(dq_code_value(__ldg(w.code + b), w.dqt), __ldg(w.step + (b >> 8))), __ldg(w.mean));
-    else
-      r.mhat = __ldg(w.absmax + b);
-  } else {
-    r.p0 = r.p1 = make_uint4(0, 0, 0, 0);
-    r.mhat = 0.0f;
+    if (w.dq) {
+      r.code = __ldg(w.code + b);
+      r.s = __ldg(w.step + (b >> 8));
+    } else {
+      r.s = __ldg(w.absmax + b);
+    }
   }
-  return r;
+}
+
+// The block constant m_hat of a loaded row-block (0 outside the weight);
+// `mean` = the tensor's mu (double quantization).
+__device__ __forceinline__ float rowblock_mhat(const RowBlockSrc &r, const NF4View &w, float mean) {
+  if (!r.valid) return 0.0f;
+  return w.dq ? __fadd_rn(__fmul_rn(dq_code_value((int8_t)r.code, w.dqt), r.s), mean) : r.s;
 }
 
 template <bool kTrans>
@@ -233,35 +242,42 @@ k_nf4_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         rb_swz[h] = (uint32_t)(nl & 7);
       }
     }
+    const float mean = p.w.dq ? __ldg(p.w.mean) : 0.0f;
     auto fetch = [&](int ks, RowBlockSrc (&r)[2]) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        if (!kTrans) r[h] = load_rowblock(p.w, rb_n[h], rb_kb0[h] + ks);
-        else r[h] = load_rowblock(p.w, rb_n[h] + (int64_t)ks * 64, rb_kb0[h]);
+        if (!kTrans) load_rowblock(p.w, rb_n[h], rb_kb0[h] + ks, r[h]);
+        else load_rowblock(p.w, rb_n[h] + (int64_t)ks * 64, rb_kb0[h], r[h]);
       }
     };
-    RowBlockSrc cur[2], nxt[2];
-    if (nmain > 0) fetch(kq0, cur);
-    for (int ks = 0; ks < nsteps; ++ks) {
+    auto body = [&](int ks, RowBlockSrc (&cur)[2]) -> bool {
       const int s = ks % STAGES;
       const uint32_t ph = (ks / STAGES) & 1;
-      const bool main_step = ks < nmain;
-      if (ks + 1 < nmain) fetch(kq0 + ks + 1, nxt);
-      if (!ptx::mbar_wait(empty(s), ph ^ 1, abort, p.status)) break;
-      if (main_step) {
+      if (!ptx::mbar_wait(empty(s), ph ^ 1, abort, p.status)) return false;
+      if (ks < nmain) {
         const uint32_t b_addr = sbase + s * STAGE_BYTES + A_BYTES;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          if (cur[h].valid) convert_rowblock(cur[h].p0, cur[h].p1, cur[h].mhat, q, b_addr + rb_dst[h], rb_swz[h]);
-          else zero_row(b_addr + rb_dst[h]);
+          if (cur[h].valid)
+            convert_rowblock(cur[h].p0, cur[h].p1, rowblock_mhat(cur[h], p.w, mean), q, b_addr + rb_dst[h], rb_swz[h]);
+          else
+            zero_row(b_addr + rb_dst[h]);
         }
         ptx::fence_proxy_async_smem();
       }
       ptx::mbar_arrive(full(s));
-      if (ks + 1 < nmain) {
-        cur[0] = nxt[0];
-        cur[1] = nxt[1];
-      }
+      return true;
+    };
+    // Two register sets taking steps in turn, each loaded two steps ahead of
+    // its use (no copies between them).
+    RowBlockSrc sa[2], sb[2];
+    if (nmain > 0) fetch(kq0, sa);
+    if (nmain > 1) fetch(kq0 + 1, sb);
+    for (int ks = 0; ks < nsteps; ks += 2) {
+      if (!body(ks, sa)) break;
+      if (ks + 2 < nmain) fetch(kq0 + ks + 2, sa);
+      if (ks + 1 >= nsteps || !body(ks + 1, sb)) break;
+      if (ks + 3 < nmain) fetch(kq0 + ks + 3, sb);
     }
     // ---------------------------------------------------------------- epilogue
     if (!*abort && ptx::mbar_wait(accf, 0, abort, p.status)) {
@@ -563,39 +579,47 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // max |m_hat| 2^E <= 448), applied exactly to every block constant
     const float s2e = kFp8 ? e4m3_weight_scale(__ldg(p.wmax)) : 1.0f;
     constexpr int RB = kFp8 ? 2 : 1;  // row-blocks per thread per step (K = 128 per E4M3 step)
+    const float mean = p.w.dq ? __ldg(p.w.mean) : 0.0f;
     auto fetch = [&](int ks, RowBlockSrc (&r)[RB]) {
 #pragma unroll
-      for (int h = 0; h < RB; ++h)
-        r[h] = kTrans ? load_rowblock(p.w, rb_n + (int64_t)ks * 64, rb_kb0)
-                      : load_rowblock(p.w, rb_n, rb_kb0 + RB * ks + h);
+      for (int h = 0; h < RB; ++h) {
+        if (kTrans) load_rowblock(p.w, rb_n + (int64_t)ks * 64, rb_kb0, r[h]);
+        else load_rowblock(p.w, rb_n, rb_kb0 + RB * ks + h, r[h]);
+      }
     };
-    // The row-blocks of stage ks + 2 are loaded while stage ks is converted.
-    RowBlockSrc cur[RB], nxt[RB];
-    if (grp < p.ksteps_main) fetch(grp, cur);
-    for (int ks = grp; ks < nsteps; ks += 2) {
+    auto body = [&](int ks, RowBlockSrc (&cur)[RB]) -> bool {
       const int s = ks % PSTAGES;
       const uint32_t ph = (ks / PSTAGES) & 1;
-      if (ks + 2 < p.ksteps_main) fetch(ks + 2, nxt);
       poll_trigger();
-      if (!ptx::mbar_wait_cluster(empty(s), ph ^ 1, abort, p.status)) break;
+      if (!ptx::mbar_wait_cluster(empty(s), ph ^ 1, abort, p.status)) return false;
       if (ks < p.ksteps_main) {
         const uint32_t b_addr = sbase + s * G::STAGE_BYTES + G::A_BYTES;
         if (kFp8) {
 #pragma unroll
           for (int h = 0; h < RB; ++h)  // an invalid row-block has zero codes and constant: zero bytes
-            convert_rowblock_e4m3(cur[h].p0, cur[h].p1, __fmul_rn(cur[h].mhat, s2e), q, b_addr + rb_dst, h, rb_swz);
+            convert_rowblock_e4m3(cur[h].p0, cur[h].p1, __fmul_rn(rowblock_mhat(cur[h], p.w, mean), s2e), q,
+                                  b_addr + rb_dst, h, rb_swz);
         } else {
-          if (cur[0].valid) convert_rowblock(cur[0].p0, cur[0].p1, cur[0].mhat, q, b_addr + rb_dst, rb_swz);
+          if (cur[0].valid) convert_rowblock(cur[0].p0, cur[0].p1, rowblock_mhat(cur[0], p.w, mean), q, b_addr + rb_dst, rb_swz);
           else zero_row(b_addr + rb_dst);
         }
         ptx::fence_proxy_async_smem();
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(full(s), 0));
-      if (ks + 2 < p.ksteps_main) {
-#pragma unroll
-        for (int h = 0; h < RB; ++h) cur[h] = nxt[h];
-      }
+      return true;
+    };
+    // This group takes stages grp, grp + 2, ...: two register sets take them
+    // in turn, each loaded two of the group's stages ahead of its use (no
+    // copies between them, so the loads stay in flight).
+    RowBlockSrc sa[RB], sb[RB];
+    if (grp < p.ksteps_main) fetch(grp, sa);
+    if (grp + 2 < p.ksteps_main) fetch(grp + 2, sb);
+    for (int ks = grp; ks < nsteps; ks += 4) {
+      if (!body(ks, sa)) break;
+      if (ks + 4 < p.ksteps_main) fetch(ks + 4, sa);
+      if (ks + 2 >= nsteps || !body(ks + 2, sb)) break;
+      if (ks + 6 < p.ksteps_main) fetch(ks + 6, sb);
     }
     // ---------------------------------------------------------------- epilogue
     if (!*abort && ptx::mbar_wait_cluster(accf, 0, abort, p.status)) {
