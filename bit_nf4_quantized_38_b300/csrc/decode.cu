@@ -345,15 +345,21 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
   const float mu = a.dq ? __ldg(a.mean) : 0.0f;
 
   // block constants of block t of a unit for the lane's 2 rows (16 w + 8 k + pg),
-  // loaded PD units ahead
+  // loaded PD units ahead as raw values (the code byte and the step, or the
+  // absmax): nothing is computed from them until the unit is reached, so the
+  // loads stay in flight until then
   struct Pre {
     float a[2], b[2];
+    int c[2];
   };
   int prg = rg0, pb = b0;  // unit of the next load_pre call
   auto load_pre = [&](int i) {
     Pre p;
 #pragma unroll
-    for (int k = 0; k < 2; ++k) p.a[k] = p.b[k] = 0.0f;
+    for (int k = 0; k < 2; ++k) {
+      p.a[k] = p.b[k] = 0.0f;
+      p.c[k] = 0;
+    }
     const int rg = prg, kb = pb * 4 + t;
     pb = pb + 1 == a.nbox ? 0 : pb + 1;
     prg += pb == 0;
@@ -364,7 +370,7 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
       if (row < a.N) {
         const int bi = row * nb_row + kb;
         if (a.dq) {
-          p.a[k] = dq_code_value(__ldg(a.code + bi), a.dqt);
+          p.c[k] = __ldg(a.code + bi);
           p.b[k] = __ldg(a.step + (bi >> 8));
         } else {
           p.a[k] = __ldg(a.absmax + bi);
@@ -373,9 +379,11 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     }
     return p;
   };
-  Pre pre[PD];
-#pragma unroll
-  for (int d = 0; d < PD; ++d) pre[d] = load_pre(d);
+  // two register sets taking units in turn (PD = 2), each reloaded for the
+  // unit two ahead as soon as its constants are used (no copies between
+  // them, which would wait for the loads)
+  static_assert(PD == 2, "two alternating sets of block constants");
+  Pre pre_a = load_pre(0), pre_b = load_pre(1);
 
   float acc[MT][4];
 #pragma unroll
@@ -402,8 +410,7 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
   };
 
   int cur_rg = -1, rg = rg0, b = b0;
-#pragma unroll 1
-  for (int i = 0; i < nu; ++i, b = b + 1 == a.nbox ? 0 : b + 1, rg += b == 0) {
+  auto unit = [&](int i, Pre &pre) {
     const int s = i % ST_STAGES;
     if (rg != cur_rg) {
       if (cur_rg >= 0) flush(cur_rg);
@@ -412,10 +419,9 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     // block constants of block t of this unit, rows k = 0, 1
     float mh[2];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) mh[k] = a.dq ? __fadd_rn(__fmul_rn(pre[0].a[k], pre[0].b[k]), mu) : pre[0].a[k];
-#pragma unroll
-    for (int d = 0; d < PD - 1; ++d) pre[d] = pre[d + 1];
-    pre[PD - 1] = load_pre(i + PD);
+    for (int k = 0; k < 2; ++k)
+      mh[k] = a.dq ? __fadd_rn(__fmul_rn(dq_code_value((int8_t)pre.c[k], a.dqt), pre.b[k]), mu) : pre.a[k];
+    pre = load_pre(i + PD);
 
     bool landed = false;
     if (!*abort_v)
@@ -487,6 +493,13 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         }
       }
     }
+    b = b + 1 == a.nbox ? 0 : b + 1;
+    rg += b == 0;
+  };
+#pragma unroll 1
+  for (int i = 0; i < nu; i += 2) {
+    unit(i, pre_a);
+    if (i + 1 < nu) unit(i + 1, pre_b);
   }
   if (cur_rg >= 0) flush(cur_rg);
   // this grid completes only after the grid before it (see the ordering note)

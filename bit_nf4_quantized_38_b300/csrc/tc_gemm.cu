@@ -609,17 +609,35 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(full(s), 0));
       return true;
     };
-    // This group takes stages grp, grp + 2, ...: two register sets take them
-    // in turn, each loaded two of the group's stages ahead of its use (no
-    // copies between them, so the loads stay in flight).
-    RowBlockSrc sa[RB], sb[RB];
-    if (grp < p.ksteps_main) fetch(grp, sa);
-    if (grp + 2 < p.ksteps_main) fetch(grp + 2, sb);
-    for (int ks = grp; ks < nsteps; ks += 4) {
-      if (!body(ks, sa)) break;
-      if (ks + 4 < p.ksteps_main) fetch(ks + 4, sa);
-      if (ks + 2 >= nsteps || !body(ks + 2, sb)) break;
-      if (ks + 6 < p.ksteps_main) fetch(ks + 6, sb);
+    // This group takes stages grp, grp + 2, ...: register sets take them in
+    // turn, each loaded as many of the group's stages ahead of its use as
+    // there are sets (no copies between them, so the loads stay in flight
+    // that long): two for bf16, three for E4M3, whose steps convert twice the
+    // elements (a third bf16 set measured no faster on the power-capped 33B
+    // step).
+    if constexpr (kFp8) {
+      RowBlockSrc sa[RB], sb[RB], sc[RB];
+      if (grp < p.ksteps_main) fetch(grp, sa);
+      if (grp + 2 < p.ksteps_main) fetch(grp + 2, sb);
+      if (grp + 4 < p.ksteps_main) fetch(grp + 4, sc);
+      for (int ks = grp; ks < nsteps; ks += 6) {
+        if (!body(ks, sa)) break;
+        if (ks + 6 < p.ksteps_main) fetch(ks + 6, sa);
+        if (ks + 2 >= nsteps || !body(ks + 2, sb)) break;
+        if (ks + 8 < p.ksteps_main) fetch(ks + 8, sb);
+        if (ks + 4 >= nsteps || !body(ks + 4, sc)) break;
+        if (ks + 10 < p.ksteps_main) fetch(ks + 10, sc);
+      }
+    } else {
+      RowBlockSrc sa[RB], sb[RB];
+      if (grp < p.ksteps_main) fetch(grp, sa);
+      if (grp + 2 < p.ksteps_main) fetch(grp + 2, sb);
+      for (int ks = grp; ks < nsteps; ks += 4) {
+        if (!body(ks, sa)) break;
+        if (ks + 4 < p.ksteps_main) fetch(ks + 4, sa);
+        if (ks + 2 >= nsteps || !body(ks + 2, sb)) break;
+        if (ks + 6 < p.ksteps_main) fetch(ks + 6, sb);
+      }
     }
     // ---------------------------------------------------------------- epilogue
     if (!*abort && ptx::mbar_wait_cluster(accf, 0, abort, p.status)) {
