@@ -319,6 +319,11 @@ int linear_fwd_fp8(const LinearArgs &a) {
   g.fp8 = true;
   g.row_exp = rows;
   g.wmax = wmax;
+  // The main loop reads the X codes, the weight and max |m_hat|: written by
+  // the operand kernel, which completed before the LoRA kernel (a dependent
+  // that waits for it at its start) let this GEMM launch; the LoRA kernel
+  // itself writes only XAs, read after the wait.
+  g.early_main = true;
   return launch_nf4_gemm(g, st);
 }
 

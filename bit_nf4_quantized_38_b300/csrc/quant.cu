@@ -13,6 +13,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace ql {
 namespace {
@@ -114,6 +115,9 @@ k_quantize(const uint4 *__restrict__ W, int64_t n_blocks, Codebook cb, uint4 *__
                           : make_uint2(0x7F800000u, 0x30800000u | 8u);
   }
   __syncthreads();
+  // the second level (a programmatic dependent) waits for this grid's
+  // completion before it reads anything: it may launch now
+  ptx::griddep_launch();
 
   const int lane = threadIdx.x & 31;
   const int sub = lane & (kQLanes - 1);
@@ -202,46 +206,66 @@ k_quantize(const uint4 *__restrict__ W, int64_t n_blocks, Codebook cb, uint4 *__
   }
 }
 
-__global__ void __launch_bounds__(256)
+// One warp per group of 256 block constants, lane l holding constants
+// 8l .. 8l + 7: the group's largest |c - mu| is a shuffle reduction, so a warp
+// takes one memory round trip per group and no block barrier.  Launched as a
+// programmatic dependent of the first level: it waits for it before reading.
+constexpr int kDqWarps = 8;
+__global__ void __launch_bounds__(kDqWarps * 32)
 k_double_quant(const float *__restrict__ absmax, int64_t n_b, int64_t total_blocks, const double *__restrict__ sum,
                int dq_type, int8_t *__restrict__ code, float *__restrict__ step, float *__restrict__ mean) {
-  __shared__ float red[8];
   __shared__ float mu_s;
-  // mu once per CTA (an fp64 division is slow; every thread taking one was
-  // most of this kernel's time)
+  ptx::griddep_wait();  // the sum and the constants are complete
+  // mu once per CTA (an fp64 division is slow on this GPU)
   if (threadIdx.x == 0) mu_s = __double2float_rn(__ddiv_rn(*sum, (double)total_blocks));
   __syncthreads();
   const float mu = mu_s;
+  const int lane = threadIdx.x & 31;
+  const bool e4m3 = dq_type == QL_DQ_E4M3;
+  const bool vec_in = (reinterpret_cast<uintptr_t>(absmax) & 15) == 0;
+  const bool vec_out = (reinterpret_cast<uintptr_t>(code) & 7) == 0;
   const int64_t n_2 = (n_b + 255) / 256;
-  for (int64_t g = blockIdx.x; g < n_2; g += gridDim.x) {
-    const int64_t i = g * 256 + threadIdx.x;
-    const bool valid = i < n_b;
-    const float c = valid ? __fsub_rn(absmax[i], mu) : 0.0f;
-    float a = fabsf(c);
+  const int64_t nw = (int64_t)gridDim.x * kDqWarps;
+  for (int64_t g = (int64_t)blockIdx.x * kDqWarps + (threadIdx.x >> 5); g < n_2; g += nw) {
+    const int64_t i0 = g * 256 + lane * 8;
+    const bool whole = i0 + 8 <= n_b;
+    float c[8];
+    if (whole && vec_in) {
+      const float4 v0 = __ldg(reinterpret_cast<const float4 *>(absmax + i0));
+      const float4 v1 = __ldg(reinterpret_cast<const float4 *>(absmax + i0 + 4));
+      c[0] = v0.x; c[1] = v0.y; c[2] = v0.z; c[3] = v0.w;
+      c[4] = v1.x; c[5] = v1.y; c[6] = v1.z; c[7] = v1.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) c[e] = i0 + e < n_b ? __ldg(absmax + i0 + e) : mu;  // past the end: c - mu = 0
+    }
+    float a = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      c[e] = __fsub_rn(c[e], mu);
+      a = fmaxf(a, fabsf(c[e]));
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
-    __syncthreads();
-    float a2 = red[0];
+    const float st = __fdiv_rn(a, e4m3 ? 448.0f : 127.0f);
+    uint32_t k[8];
 #pragma unroll
-    for (int k = 1; k < 8; ++k) a2 = fmaxf(a2, red[k]);
-    __syncthreads();  // red is rewritten by the next group
-    const bool e4m3 = dq_type == QL_DQ_E4M3;
-    const float st = __fdiv_rn(a2, e4m3 ? 448.0f : 127.0f);
-    if (valid) {
-      int k = 0;
+    for (int e = 0; e < 8; ++e) {
+      k[e] = 0u;
       if (st != 0.0f) {
-        const float x = __fdiv_rn(c, st);
-        if (e4m3) {
-          k = (int)(int8_t)(uint8_t)e4m3_code(x);
-        } else {
-          const float t = fminf(fmaxf(rintf(x), -127.0f), 127.0f);
-          k = (int)t;
-        }
+        const float x = __fdiv_rn(c[e], st);
+        k[e] = e4m3 ? (uint32_t)e4m3_code(x) : (uint32_t)(uint8_t)(int8_t)(int)fminf(fmaxf(rintf(x), -127.0f), 127.0f);
       }
-      code[i] = (int8_t)k;
     }
-    if (threadIdx.x == 0) step[g] = st;
+    if (whole && vec_out) {
+      *reinterpret_cast<uint2 *>(code + i0) = make_uint2(k[0] | (k[1] << 8) | (k[2] << 16) | (k[3] << 24),
+                                                         k[4] | (k[5] << 8) | (k[6] << 16) | (k[7] << 24));
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (i0 + e < n_b) code[i0 + e] = (int8_t)(uint8_t)k[e];
+    }
+    if (lane == 0) step[g] = st;
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) *mean = mu;
 }
@@ -362,10 +386,21 @@ cudaError_t launch_double_quant(const float *absmax, int64_t n_b, int64_t total_
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 148;
   }
-  const int64_t grid = std::min<int64_t>(n_2, (int64_t)sms * 8);
-  k_double_quant<<<(unsigned)grid, 256, 0, st>>>(absmax, n_b, total_blocks, sum, dq_type, code, step, mean);
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((n_2 + kDqWarps - 1) / kDqWarps, (int64_t)sms * 8));
+  // a programmatic dependent of the first-level kernel: its launch overlaps
+  // that kernel's tail, and it waits for it before reading
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kDqWarps * 32);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_double_quant, absmax, n_b, total_blocks, sum, dq_type, code, step, mean);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_dequantize(const ql_nf4_tensor &q, uint16_t *W_out, cudaStream_t st) {
