@@ -531,23 +531,39 @@ def run_only(args):
 
 
 def bench_forward_fp8(ql, dev, peaks, steps=20, warmup=5):
-    """The LLaMA-7B linears (M = 4096 tokens, r = 64), forward only: the bf16
-    forward and the E4M3 forward (main product on E4M3 operands), each timed
-    over `steps` passes of the 7 calls with CUDA events; flops counted as
-    2 M N K + 2 M r (N + K) per linear for both."""
+    """The LLaMA-7B linears (M = 4096 tokens, r = 64): the bf16 and the E4M3
+    forward, and the bf16 and the E4M3 backward (dX main product on E4M3),
+    each timed over `steps` passes of the 7 calls with CUDA events; flops
+    counted as 2 M N K + 2 M r (N + K) per linear forward and
+    2 M N K + 4 M r (N + K) per linear backward for both."""
     import torch
     wl = workload_of("llama7b")
     layers = build_layers(ql, dev, wl)
-    ws_bytes = max(max(ql.workspace_size(ql.OP_LINEAR_FWD, c.M, c.N, c.K, c.r),
-                       ql.workspace_size(ql.OP_LINEAR_FWD_FP8, c.M, c.N, c.K, c.r)) for c in wl.cases)
+    ws_bytes = max(max(ql.workspace_size(op, c.M, c.N, c.K, c.r)
+                       for op in (ql.OP_LINEAR_FWD, ql.OP_LINEAR_FWD_FP8, ql.OP_LINEAR_BWD, ql.OP_LINEAR_BWD_FP8))
+                   for c in wl.cases)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    flops = sum(2.0 * c.M * c.N * c.K + 2.0 * c.M * c.r * (c.N + c.K) for c in wl.cases)
-    out = {"workload": wl.name + " forward", "flops_per_pass": flops}
-    for name, fn in (("bf16", ql.qlora_linear_fwd), ("e4m3", ql.qlora_linear_fwd_fp8)):
+    fwd_flops = sum(2.0 * c.M * c.N * c.K + 2.0 * c.M * c.r * (c.N + c.K) for c in wl.cases)
+    bwd_flops = sum(2.0 * c.M * c.N * c.K + 4.0 * c.M * c.r * (c.N + c.K) for c in wl.cases)
+    out = {"workload": wl.name + " forward and backward", "flops_per_pass": fwd_flops,
+           "bwd_flops_per_pass": bwd_flops}
+
+    def fwd(fn):
         def one_pass():
             for L in layers:
                 c = L["case"]
                 fn(L["X"], L["q"], L["A"], L["B"], c.scale, Y=L["Y"], XA=L["XA"], ws=ws)
+        return one_pass
+
+    def bwd(fn):
+        def one_pass():
+            for L in layers:
+                c = L["case"]
+                fn(L["dY"], L["X"], L["XA"], L["q"], L["A"], L["B"], c.scale, dX=L["dX"], dA=L["dA"], dB=L["dB"],
+                   ws=ws)
+        return one_pass
+
+    def timed(one_pass, flops):
         for _ in range(warmup):
             one_pass()
         torch.cuda.synchronize()
@@ -558,8 +574,14 @@ def bench_forward_fp8(ql, dev, peaks, steps=20, warmup=5):
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / steps
-        out[name] = {"ms_per_pass": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12}
+        return {"ms_per_pass": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12}
+
+    out["bf16"] = timed(fwd(ql.qlora_linear_fwd), fwd_flops)
+    out["e4m3"] = timed(fwd(ql.qlora_linear_fwd_fp8), fwd_flops)
     out["speedup_e4m3_over_bf16"] = out["bf16"]["ms_per_pass"] / out["e4m3"]["ms_per_pass"]
+    out["bwd_bf16"] = timed(bwd(ql.qlora_linear_bwd), bwd_flops)
+    out["bwd_e4m3"] = timed(bwd(ql.qlora_linear_bwd_fp8), bwd_flops)
+    out["bwd_speedup_e4m3_over_bf16"] = out["bwd_bf16"]["ms_per_pass"] / out["bwd_e4m3"]["ms_per_pass"]
     out["peak_e4m3_tflops"] = 2.0 * peaks["bf16_tflops"]
     out["peak_note"] = "E4M3 dense peak taken as 2x the measured bf16 burst peak (nominal ratio)"
     del layers

@@ -96,6 +96,7 @@ extern "C" size_t ql_workspace_size(int op, int64_t M, int64_t N, int64_t K, int
     case QL_OP_LINEAR_BWD: return linear_bwd_ws(M, N, K, r);
     case QL_OP_QUANTIZE_HOST: return quantize_host_ws(N, K);
     case QL_OP_LINEAR_FWD_FP8: return linear_fwd_fp8_ws(M, N, K, r);
+    case QL_OP_LINEAR_BWD_FP8: return linear_bwd_fp8_ws(M, N, K, r);
     default: return (size_t)-1;
   }
 }
@@ -242,6 +243,20 @@ extern "C" int qlora_linear_bwd(const uint16_t *dY, const uint16_t *X, const uin
   a.dX = dX; a.dA = dA; a.dB = dB; a.ws = ws; a.ws_bytes = ws_bytes;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   return linear_bwd(a);
+}
+
+extern "C" int qlora_linear_bwd_fp8(const uint16_t *dY, const uint16_t *X, const uint16_t *XA, int64_t M,
+                                const ql_nf4_tensor *W, const uint16_t *A, const uint16_t *B, int32_t r,
+                                float scale, uint16_t *dX, float *dA, float *dB, void *ws, size_t ws_bytes,
+                                ql_stream_t stream) {
+  g_msg[0] = 0;
+  int rc = check_tensor(W, "qlora_linear_bwd_fp8", true);
+  if (rc) return rc;
+  LinearArgs a{};
+  a.dY = dY; a.X = X; a.XA_in = XA; a.M = M; a.W = *W; a.A = A; a.B = B; a.r = r; a.scale = scale;
+  a.dX = dX; a.dA = dA; a.dB = dB; a.ws = ws; a.ws_bytes = ws_bytes;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  return linear_bwd_fp8(a);
 }
 
 extern "C" int qlora_merge(const ql_nf4_tensor *W, const uint16_t *A, const uint16_t *B, int32_t r, float scale,

@@ -1,13 +1,16 @@
 // Operand preparation for the E4M3 forward (the FP8 variant of the training
 // GEMM; E4M3 = 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, largest
 // finite 448), one launch, two kinds of CTA:
-//   CTAs [0, M)      row m of X: E_m = the largest exponent with
-//                    amax_m * 2^E_m <= 448 (0 for an all-zero row), and the
-//                    codes e4m3(x * 2^E_m) (exact scaling, then round to
-//                    nearest even, saturating)
-//   CTAs [M, M + G)  the largest |m_hat| over the weight's blocks (atomic max
-//                    into a word the caller cleared), from which the GEMM
-//                    takes the weight's exponent E the same way
+//   CTAs [0, gw)      the largest |m_hat| over the weight's blocks (atomic max
+//                     into a word the caller cleared), from which the GEMM
+//                     takes the weight's exponent E
+//   CTAs [gw, grid)   rows of X in turn (a persistent grid): E_m = the largest
+//                     exponent with amax_m * 2^E_m <= 448 (0 for an all-zero
+//                     row), and the codes e4m3(x * 2^E_m) (exact scaling, then
+//                     round to nearest even, saturating)
+// A row CTA holds its row in registers and has the next row's loads in
+// flight while it codes the current one (two register sets taking rows in
+// turn), so every row costs one read of X and no exposed memory latency.
 #include <algorithm>
 
 #include "common.cuh"
@@ -17,11 +20,7 @@
 namespace ql {
 namespace {
 
-constexpr int kWmaxCtas = 148 * 2;
-// rows of up to kRowRegs x (threads) x 8 elements stay in registers between
-// the two passes; rows of up to 6144 elements take 128-thread CTAs (more rows
-// in flight per SM), longer ones 256
-constexpr int kRowRegs = 6;
+constexpr int kWmaxCtas = 148;
 
 __device__ __forceinline__ float absmax8(const uint4 v) {
   const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
@@ -31,20 +30,23 @@ __device__ __forceinline__ float absmax8(const uint4 v) {
   return a;
 }
 
+// Eight codes e4m3(x 2^E_m) (the scaling is exact), element 2j in the low byte
+// of pair j: the hardware conversion (round to nearest even, saturating at
+// +-448), which equals e4m3_code for every finite input.
 __device__ __forceinline__ uint2 codes8(const uint4 v, float sc) {
   const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
-  uint32_t b[8];
+  uint32_t h[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    b[2 * j] = e4m3_code(__fmul_rn(bf16lo_to_f32(wd[j]), sc));
-    b[2 * j + 1] = e4m3_code(__fmul_rn(bf16hi_to_f32(wd[j]), sc));
-  }
-  return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+  for (int j = 0; j < 4; ++j)
+    h[j] = ptx::cvt_e4m3x2(__fmul_rn(bf16lo_to_f32(wd[j]), sc), __fmul_rn(bf16hi_to_f32(wd[j]), sc));
+  return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
 }
 
-// The row's amax over the CTA (a: this thread's share) -> E_m (stored by
-// thread 0) and the exact scale 2^E_m.
-__device__ __forceinline__ float row_scale(float a, float *red, int warp, int lane, int *row_exp, int64_t row) {
+// The row's amax over the CTA (a: this thread's share; red: this row's
+// buffer of the two the CTA alternates, so one barrier per row suffices) ->
+// E_m (stored by thread 0) and the exact scale 2^E_m.
+__device__ __forceinline__ float row_scale(float a, float *red, int64_t row, int *row_exp) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
   if (lane == 0) red[warp] = a;
@@ -56,59 +58,138 @@ __device__ __forceinline__ float row_scale(float a, float *red, int warp, int la
   return __uint_as_float((uint32_t)(E + 127) << 23);
 }
 
-__global__ void __launch_bounds__(256, 4) k_prep_e4m3(const uint4 *__restrict__ X, int64_t M, int64_t K,
-                                                   uint2 *__restrict__ codes, int *__restrict__ row_exp, NF4View w,
-                                                   float *__restrict__ wmax) {
-  __shared__ float red[8];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if ((int64_t)blockIdx.x >= M) {
+// R: 16-byte pieces of a row per thread held in registers (rows of up to
+// R x threads x 8 elements; longer rows are read twice).
+template <int R>
+__global__ void __launch_bounds__(R == 4 ? 128 : 256, R == 4 ? 8 : 3) k_prep_e4m3(const uint4 *__restrict__ X, int64_t M, int64_t K,
+                                                                  uint2 *__restrict__ codes, int *__restrict__ row_exp,
+                                                                  NF4View w, float *__restrict__ wmax, int gw) {
+  __shared__ float red[2][8];
+  if ((int)blockIdx.x < gw) {
     // ------------------------------------------------ weight: max |m_hat|
-    const int64_t n_b = w.rows * w.cols / 64;
+    // 16 consecutive blocks per thread and load (one 16-byte load of codes,
+    // or four of fp32 constants; the 16 share one second-level step), two
+    // such loads in flight
+    const int64_t n_b = w.rows * w.cols / 64, nch = (n_b + 15) / 16;
     const float mu = w.dq ? __ldg(w.mean) : 0.0f;
+    const int64_t stride = (int64_t)gw * blockDim.x;
     float m = 0.0f;
-    const int64_t stride = (int64_t)(gridDim.x - M) * blockDim.x;
-    for (int64_t b = ((int64_t)blockIdx.x - M) * blockDim.x + threadIdx.x; b < n_b; b += stride) {
-      const float mh = w.dq ? __fadd_rn(__fmul_rn(dq_code_value(__ldg(w.code + b), w.dqt), __ldg(w.step + (b >> 8))),
-                                        mu)
-                            : __ldg(w.absmax + b);
-      m = fmaxf(m, fabsf(mh));
+    auto chunk = [&](int64_t c) {
+      const int64_t b0 = c * 16;
+      float v[16];
+      if (b0 + 16 <= n_b) {
+        if (w.dq) {
+          const uint4 q = __ldg(reinterpret_cast<const uint4 *>(w.code + b0));
+          const float st = __ldg(w.step + (b0 >> 8));
+          const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            v[e] = __fadd_rn(__fmul_rn(dq_code_value((int8_t)(wd[e >> 2] >> (8 * (e & 3))), w.dqt), st), mu);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4 f = __ldg(reinterpret_cast<const float4 *>(w.absmax + b0) + e);
+            v[4 * e] = f.x; v[4 * e + 1] = f.y; v[4 * e + 2] = f.z; v[4 * e + 3] = f.w;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int64_t b = b0 + e;
+          v[e] = 0.0f;
+          if (b < n_b)
+            v[e] = w.dq ? __fadd_rn(__fmul_rn(dq_code_value(__ldg(w.code + b), w.dqt), __ldg(w.step + (b >> 8))), mu)
+                        : __ldg(w.absmax + b);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(v[e]));
+    };
+    for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < nch; c += 2 * stride) {
+      chunk(c);
+      if (c + stride < nch) chunk(c + stride);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) red[warp] = m;
+    if ((threadIdx.x & 31) == 0) red[0][threadIdx.x >> 5] = m;
     __syncthreads();
     if (threadIdx.x == 0) {
-      for (int i = 1; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
+      for (int i = 1; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[0][i]);
       atomicMax(reinterpret_cast<int *>(wmax), __float_as_int(m));  // non-negative: bit order = value order
     }
     return;
   }
-  // ------------------------------------------------ row of X
-  const int64_t row = blockIdx.x, n8 = K / 8;
-  const uint4 *x = X + row * n8;
-  uint2 *c = codes + row * n8;
-  if (n8 <= (int64_t)kRowRegs * blockDim.x) {
-    // the whole row in registers: one read of X
-    uint4 v[kRowRegs];
-    float a = 0.0f;
+  // ------------------------------------------------ rows of X
+  const int64_t n8 = K / 8, gr = (int64_t)gridDim.x - gw;
+  const int nt = blockDim.x;
+  int64_t row = (int64_t)blockIdx.x - gw;
+  if (n8 <= (int64_t)R * nt) {
+    auto load = [&](int64_t r, uint4 (&v)[R]) {
 #pragma unroll
-    for (int j = 0; j < kRowRegs; ++j) {
-      const int64_t i = threadIdx.x + (int64_t)j * blockDim.x;
-      v[j] = i < n8 ? __ldg(x + i) : make_uint4(0u, 0u, 0u, 0u);
-      a = fmaxf(a, absmax8(v[j]));
-    }
-    const float sc = row_scale(a, red, warp, lane, row_exp, row);
+      for (int j = 0; j < R; ++j) {
+        const int64_t i = threadIdx.x + (int64_t)j * nt;
+        v[j] = (r < M && i < n8) ? __ldg(X + r * n8 + i) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    auto code = [&](int64_t r, const uint4 (&v)[R], float *rd) {
+      float a = 0.0f;
 #pragma unroll
-    for (int j = 0; j < kRowRegs; ++j) {
-      const int64_t i = threadIdx.x + (int64_t)j * blockDim.x;
-      if (i < n8) c[i] = codes8(v[j], sc);
+      for (int j = 0; j < R; ++j) a = fmaxf(a, absmax8(v[j]));
+      const float sc = row_scale(a, rd, r, row_exp);
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        const int64_t i = threadIdx.x + (int64_t)j * nt;
+        if (i < n8) codes[r * n8 + i] = codes8(v[j], sc);
+      }
+    };
+    uint4 va[R], vb[R];
+    load(row, va);
+#pragma unroll 1
+    for (; row < M; row += 2 * gr) {
+      load(row + gr, vb);
+      code(row, va, red[0]);
+      if (row + gr >= M) break;
+      load(row + 2 * gr, va);
+      code(row + gr, vb, red[1]);
     }
     return;
   }
-  float a = 0.0f;
-  for (int64_t i = threadIdx.x; i < n8; i += blockDim.x) a = fmaxf(a, absmax8(__ldg(x + i)));
-  const float sc = row_scale(a, red, warp, lane, row_exp, row);
-  for (int64_t i = threadIdx.x; i < n8; i += blockDim.x) c[i] = codes8(__ldg(x + i), sc);  // again (mostly L2)
+  int par = 0;
+#pragma unroll 1
+  for (; row < M; row += gr, par ^= 1) {  // long rows: amax pass, then the row again (mostly from L2)
+    const uint4 *x = X + row * n8;
+    float a = 0.0f;
+    for (int64_t i = threadIdx.x; i < n8; i += nt) a = fmaxf(a, absmax8(__ldg(x + i)));
+    const float sc = row_scale(a, red[par], row, row_exp);
+    for (int64_t i = threadIdx.x; i < n8; i += nt) codes[row * n8 + i] = codes8(__ldg(x + i), sc);
+  }
+}
+
+template <int R>
+int row_ctas_per_sm() {
+  static int n[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!n[dev & 63]) {
+    int k = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, k_prep_e4m3<R>, R == 4 ? 128 : 256, 0) != cudaSuccess ||
+        k < 1)
+      k = 1;
+    n[dev & 63] = k;
+  }
+  return n[dev & 63];
+}
+
+int sm_count() {
+  static int sms[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!sms[dev & 63]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    sms[dev & 63] = v > 0 ? v : 148;
+  }
+  return sms[dev & 63];
 }
 
 }  // namespace
@@ -118,10 +199,19 @@ cudaError_t launch_prep_e4m3(const uint16_t *X, int64_t M, int64_t K, const NF4V
   cudaError_t e = cudaMemsetAsync(wmax, 0, sizeof(float), st);
   if (e != cudaSuccess) return e;
   const int64_t n_b = w.rows * w.cols / 64;
-  const int64_t g = std::max<int64_t>(1, std::min<int64_t>((n_b + 255) / 256, kWmaxCtas));
-  const unsigned threads = K <= 6144 ? 128u : 256u;
-  k_prep_e4m3<<<(unsigned)(M + g), threads, 0, st>>>(reinterpret_cast<const uint4 *>(X), M, K,
-                                                     reinterpret_cast<uint2 *>(codes), row_exp, w, wmax);
+  const bool small = K <= 4 * 128 * 8;  // rows of up to 4096 elements: 128 threads x 4 pieces
+  const int nt = small ? 128 : 256;
+  const int64_t per_cta = (int64_t)nt * 16 * 2;  // blocks a weight CTA takes per round
+  const int gw = (int)std::max<int64_t>(1, std::min<int64_t>((n_b + per_cta - 1) / per_cta, kWmaxCtas));
+  const int64_t per_sm = small ? row_ctas_per_sm<4>() : row_ctas_per_sm<6>();
+  const int64_t gr = std::max<int64_t>(1, std::min<int64_t>(M, per_sm * sm_count()));
+  const dim3 grid((unsigned)(gw + gr));
+  if (small)
+    k_prep_e4m3<4><<<grid, nt, 0, st>>>(reinterpret_cast<const uint4 *>(X), M, K, reinterpret_cast<uint2 *>(codes),
+                                        row_exp, w, wmax, gw);
+  else
+    k_prep_e4m3<6><<<grid, nt, 0, st>>>(reinterpret_cast<const uint4 *>(X), M, K, reinterpret_cast<uint2 *>(codes),
+                                        row_exp, w, wmax, gw);
   count_launch();
   return cudaGetLastError();
 }

@@ -327,6 +327,91 @@ int linear_fwd_fp8(const LinearArgs &a) {
   return launch_nf4_gemm(g, st);
 }
 
+// E4M3 backward workspace: [max |m_hat| | pad][row exponents of dY, M int32]
+// [dY codes M x N bytes][Gs' M x r bf16][G M x r bf16][XA M x r bf16 (recomputed
+// when the caller passes none)]
+size_t linear_bwd_fp8_ws(int64_t M, int64_t N, int64_t K, int32_t r) {
+  if (M <= 0 || N <= 0 || K <= 0 || !rank_ok(r)) return 0;
+  return 256 + up256((size_t)M * 4) + up256((size_t)M * N) + 3 * up256((size_t)M * r * 2);
+}
+
+// Backward with E4M3 main steps in dX (5 or 6 launches, in stream order):
+//   1. dY codes e4m3(dy 2^E_m) with the row exponents, and max |m_hat|  (k_prep_e4m3)
+//   (XA = X A, when the caller passes no saved XA)                       LoRA kernel
+//   2. G = dY B^T -> G16 = bf16(G) and Gs' = bf16(fl32(s G) 2^(E_m + E)) LoRA kernel
+//   3. dX = 2^(-E_m - E) (dY_e4m3 . W_e4m3 + Gs' A^T)                     CTA-pair GEMM
+//   4. dA = s X^T G16 and dB = s XA^T dY (as in the bf16 backward)       one LoRA launch
+int linear_bwd_fp8(const LinearArgs &a) {
+  const char *fn = "qlora_linear_bwd_fp8";
+  if (!a.dY || !a.X || !a.A || !a.B || !a.dX || !a.dA || !a.dB)
+    return set_error(QL_ERR_INVALID, "%s: null operand", fn);
+  if (!al16(a.dY) || !al16(a.X) || !al16(a.A) || !al16(a.B) || !al16(a.dX) || !al16(a.dA) || !al16(a.dB) ||
+      (a.XA_in && !al16(a.XA_in)))
+    return set_error(QL_ERR_MISALIGNED, "%s: operand not 16-byte aligned", fn);
+  const int64_t M = a.M, N = a.W.rows, K = a.W.cols;
+  const int r = a.r;
+  QL_TRY(check_common(a, fn, linear_bwd_fp8_ws(M, N, K, r)));
+  if (N % 16)  // rows of dY codes are TMA rows: a multiple of 16 bytes
+    return set_error(QL_ERR_UNSUPPORTED, "%s: N = %lld not a multiple of 16", fn, (long long)N);
+  cudaStream_t st = a.stream;
+  note_other_call(st);  // the next call waits for this one in full
+  char *ws = static_cast<char *>(a.ws);
+  float *wmax = reinterpret_cast<float *>(ws);
+  int *rows = reinterpret_cast<int *>(ws + 256);
+  uint8_t *dyq = reinterpret_cast<uint8_t *>(ws + 256 + up256((size_t)M * 4));
+  uint16_t *gs8 = reinterpret_cast<uint16_t *>(ws + 256 + up256((size_t)M * 4) + up256((size_t)M * N));
+  uint16_t *g16 = reinterpret_cast<uint16_t *>(reinterpret_cast<char *>(gs8) + up256((size_t)M * r * 2));
+  uint16_t *xa_tmp = reinterpret_cast<uint16_t *>(reinterpret_cast<char *>(g16) + up256((size_t)M * r * 2));
+  const NF4View w = nf4_view(a.W);
+  QL_TRY(check_cuda(launch_prep_e4m3(a.dY, M, N, w, dyq, rows, wmax, st), "qlora_linear_bwd_fp8: operand codes"));
+  const uint16_t *xa = a.XA_in;
+  if (!xa) {  // XA = X A (fp32 accumulation, bf16)
+    LoraProblem L{};
+    L.A = a.X; L.a_mn = false; L.B = a.A; L.b_mn = true;
+    L.P = M; L.Q = r; L.T = K; L.mode = 0; L.scale = 1.0f; L.out = xa_tmp; L.ldo = r;
+    L.dep = kDepStart;
+    QL_TRY(launch_lora(L, st));
+    xa = xa_tmp;
+  }
+  {  // G16 = bf16(dY B^T), Gs' = bf16(fl32(s G) 2^(E_m + E)): dY [M][N], B [r][N]
+    LoraProblem L{};
+    L.A = a.dY; L.a_mn = false; L.B = a.B; L.b_mn = false;
+    L.P = M; L.Q = r; L.T = N; L.mode = 0; L.scale = a.scale; L.out = gs8; L.ldo = r;
+    L.out2 = g16; L.ldo2 = r;
+    L.row_exp = rows;
+    L.wmax = wmax;
+    L.dep = kDepStart;
+    QL_TRY(launch_lora(L, st));
+  }
+  {  // dX = 2^(-E_m - E) (dY_e4m3 W_e4m3 + Gs' A^T)
+    GemmProblem g{};
+    g.trans = true;
+    g.A = reinterpret_cast<const uint16_t *>(dyq); g.M = M; g.Kred = N;
+    g.A2 = gs8; g.B2 = a.A; g.r = r;
+    g.w = w;
+    g.out = a.dX; g.Nout = K;
+    g.fp8 = true;
+    g.row_exp = rows;
+    g.wmax = wmax;
+    // the main loop reads the dY codes, the weight and max |m_hat|, written
+    // by the operand kernel, which completed before the G kernel (a
+    // dependent that waits for it at its start) let this GEMM launch
+    g.early_main = true;
+    QL_TRY(launch_nf4_gemm(g, st));
+  }
+  // dA = s X^T G16 (X [M][K], G16 [M][r] read MN-major); dB = s XA^T dY, stored
+  // transposed; their inputs were complete before the dX GEMM let them start
+  LoraProblem LA{};
+  LA.A = a.X; LA.a_mn = true; LA.B = g16; LA.b_mn = true;
+  LA.P = K; LA.Q = r; LA.T = M; LA.mode = 1; LA.scale = a.scale; LA.out = a.dA; LA.ldo = r;
+  LA.dep = kDepExit;
+  LoraProblem LB{};
+  LB.A = a.dY; LB.a_mn = true; LB.B = xa; LB.b_mn = true;
+  LB.P = N; LB.Q = r; LB.T = M; LB.mode = 2; LB.scale = a.scale; LB.out = a.dB; LB.ldo = N;
+  LB.dep = kDepExit;
+  return launch_lora2(LA, LB, st);
+}
+
 int linear_bwd(const LinearArgs &a) {
   const char *fn = "qlora_linear_bwd";
   if (!a.dY || !a.X || !a.A || !a.B || !a.dX || !a.dA || !a.dB)

@@ -24,6 +24,9 @@ int linear_bwd(const LinearArgs &a);
 // The E4M3 forward (main product on E4M3 operands, LoRA term in bf16).
 size_t linear_fwd_fp8_ws(int64_t M, int64_t N, int64_t K, int32_t r);
 int linear_fwd_fp8(const LinearArgs &a);
+// The E4M3 backward (dX main product on E4M3 operands; dA, dB as in bf16).
+size_t linear_bwd_fp8_ws(int64_t M, int64_t N, int64_t K, int32_t r);
+int linear_bwd_fp8(const LinearArgs &a);
 // Record that a call other than a training linear was issued on `st` (its
 // kernels do not let dependents start early; see linear.cu).
 void note_other_call(cudaStream_t st);

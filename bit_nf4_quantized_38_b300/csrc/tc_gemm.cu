@@ -377,18 +377,21 @@ struct Geo {
 };
 }  // namespace pairk
 
-// With kFp8 (forward form only) the main steps are E4M3 x E4M3 products on
-// kind::f8f6f4: A = X quantized per row to E4M3 (the same 128-byte smem rows
+// With kFp8 the main steps are E4M3 x E4M3 products on kind::f8f6f4: A = X
+// (forward) or dY (dX) quantized per row to E4M3 (the same 128-byte smem rows
 // now hold 128 reduction elements, so a step covers K = 128 with the same four
 // MMA instructions of K = 32), B = the weight converted to E4M3 with a
 // power-of-two scale 2^E; the LoRA steps stay bf16 into the same accumulator
-// with XAs already multiplied by 2^(E_m + E), and the epilogue multiplies
-// each row by 2^(-E_m - E) (exact).
+// with their A operand (XAs, or s G) already multiplied by 2^(E_m + E), and
+// the epilogue multiplies each row by 2^(-E_m - E) (exact).  In the dX form
+// each converter thread writes one 128-byte row: the E4M3 values of weight
+// row n (a reduction index) over this CTA's 128 output columns, which the
+// tensor core reads as an MN-major B operand (one 128-column atom, 8-row
+// groups 1 KB apart, 32 reduction rows = 4 KB per instruction).
 template <bool kTrans, int NACC, bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pairk::THREADS, 1)
 k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                 const __grid_constant__ CUtensorMap tmB2, const GemmArgs p) {
-  static_assert(!(kFp8 && kTrans), "E4M3 main steps: forward form only");
   using G = pairk::Geo<NACC>;
   constexpr int PSTAGES = pairk::STAGES, PBK = pairk::BK, BMH = pairk::BMH, BNH = pairk::BNH,
                 GROUP_WARPS = pairk::GROUP_WARPS;
@@ -528,17 +531,20 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         // K-major B half: 128 rows of 128 B.  MN-major B half (W_hat^T, or
         // the LoRA B in the forward): 2 MN-atoms of 64 output columns, 8 KB
         // apart, each 8 K-atoms of 8 reduction rows, 1 KB apart.
-        const uint64_t b_desc = bmn ? ptx::desc_sw128(b_addr, 8192, 1024) : ptx::desc_sw128(b_addr, 16, 1024);
         const bool e4m3 = kFp8 && ks < p.ksteps_main;
+        // (an E4M3 MN-major half is one 128-column atom: no second atom, LBO 0)
+        const uint64_t b_desc = bmn ? ptx::desc_sw128(b_addr, e4m3 ? 0 : 8192, 1024) : ptx::desc_sw128(b_addr, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < PBK / 16; ++kk) {
-          // 32 bytes per instruction either way: 16 bf16 or 32 E4M3 elements
-          const uint64_t bd = b_desc + (uint64_t)(bmn ? kk * 128 : kk * 2);
+          // K-major: 32 bytes per instruction either way (16 bf16 or 32 E4M3
+          // elements); MN-major: 16 bf16 reduction rows (2 KB) or 32 E4M3
+          // rows (4 KB)
+          const uint64_t bd = b_desc + (uint64_t)(bmn ? kk * (e4m3 ? 256 : 128) : kk * 2);
 #pragma unroll
           for (int a = 0; a < NACC; ++a) {
             const uint64_t ad = ptx::desc_sw128(a_addr + a * G::A_ONE, 16, 1024) + (uint64_t)(kk * 2);
             if (e4m3)
-              ptx::mma_e4m3_pair(tmem + a * 256, ad, bd, ptx::idesc_e4m3(256, 256, false),
+              ptx::mma_e4m3_pair(tmem + a * 256, ad, bd, ptx::idesc_e4m3(256, 256, bmn),
                                  (ks > 0 || kk > 0) ? 1u : 0u);
             else
               ptx::mma_bf16_pair(tmem + a * 256, ad, bd, bmn ? idesc_mn : idesc_kmaj,
@@ -568,6 +574,11 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       rb_kb0 = 0;                         // + ks
       rb_dst = (uint32_t)ct * 128u;
       rb_swz = (uint32_t)(ct & 7);
+    } else if (kFp8) {
+      rb_n = ct;                                          // + 128 ks: the reduction row
+      rb_kb0 = (n0 + (int)crank * BNH) >> 6;              // + h: output columns / 64
+      rb_dst = (uint32_t)ct * 128u;
+      rb_swz = (uint32_t)(ct & 7);
     } else {
       const int nl = ct & 63, kbl = ct >> 6;
       rb_n = nl;                                          // + 64 ks
@@ -583,7 +594,7 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     auto fetch = [&](int ks, RowBlockSrc (&r)[RB]) {
 #pragma unroll
       for (int h = 0; h < RB; ++h) {
-        if (kTrans) load_rowblock(p.w, rb_n + (int64_t)ks * 64, rb_kb0, r[h]);
+        if (kTrans) load_rowblock(p.w, rb_n + (int64_t)ks * 64 * RB, rb_kb0 + h, r[h]);
         else load_rowblock(p.w, rb_n, rb_kb0 + RB * ks + h, r[h]);
       }
     };
@@ -883,8 +894,11 @@ int launch_nf4_gemm(const GemmProblem &g, cudaStream_t st) {
   unsigned long long *span = (sp.on && sp.used < sp.capacity) ? sp.buf + 2 * sp.used : nullptr;
   int rc;
   if (g.fp8) {
-    if (g.trans || !g.row_exp || !g.wmax) return set_error(QL_ERR_INVALID, "E4M3 GEMM: forward form with scales only");
-    rc = g.M <= 256 ? launch_pair<false, 1, true>(g, span, st) : launch_pair<false, 2, true>(g, span, st);
+    if (!g.row_exp || !g.wmax) return set_error(QL_ERR_INVALID, "E4M3 GEMM: scales missing");
+    if (g.trans)
+      rc = g.M <= 256 ? launch_pair<true, 1, true>(g, span, st) : launch_pair<true, 2, true>(g, span, st);
+    else
+      rc = g.M <= 256 ? launch_pair<false, 1, true>(g, span, st) : launch_pair<false, 2, true>(g, span, st);
   } else if (!g.trans && g.M <= kSkinnyMaxM && g.part) {
     rc = launch_nf4_skinny(g, span, st);
   } else if (g.M <= 128) {

@@ -16,7 +16,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libq
 QL_OK, QL_ERR_INVALID, QL_ERR_UNSUPPORTED, QL_ERR_MISALIGNED, QL_ERR_CUDA, QL_ERR_TIMEOUT = range(6)
 QL_NF4, QL_FP4 = 0, 1
 QL_DQ_INT8, QL_DQ_E4M3 = 0, 1  # second-level codes (ql_nf4_tensor.dq_type)
-OP_QUANTIZE, OP_DEQUANTIZE, OP_LINEAR_FWD, OP_LINEAR_BWD, OP_QUANTIZE_HOST, OP_LINEAR_FWD_FP8 = range(6)
+(OP_QUANTIZE, OP_DEQUANTIZE, OP_LINEAR_FWD, OP_LINEAR_BWD, OP_QUANTIZE_HOST, OP_LINEAR_FWD_FP8,
+ OP_LINEAR_BWD_FP8) = range(7)
 
 _c_i64, _c_i32, _c_f32, _c_p, _c_sz = (ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
                                        ctypes.c_void_p, ctypes.c_size_t)
@@ -44,6 +45,8 @@ _SIGNATURES = {
                                             _c_f32, _c_p, _c_p, _c_p, _c_sz, _c_p]),
     "qlora_linear_bwd": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, ctypes.POINTER(NF4Struct), _c_p,
                                         _c_p, _c_i32, _c_f32, _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p]),
+    "qlora_linear_bwd_fp8": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, ctypes.POINTER(NF4Struct), _c_p,
+                                            _c_p, _c_i32, _c_f32, _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p]),
     "qlora_merge": (ctypes.c_int, [ctypes.POINTER(NF4Struct), _c_p, _c_p, _c_i32, _c_f32, _c_p, _c_p]),
     "ql_get_device_status": (ctypes.c_int, [_c_p]),
     "ql_selftest_wait": (ctypes.c_int, [ctypes.c_int64, _c_p]),
@@ -336,6 +339,16 @@ def qlora_linear_fwd_fp8(X, q, A, B, scale, Y=None, XA=None, ws=None, stream=Non
 
 def qlora_linear_bwd(dY, X, XA, q, A, B, scale, dX=None, dA=None, dB=None, ws=None, stream=None):
     """Returns (dX bf16, dA fp32, dB fp32)."""
+    return _linear_bwd(lib.qlora_linear_bwd, OP_LINEAR_BWD, dY, X, XA, q, A, B, scale, dX, dA, dB, ws, stream)
+
+
+def qlora_linear_bwd_fp8(dY, X, XA, q, A, B, scale, dX=None, dA=None, dB=None, ws=None, stream=None):
+    """The backward with the dX main product on E4M3 operands; returns (dX bf16, dA fp32, dB fp32)."""
+    return _linear_bwd(lib.qlora_linear_bwd_fp8, OP_LINEAR_BWD_FP8, dY, X, XA, q, A, B, scale, dX, dA, dB, ws,
+                       stream)
+
+
+def _linear_bwd(fn, op, dY, X, XA, q, A, B, scale, dX, dA, dB, ws, stream):
     M = X.shape[0]
     r = A.shape[1]
     _need(dY, torch.bfloat16, "dY", (M, q.rows))
@@ -351,11 +364,10 @@ def qlora_linear_bwd(dY, X, XA, q, A, B, scale, dX=None, dA=None, dB=None, ws=No
     _need(dX, torch.bfloat16, "dX", (M, q.cols))
     _need(dA, torch.float32, "dA", (q.cols, r))
     _need(dB, torch.float32, "dB", (r, q.rows))
-    ws, nbytes = _workspace(workspace_size(OP_LINEAR_BWD, M, q.rows, q.cols, r), dev, ws)
+    ws, nbytes = _workspace(workspace_size(op, M, q.rows, q.cols, r), dev, ws)
     s = q.struct()
-    _check(lib.qlora_linear_bwd(_ptr(dY), _ptr(X), _ptr(XA), M, ctypes.byref(s), _ptr(A), _ptr(B), r,
-                                float(scale), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(ws), nbytes,
-                                _stream(stream)))
+    _check(fn(_ptr(dY), _ptr(X), _ptr(XA), M, ctypes.byref(s), _ptr(A), _ptr(B), r, float(scale), _ptr(dX),
+              _ptr(dA), _ptr(dB), _ptr(ws), nbytes, _stream(stream)))
     return dX, dA, dB
 
 

@@ -61,7 +61,8 @@ enum ql_op {
   QL_OP_LINEAR_FWD = 2,
   QL_OP_LINEAR_BWD = 3,
   QL_OP_QUANTIZE_HOST = 4,
-  QL_OP_LINEAR_FWD_FP8 = 5
+  QL_OP_LINEAR_FWD_FP8 = 5,
+  QL_OP_LINEAR_BWD_FP8 = 6
 };
 
 /*
@@ -276,13 +277,14 @@ QL_API int qlora_linear_fwd(const uint16_t *X, int64_t M, const ql_nf4_tensor *W
  * exponent bits with bias 7, 3 mantissa bits, largest finite 448) -- the FP8
  * variant of the compute dtype the QLoRA project page's configuration example
  * sets (bnb_4bit_compute_dtype); the LoRA term stays bf16:
- *   maxm = max |m_hat| over the weight's blocks; 2^E the largest power of two
- *          with maxm 2^E <= 448 (1 if maxm = 0)
+ *   maxm = max |m_hat| over the weight's blocks; E the largest integer with
+ *          maxm 2^E <= 448 (0 if maxm = 0), clamped to [-60, 60]
  *   Wq   = e4m3(fl32(q[code] * m_hat) * 2^E)      (the weight before its
  *          bf16 rounding, scaled exactly)
- *   per row m of X: sx = fl32(amax_m / 448) (1 for an all-zero row),
- *          Xq = e4m3(fl32(x / sx))
- *   Y[m] = bf16(fl32(sx 2^-E) * (Xq Wq^T + bf16(fl32(s XA) / fl32(sx 2^-E)) B))
+ *   per row m of X: E_m the largest integer with amax_m 2^E_m <= 448 (0 for
+ *          an all-zero row), same clamp; Xq = e4m3(x 2^E_m)  (exact scaling)
+ *   Y[m] = bf16(2^(-E_m - E) (Xq Wq^T + XAs' B)),
+ *          XAs' = bf16(fl32(s XA) 2^(E_m + E))
  * e4m3(x): nearest value, ties to the even code, saturating at +-448; the
  * products accumulate in fp32.  Arguments, layouts and XA_out as for
  * qlora_linear_fwd; K % 8 == 0 (always, as K % 64 == 0).
@@ -310,6 +312,28 @@ QL_API int qlora_linear_bwd(const uint16_t *dY, const uint16_t *X, const uint16_
                      const uint16_t *B, int32_t r, float scale, uint16_t *dX,
                      float *dA, float *dB, void *ws, size_t ws_bytes,
                      ql_stream_t stream);
+
+/*
+ * The same backward with the dX main product on 8-bit floats (E4M3, as in
+ * qlora_linear_fwd_fp8, with dY in the role of X):
+ *   Wq   = the E4M3 weight of qlora_linear_fwd_fp8 (same E)
+ *   per row m of dY: E_m and dYq = e4m3(dy 2^E_m) by the rule of the X rows
+ *   G    = dY B^T (from the bf16 dY, fp32 accumulation)
+ *   dX[m] = bf16(2^(-E_m - E) (dYq Wq + Gs' A^T)),
+ *          Gs' = bf16(fl32(s G) 2^(E_m + E))
+ *   dA = s X^T bf16(G), dB = s (X A)^T dY     (fp32, overwritten; bf16
+ *          operands as in qlora_linear_bwd)
+ * Arguments and layouts as for qlora_linear_bwd; N % 16 == 0 (the rows of
+ * the dY codes are TMA rows), else QL_ERR_UNSUPPORTED.
+ *   ws : ql_workspace_size(QL_OP_LINEAR_BWD_FP8, M, N, K, r) bytes.
+ * Every M takes the tensor-core path (tiles of 256 tokens).  The next call on
+ * the stream waits for this one to complete.
+ */
+QL_API int qlora_linear_bwd_fp8(const uint16_t *dY, const uint16_t *X, const uint16_t *XA,
+                         int64_t M, const ql_nf4_tensor *W, const uint16_t *A,
+                         const uint16_t *B, int32_t r, float scale, uint16_t *dX,
+                         float *dA, float *dB, void *ws, size_t ws_bytes,
+                         ql_stream_t stream);
 
 /*
  * LoRA merge for inference (LoRA tutorial, Lit-LLaMA translation: the

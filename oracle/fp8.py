@@ -1,4 +1,4 @@
-"""The E4M3 forward of the frozen-NF4 linear -- CPU oracle (test infrastructure only).
+"""The E4M3 forward and dX of the frozen-NF4 linear -- CPU oracle (test infrastructure only).
 
 What the pages fix: the QLoRA project page's configuration example sets the
 compute dtype of the 4-bit layer (bnb_4bit_compute_dtype = bfloat16); the
@@ -18,6 +18,11 @@ Reading R22 (the FP8 variant of that compute dtype; plainest choices):
   * Y[m] = 2^(-E_m - E) * (Xq Wq^T) + s (X A) B -- the main product of the
     E4M3 values exactly (fp64 here, fp32 accumulation on the GPU), the LoRA
     term in the same precision as the bf16 forward.
+Reading R24 (the backward, QLoRA abstract: gradients flow through the frozen
+4-bit weight into the adapters): the dX product dY W_hat takes the same E4M3
+weight Wq (same E) and dY coded per row by the X-row rule; G = dY B^T comes
+from the bf16 dY, so dX[m] = 2^(-E_m - E) (dYq Wq) + s G A^T; dA and dB are
+the bf16 backward's (no 8-bit operand enters them).
 Parity: the quantized operands are pinned by the E4M3 coder's own pins and by
 closed-form checks of the scale rules; the product is a library matmul.
 """
@@ -72,3 +77,13 @@ def lora_forward_e4m3(x_bits, qt, a_bits, b_bits, s):
     x = bf16_bits_to_f64(np.asarray(x_bits, dtype=np.uint16))
     lora = float(s) * ((x @ bf16_bits_to_f64(a_bits)) @ bf16_bits_to_f64(b_bits))
     return rs[:, None] * (xq @ wq.T) + lora, (E, Em, rs)
+
+
+def lora_backward_e4m3(dy_bits, qt, a_bits, b_bits, s):
+    """dX (fp64, M x K) of R24, and (E, E_m of the dY rows, row factors 2^(-E_m - E))."""
+    E, wq = weight_e4m3(qt)
+    Em, dyq = rows_e4m3(dy_bits)
+    rs = np.ldexp(1.0, -Em - E)
+    dy = bf16_bits_to_f64(np.asarray(dy_bits, dtype=np.uint16))
+    lora = float(s) * ((dy @ bf16_bits_to_f64(b_bits).T) @ bf16_bits_to_f64(a_bits).T)
+    return rs[:, None] * (dyq @ wq) + lora, (E, Em, rs)

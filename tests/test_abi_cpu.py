@@ -128,6 +128,19 @@ def test_linear_calls_reject_bad_arguments_on_host(ql):
     need = ql.workspace_size(ql.OP_LINEAR_BWD, 64, 256, 512, 16)
     assert need > 0 and bwd(wsb=need - 1) == E.QL_ERR_UNSUPPORTED
 
+    # the E4M3 backward: the same checks, and N a multiple of 16 (TMA rows of dY codes)
+    def bwd8(dY=p, X=p, XA=None, M=64, w=None, A=p, B=p, r=16, dX=p, dA=p, dB=p, ws=p, wsb=big):
+        w = w or W()
+        return lib.qlora_linear_bwd_fp8(dY, X, XA, M, ctypes.byref(w), A, B, r, 1.0, dX, dA, dB, ws, wsb, None)
+
+    assert bwd8(dB=None) == E.QL_ERR_INVALID
+    assert bwd8(dY=odd) == E.QL_ERR_MISALIGNED
+    assert bwd8(r=24) == E.QL_ERR_UNSUPPORTED
+    assert bwd8(w=W(rows=264)) == E.QL_ERR_UNSUPPORTED
+    assert "multiple of 16" in lib.ql_last_error().decode()
+    need = ql.workspace_size(ql.OP_LINEAR_BWD_FP8, 64, 256, 512, 16)
+    assert need >= 64 * 256 and bwd8(wsb=need - 1) == E.QL_ERR_UNSUPPORTED  # holds the M x N dY codes
+
 
 def test_dequantize_and_noalloc_reject_bad_arguments_on_host(ql):
     _fake_pointers_only_without_gpu()

@@ -1,7 +1,9 @@
-"""GPU parity of the E4M3 forward (qlora_linear_fwd_fp8) against the oracle's
-E4M3 forward (oracle/fp8.py): same quantized operands, fp32 accumulation on
-the GPU vs fp64 -- the usual GEMM tolerance (relative Frobenius <= 5e-3,
-|err| <= 1e-2 (|ref| + rms(ref)) per element).  One-hot tokens pin the weight
+"""GPU parity of the E4M3 forward and backward (qlora_linear_fwd_fp8,
+qlora_linear_bwd_fp8) against the oracle's E4M3 forward and dX
+(oracle/fp8.py): same quantized operands, fp32 accumulation on the GPU vs
+fp64 -- the usual GEMM tolerance (relative Frobenius <= 5e-3, |err| <=
+1e-2 (|ref| + rms(ref)) per element).  One-hot tokens (forward) and one-hot
+gradient rows (dX, through the MN-major E4M3 operand) pin the weight
 conversion, the row codes and the epilogue factor bit for bit."""
 import numpy as np
 import pytest
@@ -106,3 +108,76 @@ def test_llama7b_q_proj_full_size_sampled(ql):
     qt = nf4.quantize(bits(W))
     Yr, _ = fp8.lora_forward_e4m3(bits(X)[rows], qt, bits(A), bits(B), case.scale)
     assert_close("Y e4m3 llama7b q_proj rows", f64(Y)[rows], Yr)
+
+
+# ------------------------------------------------------------------ backward (dX on E4M3)
+
+@pytest.mark.parametrize("N,K,M,r,dq,dqt,saved_xa", [
+    (528, 1088, 200, 16, 256, 0, True),    # one accumulator per CTA; ragged last reduction step (N % 128 = 16)
+    (1040, 576, 1100, 32, 256, 0, False),  # two accumulators, ragged M and output columns; XA recomputed
+    (272, 640, 17, 64, 256, 0, True),      # few tokens
+    (1024, 1024, 300, 128, 256, 1, True),  # rank 128; E4M3 second-level codes
+    (784, 1088, 513, 8, 0, 0, False),      # double quantization off
+])
+def test_backward_matches_the_e4m3_oracle(ql, N, K, M, r, dq, dqt, saved_xa):
+    W, X, A, B, s = make(N, K, M, r, seed=N + 2 * K + M + r)
+    from bit_nf4_quantized_38_b300.workloads import normal_bf16
+    dY = normal_bf16((M, N), 1.0, N + M)
+    dev = torch.device("cuda")
+    q = ql.nf4_quantize(W.to(dev), dq_blocksize=dq, dq_type=dqt)
+    Xd, Ad, Bd, dYd = X.to(dev), A.to(dev), B.to(dev), dY.to(dev)
+    XA = ql.qlora_linear_fwd(Xd, q, Ad, Bd, s)[1] if saved_xa else None
+    dX, dA, dB = ql.qlora_linear_bwd_fp8(dYd, Xd, XA, q, Ad, Bd, s)
+    torch.cuda.synchronize()
+    ql.device_status()
+    qt = nf4.quantize(bits(W), dq_blocksize=dq, dq_type=dqt)
+    dXr, _ = fp8.lora_backward_e4m3(bits(dY), qt, bits(A), bits(B), s)
+    dAr, dBr, _ = linear.lora_adapter_grads(bits(dY), bits(X), bits(A), bits(B), s)
+    tag = f"{N}x{K} M={M} r={r} dq={dq} dqt={dqt} xa={saved_xa}"
+    assert_close(f"dX e4m3 {tag}", f64(dX), dXr)
+    assert_close(f"dA e4m3 bwd {tag}", dA.double().cpu().numpy(), dAr)
+    assert_close(f"dB e4m3 bwd {tag}", dB.double().cpu().numpy(), dBr)
+    # and dX stays near the bf16 backward's (3 mantissa bits per operand)
+    dX16 = linear.lora_backward(bits(dY), bits(X), nf4.dequantize(qt), bits(A), bits(B), s)[0]
+    assert np.linalg.norm(f64(dX) - dX16) / np.linalg.norm(dX16) < 0.06
+
+
+def test_backward_one_hot_gradients_are_bit_exact(ql):
+    """dY row m one-hot (1.0) at n_m, B = 0 (so G = 0): the row exponent is 8
+    and the code 256, so dX[m, k] = bf16(Wq[n_m, k] 2^-E) exactly -- the
+    weight's E4M3 codes read back through the MN-major operand, bit for bit."""
+    from bit_nf4_quantized_38_b300.workloads import normal_with_outliers_bf16
+    N, K = 272, 576
+    W = normal_with_outliers_bf16((N, K), 0.02, 0.001, 20.0, seed=29)
+    qt = nf4.quantize(bits(W))
+    E, wq = fp8.weight_e4m3(qt)
+    dev = torch.device("cuda")
+    q = ql.nf4_quantize(W.to(dev))
+    X = torch.randn(N, K).to(torch.bfloat16).to(dev)
+    A = torch.randn(K, 16).to(torch.bfloat16).to(dev)
+    Bz = torch.zeros(16, N, dtype=torch.bfloat16, device=dev)
+    ns = np.arange(N)
+    dY = torch.zeros(N, N, dtype=torch.bfloat16)
+    dY[torch.arange(N), torch.from_numpy(ns)] = 1.0
+    dX, _, _ = ql.qlora_linear_bwd_fp8(dY.to(dev), X, None, q, A, Bz, 2.0)
+    torch.cuda.synchronize()
+    expect = f32_to_bf16_bits(np.ldexp(wq[ns], -E).astype(np.float32))
+    assert np.array_equal(bits(dX), expect)
+
+
+def test_backward_llama7b_q_proj_full_size_sampled(ql):
+    """LLaMA-7B q_proj (4096 x 4096) at 4096 tokens, r = 64: 64 sampled rows
+    of dX against the oracle."""
+    from bit_nf4_quantized_38_b300.workloads import case_inputs, case_weight, llama7b_linears
+    case = llama7b_linears().cases[0]
+    W = case_weight(case)
+    X, A, B, dY = case_inputs(case)
+    dev = torch.device("cuda")
+    q = ql.nf4_quantize(W.to(dev))
+    dX, _, _ = ql.qlora_linear_bwd_fp8(dY.to(dev), X.to(dev), None, q, A.to(dev), B.to(dev), case.scale)
+    torch.cuda.synchronize()
+    ql.device_status()
+    rows = np.sort(np.random.default_rng(8).choice(case.M, 64, replace=False))
+    qt = nf4.quantize(bits(W))
+    dXr, _ = fp8.lora_backward_e4m3(bits(dY)[rows], qt, bits(A), bits(B), case.scale)
+    assert_close("dX e4m3 llama7b q_proj rows", f64(dX)[rows], dXr)

@@ -111,3 +111,55 @@ def test_e4m3_forward_stays_near_the_bf16_forward():
     Y16, _ = linear.lora_forward(X, nf4.dequantize(qt), A, B, 1.0)
     rel = np.linalg.norm(Y8 - Y16) / np.linalg.norm(Y16)
     assert 1e-4 < rel < 0.06
+
+
+def test_backward_matches_a_plain_loop_on_a_tiny_case():
+    """dX of R24 restated element by element: the same E4M3 weight (E from
+    max |m_hat|), dY rows coded by the X-row rule, G from the bf16 dY."""
+    rng = np.random.default_rng(35)
+    M, K, N, r, s = 3, 64, 6, 2, 0.75
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    qt = nf4.quantize(_bits(W))
+    dY = _bits(rng.standard_normal((M, N)) * 3.0)
+    A, B = _bits(rng.standard_normal((K, r)) * 0.3), _bits(rng.standard_normal((r, N)) * 0.1)
+    dX, (E, Em, rs) = fp8.lora_backward_e4m3(dY, qt, A, B, s)
+    q = nf4.nf4_levels()
+    codes = nf4.unpack_nibbles(qt["packed"]).reshape(N, K)
+    mh = nf4.absmax_hat(qt).reshape(N, K // 64)
+    maxm = max(abs(float(v)) for v in mh.ravel())
+    E2 = 0
+    while maxm * 2.0 ** (E2 + 1) <= 448.0:
+        E2 += 1
+    while maxm * 2.0 ** E2 > 448.0:
+        E2 -= 1
+    assert E == E2
+    dyf, af, bf = bf16_bits_to_f32(dY), bf16_bits_to_f32(A), bf16_bits_to_f32(B)
+    for m in range(M):
+        amax = max(abs(float(v)) for v in dyf[m])
+        em = 0
+        while amax * 2.0 ** (em + 1) <= 448.0:
+            em += 1
+        while amax * 2.0 ** em > 448.0:
+            em -= 1
+        assert em == Em[m]
+        g = [sum(float(dyf[m, n]) * float(bf[j, n]) for n in range(N)) for j in range(r)]
+        for k in range(K):
+            acc = 0.0
+            for n in range(N):
+                wv = _e4m3_brute(float(np.float32(np.float32(q[codes[n, k]]) * np.float32(mh[n, k // 64]))) * 2.0 ** E)
+                acc += _e4m3_brute(float(dyf[m, n]) * 2.0 ** em) * wv
+            ref = 2.0 ** (-em - E) * acc + s * sum(g[j] * float(af[k, j]) for j in range(r))
+            assert abs(dX[m, k] - ref) <= 1e-12 * (abs(ref) + 1)
+
+
+def test_e4m3_backward_stays_near_the_bf16_backward():
+    rng = np.random.default_rng(36)
+    M, K, N, r = 64, 256, 192, 16
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    qt = nf4.quantize(_bits(W))
+    dY, X = _bits(rng.standard_normal((M, N))), _bits(rng.standard_normal((M, K)))
+    A, B = _bits(rng.standard_normal((K, r)) * 0.25), _bits(rng.standard_normal((r, N)) * 0.01)
+    dX8, _ = fp8.lora_backward_e4m3(dY, qt, A, B, 1.0)
+    dX16 = linear.lora_backward(dY, X, nf4.dequantize(qt), A, B, 1.0)[0]
+    rel = np.linalg.norm(dX8 - dX16) / np.linalg.norm(dX16)
+    assert 1e-4 < rel < 0.06
