@@ -6,7 +6,8 @@ filled with a fixed pattern; after quantize, dequantize, the forward (both
 the tensor-core and the decode path) and the backward on ragged shapes (N,
 M and K not multiples of the tiles, ranks 8 and 128), every guard byte must
 still hold the pattern.  The outputs themselves are checked by the parity
-tests; here only what lies around them is."""
+tests; here only what lies around them is.  The E4M3 forward and backward
+get the same check."""
 import numpy as np
 import pytest
 import torch
@@ -98,5 +99,40 @@ def test_no_write_outside_buffers(ql, N, K, M, r, dq):
     ql.device_status()
     g.check()
     # the outputs were written (not left at the pattern)
+    assert not bool((Y.view(torch.uint8) == PATTERN).all())
+    assert not bool((dX.view(torch.uint8) == PATTERN).all())
+
+
+@pytest.mark.parametrize("N,K,M,r", [
+    (336, 320, 200, 16),    # one accumulator, ragged output tiles and reduction steps
+    (1040, 576, 1100, 128), # two accumulators, partial pair tile, rank 128
+    (272, 640, 17, 8),      # few tokens
+])
+def test_e4m3_calls_write_no_byte_outside_their_buffers(ql, N, K, M, r):
+    """The E4M3 forward and backward: the operand kernel's codes and row
+    exponents in the workspace, the MN-major dX path and both epilogues."""
+    from bit_nf4_quantized_38_b300.workloads import normal_bf16, normal_with_outliers_bf16
+    dev = torch.device("cuda")
+    g = Guarded(dev)
+    W = normal_with_outliers_bf16((N, K), 0.02, 0.001, 20.0, N + K + 1).to(dev)
+    q = guarded_nf4(ql, g, N, K, 256)
+    wsq = g.view((ql.workspace_size(ql.OP_QUANTIZE, 0, N, K, 0),), torch.uint8)
+    ql.nf4_quantize(W, out=q, ws=wsq)
+    X = normal_bf16((M, K), 1.0, 5).to(dev)
+    A = normal_bf16((K, r), 0.25, 6).to(dev)
+    B = normal_bf16((r, N), 0.01, 7).to(dev)
+    dY = normal_bf16((M, N), 1.0, 8).to(dev)
+    Y = g.view((M, N), torch.bfloat16)
+    XA = g.view((M, r), torch.bfloat16)
+    wsf = g.view((ql.workspace_size(ql.OP_LINEAR_FWD_FP8, M, N, K, r),), torch.uint8)
+    ql.qlora_linear_fwd_fp8(X, q, A, B, 0.5, Y=Y, XA=XA, ws=wsf)
+    dX = g.view((M, K), torch.bfloat16)
+    dA = g.view((K, r), torch.float32)
+    dB = g.view((r, N), torch.float32)
+    wsb = g.view((ql.workspace_size(ql.OP_LINEAR_BWD_FP8, M, N, K, r),), torch.uint8)
+    for xa in (XA, None):
+        ql.qlora_linear_bwd_fp8(dY, X, xa, q, A, B, 0.5, dX=dX, dA=dA, dB=dB, ws=wsb)
+    ql.device_status()
+    g.check()
     assert not bool((Y.view(torch.uint8) == PATTERN).all())
     assert not bool((dX.view(torch.uint8) == PATTERN).all())
