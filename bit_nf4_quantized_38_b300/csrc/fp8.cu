@@ -1,9 +1,10 @@
 // Operand preparation for the E4M3 forward (the FP8 variant of the training
 // GEMM; E4M3 = 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, largest
 // finite 448), one launch, two kinds of CTA:
-//   CTAs [0, gw)      the largest |m_hat| over the weight's blocks (atomic max
-//                     into a word the caller cleared), from which the GEMM
-//                     takes the weight's exponent E
+//   CTAs [0, gw)      the largest |m_hat| over a share of the weight's blocks,
+//                     one partial per CTA (wpart[c]; no atomics, nothing to
+//                     clear): the consumers take the maximum of the gw
+//                     partials and from it the weight's exponent E
 //   CTAs [gw, grid)   rows of X in turn (a persistent grid): E_m = the largest
 //                     exponent with amax_m * 2^E_m <= 448 (0 for an all-zero
 //                     row), and the codes e4m3(x * 2^E_m) (exact scaling, then
@@ -11,6 +12,10 @@
 // A row CTA holds its row in registers and has the next row's loads in
 // flight while it codes the current one (two register sets taking rows in
 // turn), so every row costs one read of X and no exposed memory latency.
+// Launched as a programmatic dependent of the previous kernel: with `free`
+// it reads and writes nothing that kernel touches (the caller checks), so it
+// runs alongside it and only its last CTA waits for it before exiting
+// (completion still implies the predecessor's); otherwise it waits first.
 #include <algorithm>
 
 #include "common.cuh"
@@ -20,7 +25,6 @@
 namespace ql {
 namespace {
 
-constexpr int kWmaxCtas = 148;
 
 __device__ __forceinline__ float absmax8(const uint4 v) {
   const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
@@ -63,8 +67,14 @@ __device__ __forceinline__ float row_scale(float a, float *red, int64_t row, int
 template <int R>
 __global__ void __launch_bounds__(R == 4 ? 128 : 256, R == 4 ? 8 : 3) k_prep_e4m3(const uint4 *__restrict__ X, int64_t M, int64_t K,
                                                                   uint2 *__restrict__ codes, int *__restrict__ row_exp,
-                                                                  NF4View w, float *__restrict__ wmax, int gw) {
+                                                                  NF4View w, float *__restrict__ wpart, int gw,
+                                                                  int free_) {
   __shared__ float red[2][8];
+  if (!free_) ptx::griddep_wait();
+  ptx::griddep_launch();  // the dependents wait for this grid before reading its output
+  // the CTA that waits for the predecessor at exit (free_); the grid's last
+  // CTA is a row CTA
+  const bool waiter = free_ && blockIdx.x == gridDim.x - 1 && threadIdx.x == 0;
   if ((int)blockIdx.x < gw) {
     // ------------------------------------------------ weight: max |m_hat|
     // 16 consecutive blocks per thread and load (one 16-byte load of codes,
@@ -115,7 +125,7 @@ __global__ void __launch_bounds__(R == 4 ? 128 : 256, R == 4 ? 8 : 3) k_prep_e4m
     __syncthreads();
     if (threadIdx.x == 0) {
       for (int i = 1; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[0][i]);
-      atomicMax(reinterpret_cast<int *>(wmax), __float_as_int(m));  // non-negative: bit order = value order
+      wpart[blockIdx.x] = m;
     }
     return;
   }
@@ -152,17 +162,18 @@ __global__ void __launch_bounds__(R == 4 ? 128 : 256, R == 4 ? 8 : 3) k_prep_e4m
       load(row + 2 * gr, va);
       code(row + gr, vb, red[1]);
     }
-    return;
-  }
-  int par = 0;
+  } else {
+    int par = 0;
 #pragma unroll 1
-  for (; row < M; row += gr, par ^= 1) {  // long rows: amax pass, then the row again (mostly from L2)
-    const uint4 *x = X + row * n8;
-    float a = 0.0f;
-    for (int64_t i = threadIdx.x; i < n8; i += nt) a = fmaxf(a, absmax8(__ldg(x + i)));
-    const float sc = row_scale(a, red[par], row, row_exp);
-    for (int64_t i = threadIdx.x; i < n8; i += nt) codes[row * n8 + i] = codes8(__ldg(x + i), sc);
+    for (; row < M; row += gr, par ^= 1) {  // long rows: amax pass, then the row again (mostly from L2)
+      const uint4 *x = X + row * n8;
+      float a = 0.0f;
+      for (int64_t i = threadIdx.x; i < n8; i += nt) a = fmaxf(a, absmax8(__ldg(x + i)));
+      const float sc = row_scale(a, red[par], row, row_exp);
+      for (int64_t i = threadIdx.x; i < n8; i += nt) codes[row * n8 + i] = codes8(__ldg(x + i), sc);
+    }
   }
+  if (waiter) ptx::griddep_wait();  // this grid completes after its predecessor
 }
 
 template <int R>
@@ -195,25 +206,31 @@ int sm_count() {
 }  // namespace
 
 cudaError_t launch_prep_e4m3(const uint16_t *X, int64_t M, int64_t K, const NF4View &w, uint8_t *codes, int *row_exp,
-                             float *wmax, cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(wmax, 0, sizeof(float), st);
-  if (e != cudaSuccess) return e;
+                             float *wpart, int *n_wpart, bool free_, cudaStream_t st) {
   const int64_t n_b = w.rows * w.cols / 64;
   const bool small = K <= 4 * 128 * 8;  // rows of up to 4096 elements: 128 threads x 4 pieces
   const int nt = small ? 128 : 256;
   const int64_t per_cta = (int64_t)nt * 16 * 2;  // blocks a weight CTA takes per round
-  const int gw = (int)std::max<int64_t>(1, std::min<int64_t>((n_b + per_cta - 1) / per_cta, kWmaxCtas));
+  const int gw = (int)std::max<int64_t>(1, std::min<int64_t>((n_b + per_cta - 1) / per_cta, kWmaxParts));
+  *n_wpart = gw;
   const int64_t per_sm = small ? row_ctas_per_sm<4>() : row_ctas_per_sm<6>();
   const int64_t gr = std::max<int64_t>(1, std::min<int64_t>(M, per_sm * sm_count()));
-  const dim3 grid((unsigned)(gw + gr));
-  if (small)
-    k_prep_e4m3<4><<<grid, nt, 0, st>>>(reinterpret_cast<const uint4 *>(X), M, K, reinterpret_cast<uint2 *>(codes),
-                                        row_exp, w, wmax, gw);
-  else
-    k_prep_e4m3<6><<<grid, nt, 0, st>>>(reinterpret_cast<const uint4 *>(X), M, K, reinterpret_cast<uint2 *>(codes),
-                                        row_exp, w, wmax, gw);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(gw + gr));
+  cfg.blockDim = dim3((unsigned)nt);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const uint4 *x4 = reinterpret_cast<const uint4 *>(X);
+  uint2 *c2 = reinterpret_cast<uint2 *>(codes);
+  const int fr = free_ ? 1 : 0;
+  cudaError_t e = small ? cudaLaunchKernelEx(&cfg, k_prep_e4m3<4>, x4, M, K, c2, row_exp, w, wpart, gw, fr)
+                        : cudaLaunchKernelEx(&cfg, k_prep_e4m3<6>, x4, M, K, c2, row_exp, w, wpart, gw, fr);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace ql

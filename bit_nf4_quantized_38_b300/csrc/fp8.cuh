@@ -6,10 +6,23 @@
 namespace ql {
 
 // codes [M][K] = e4m3(x * 2^E_m) per X row with row_exp[M] = E_m, and
-// *wmax = max |m_hat| of the weight (cleared here first).  K % 8 == 0; X 16-
-// and codes 8-byte aligned.
+// partial maxima of |m_hat| over the weight's blocks in wpart[0, *n_wpart)
+// (at most kWmaxParts; max |m_hat| = the largest of them: wmax_of_warp).  K % 8
+// == 0; X 16- and codes 8-byte aligned.  free_: X and the weight are not
+// written, and codes, row_exp and wpart not read or written, by any kernel
+// that may still be running (the kernel then runs alongside its predecessor).
+constexpr int kWmaxParts = 148;
 cudaError_t launch_prep_e4m3(const uint16_t *X, int64_t M, int64_t K, const NF4View &w, uint8_t *codes, int *row_exp,
-                             float *wmax, cudaStream_t st);
+                             float *wpart, int *n_wpart, bool free_, cudaStream_t st);
+
+// max |m_hat| from the partial maxima, by one warp (every lane gets it).
+__device__ __forceinline__ float wmax_of_warp(const float *wpart, int n) {
+  float m = 0.0f;
+  for (int i = (int)(threadIdx.x & 31); i < n; i += 32) m = fmaxf(m, __ldg(wpart + i));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  return m;
+}
 
 // 2^(-E_m - E): the factor of output row m (E from the weight's max |m_hat|).
 __device__ __forceinline__ float e4m3_row_factor(int row_exp, float wmax) {

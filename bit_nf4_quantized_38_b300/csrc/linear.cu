@@ -274,17 +274,26 @@ int linear_fwd(const LinearArgs &a) {
   return launch_nf4_gemm(g, st);
 }
 
-// E4M3 forward workspace: [max |m_hat| | pad][row exponents M int32][X codes
+// E4M3 forward workspace: two halves (calls on a stream alternate), each
+// [partial maxima of |m_hat| | pad to 1 KB][row exponents M int32][X codes
 // M x K bytes][XAs M x r bf16]
+size_t fp8_fwd_half(int64_t M, int64_t K, int32_t r) {
+  return 1024 + up256((size_t)M * 4) + up256((size_t)M * K) + up256((size_t)M * r * 2);
+}
 size_t linear_fwd_fp8_ws(int64_t M, int64_t N, int64_t K, int32_t r) {
   if (M <= 0 || N <= 0 || K <= 0 || !rank_ok(r)) return 0;
-  return 256 + up256((size_t)M * 4) + up256((size_t)M * K) + up256((size_t)M * r * 2);
+  return 2 * fp8_fwd_half(M, K, r);
 }
 
 // Forward with E4M3 main steps (3 launches, in stream order):
-//   1. X codes e4m3(x 2^E_m) with the row exponents, and max |m_hat|  (k_prep_e4m3)
-//   2. XA = X A -> XA_out, and XAs = bf16(fl32(s XA) 2^(E_m + E))    LoRA kernel
-//   3. Y = 2^(-E_m - E) (X_e4m3 . W_e4m3^T + XAs B)                  CTA-pair GEMM
+//   1. X codes e4m3(x 2^E_m) with the row exponents, and max |m_hat| partials  (k_prep_e4m3)
+//   2. XA = X A -> XA_out, and XAs = bf16(fl32(s XA) 2^(E_m + E))              LoRA kernel
+//   3. Y = 2^(-E_m - E) (X_e4m3 . W_e4m3^T + XAs B)                            CTA-pair GEMM
+// When X and the weight are not written by the previous call on the stream,
+// and this call's workspace half is not touched by it, the operand kernel and
+// the LoRA kernel's main loop run alongside that call's GEMM (its last wave
+// leaves SMs idle); the LoRA kernel stores once the operand kernel (and so
+// the previous call) has completed, and the GEMM follows it.
 int linear_fwd_fp8(const LinearArgs &a) {
   const char *fn = "qlora_linear_fwd_fp8";
   if (!a.X || !a.A || !a.B || !a.Y) return set_error(QL_ERR_INVALID, "%s: null X, A, B or Y", fn);
@@ -294,21 +303,39 @@ int linear_fwd_fp8(const LinearArgs &a) {
   const int r = a.r;
   QL_TRY(check_common(a, fn, linear_fwd_fp8_ws(M, N, K, r)));
   cudaStream_t st = a.stream;
-  note_other_call(st);  // the next call waits for this one in full
-  char *ws = static_cast<char *>(a.ws);
-  float *wmax = reinterpret_cast<float *>(ws);
-  int *rows = reinterpret_cast<int *>(ws + 256);
-  uint8_t *xq = reinterpret_cast<uint8_t *>(ws + 256 + up256((size_t)M * 4));
-  uint16_t *xas = reinterpret_cast<uint16_t *>(ws + 256 + up256((size_t)M * 4) + up256((size_t)M * K));
+  const size_t half = fp8_fwd_half(M, K, r);
+  char *ws = static_cast<char *>(a.ws) + (next_ws_half(st) ? half : 0);
+  float *wpart = reinterpret_cast<float *>(ws);
+  int *rows = reinterpret_cast<int *>(ws + 1024);
+  uint8_t *xq = reinterpret_cast<uint8_t *>(ws + 1024 + up256((size_t)M * 4));
+  uint16_t *xas = reinterpret_cast<uint16_t *>(ws + 1024 + up256((size_t)M * 4) + up256((size_t)M * K));
   const NF4View w = nf4_view(a.W);
-  QL_TRY(check_cuda(launch_prep_e4m3(a.X, M, K, w, xq, rows, wmax, st), "qlora_linear_fwd_fp8: operand codes"));
+
+  std::vector<Range> prep_reads = {range(a.X, (size_t)(M * K * 2))};
+  weight_ranges(a.W, prep_reads);
+  const bool prep_free = reads_clear_of_previous(st, prep_reads) && writes_clear_of_previous(st, {range(ws, half)});
+  const bool lora_early = reads_clear_of_previous(st, {range(a.X, (size_t)(M * K * 2)), range(a.A, (size_t)(K * r * 2))});
+  std::vector<Range> reads = prep_reads;
+  reads.push_back(range(a.A, (size_t)(K * r * 2)));
+  reads.push_back(range(a.B, (size_t)(r * N * 2)));
+  std::vector<Range> writes = {range(ws, half), range(a.Y, (size_t)(M * N * 2))};
+  if (a.XA) writes.push_back(range(a.XA, (size_t)(M * r * 2)));
+  note_call(st, true, std::move(writes), reads);
+
+  int nwpart = 0;
+  QL_TRY(check_cuda(launch_prep_e4m3(a.X, M, K, w, xq, rows, wpart, &nwpart, prep_free, st),
+                    "qlora_linear_fwd_fp8: operand codes"));
   LoraProblem L{};
   L.A = a.X; L.a_mn = false; L.B = a.A; L.b_mn = true;  // X [M][K], A [K][r]
   L.P = M; L.Q = r; L.T = K; L.mode = 0; L.scale = a.scale;
   L.out = xas; L.ldo = r; L.out2 = a.XA; L.ldo2 = r;
   L.row_exp = rows;
-  L.wmax = wmax;
-  L.dep = kDepStart;
+  L.wmax = wpart;
+  L.nwpart = nwpart;
+  // reads X and A alongside the operand kernel (and the previous call's
+  // GEMM, when the operand kernel runs free); stores, and reads the scales,
+  // after the operand kernel completes
+  L.dep = (prep_free && lora_early) ? kDepStores : kDepStart;
   QL_TRY(launch_lora(L, st));
   GemmProblem g{};
   g.trans = false;
@@ -318,21 +345,22 @@ int linear_fwd_fp8(const LinearArgs &a) {
   g.out = a.Y; g.Nout = N;
   g.fp8 = true;
   g.row_exp = rows;
-  g.wmax = wmax;
-  // The main loop reads the X codes, the weight and max |m_hat|: written by
-  // the operand kernel, which completed before the LoRA kernel (a dependent
-  // that waits for it at its start) let this GEMM launch; the LoRA kernel
-  // itself writes only XAs, read after the wait.
+  g.wmax = wpart;
+  g.nwpart = nwpart;
+  // The main loop reads the X codes, the weight and the |m_hat| partials:
+  // written by the operand kernel, which completed before the LoRA kernel
+  // (a dependent that waits for it before letting this GEMM start) did; the
+  // LoRA kernel itself writes only XAs, read after the wait.
   g.early_main = true;
   return launch_nf4_gemm(g, st);
 }
 
-// E4M3 backward workspace: [max |m_hat| | pad][row exponents of dY, M int32]
+// E4M3 backward workspace: [partial maxima of |m_hat| | pad to 1 KB][row exponents of dY, M int32]
 // [dY codes M x N bytes][Gs' M x r bf16][G M x r bf16][XA M x r bf16 (recomputed
 // when the caller passes none)]
 size_t linear_bwd_fp8_ws(int64_t M, int64_t N, int64_t K, int32_t r) {
   if (M <= 0 || N <= 0 || K <= 0 || !rank_ok(r)) return 0;
-  return 256 + up256((size_t)M * 4) + up256((size_t)M * N) + 3 * up256((size_t)M * r * 2);
+  return 1024 + up256((size_t)M * 4) + up256((size_t)M * N) + 3 * up256((size_t)M * r * 2);
 }
 
 // Backward with E4M3 main steps in dX (5 or 6 launches, in stream order):
@@ -356,14 +384,16 @@ int linear_bwd_fp8(const LinearArgs &a) {
   cudaStream_t st = a.stream;
   note_other_call(st);  // the next call waits for this one in full
   char *ws = static_cast<char *>(a.ws);
-  float *wmax = reinterpret_cast<float *>(ws);
-  int *rows = reinterpret_cast<int *>(ws + 256);
-  uint8_t *dyq = reinterpret_cast<uint8_t *>(ws + 256 + up256((size_t)M * 4));
-  uint16_t *gs8 = reinterpret_cast<uint16_t *>(ws + 256 + up256((size_t)M * 4) + up256((size_t)M * N));
+  float *wpart = reinterpret_cast<float *>(ws);
+  int *rows = reinterpret_cast<int *>(ws + 1024);
+  uint8_t *dyq = reinterpret_cast<uint8_t *>(ws + 1024 + up256((size_t)M * 4));
+  uint16_t *gs8 = reinterpret_cast<uint16_t *>(ws + 1024 + up256((size_t)M * 4) + up256((size_t)M * N));
   uint16_t *g16 = reinterpret_cast<uint16_t *>(reinterpret_cast<char *>(gs8) + up256((size_t)M * r * 2));
   uint16_t *xa_tmp = reinterpret_cast<uint16_t *>(reinterpret_cast<char *>(g16) + up256((size_t)M * r * 2));
   const NF4View w = nf4_view(a.W);
-  QL_TRY(check_cuda(launch_prep_e4m3(a.dY, M, N, w, dyq, rows, wmax, st), "qlora_linear_bwd_fp8: operand codes"));
+  int nwpart = 0;
+  QL_TRY(check_cuda(launch_prep_e4m3(a.dY, M, N, w, dyq, rows, wpart, &nwpart, false, st),
+                    "qlora_linear_bwd_fp8: operand codes"));
   const uint16_t *xa = a.XA_in;
   if (!xa) {  // XA = X A (fp32 accumulation, bf16)
     LoraProblem L{};
@@ -379,7 +409,8 @@ int linear_bwd_fp8(const LinearArgs &a) {
     L.P = M; L.Q = r; L.T = N; L.mode = 0; L.scale = a.scale; L.out = gs8; L.ldo = r;
     L.out2 = g16; L.ldo2 = r;
     L.row_exp = rows;
-    L.wmax = wmax;
+    L.wmax = wpart;
+    L.nwpart = nwpart;
     L.dep = kDepStart;
     QL_TRY(launch_lora(L, st));
   }
@@ -392,7 +423,8 @@ int linear_bwd_fp8(const LinearArgs &a) {
     g.out = a.dX; g.Nout = K;
     g.fp8 = true;
     g.row_exp = rows;
-    g.wmax = wmax;
+    g.wmax = wpart;
+    g.nwpart = nwpart;
     // the main loop reads the dY codes, the weight and max |m_hat|, written
     // by the operand kernel, which completed before the G kernel (a
     // dependent that waits for it at its start) let this GEMM launch

@@ -20,6 +20,7 @@
 #include "common.cuh"
 #include "ptx.cuh"
 #include "tc_gemm.cuh"
+#include "fp8.cuh"
 
 namespace ql {
 namespace {
@@ -35,7 +36,8 @@ struct LoraTcArgs {
   uint16_t *out2;
   int64_t ldo2;
   const int *row_exp;  // mode 0: out[p][q] = bf16(fl32(scale v) 2^(row_exp[p] + E)) when set
-  const float *wmax;   // E = e4m3_weight_exponent(*wmax)
+  const float *wmax;   // E = e4m3_weight_exponent(the largest of wmax[0, nwpart))
+  int nwpart;
   int dep;  // kDepStart, kDepStores or kDepExit (see LoraProblem)
   int *status;
 };
@@ -183,6 +185,16 @@ k_lora_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
     ptx::griddep_wait();
     ptx::griddep_launch();
   }
+  // E4M3 scaling: E from the operand kernel's partial maxima (complete: this
+  // grid has waited for its predecessor by now, in every mode that scales)
+  __shared__ int e_w;
+  if (a.row_exp) {
+    if (warp == 0) {
+      const float m = wmax_of_warp(a.wmax, a.nwpart);
+      if (lane == 0) e_w = e4m3_weight_exponent(m);
+    }
+    __syncthreads();
+  }
 
   // ---------------------------------------------------------------- cluster reduction
   // CTA c finishes rows [c*128/S, (c+1)*128/S) of the tile, adding the S
@@ -219,8 +231,7 @@ k_lora_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
       if (q >= a.Q) break;
       float sv = __fmul_rn(vals[e], a.scale);
       if (a.mode == 0) {
-        if (a.row_exp) sv = __fmul_rn(sv, __uint_as_float((uint32_t)(__ldg(a.row_exp + p) +
-                                                             e4m3_weight_exponent(__ldg(a.wmax)) + 127) << 23));
+        if (a.row_exp) sv = __fmul_rn(sv, __uint_as_float((uint32_t)(__ldg(a.row_exp + p) + e_w + 127) << 23));
         static_cast<uint16_t *>(a.out)[p * a.ldo + q] = (uint16_t)(pack_bf16x2(sv, 0.f) & 0xFFFFu);
         if (a.out2) a.out2[p * a.ldo2 + q] = (uint16_t)(pack_bf16x2(vals[e], 0.f) & 0xFFFFu);
       } else if (a.mode == 1) {
@@ -254,6 +265,7 @@ int prepare(const LoraProblem &L, CUtensorMap *tA, CUtensorMap *tB, LoraTcArgs *
   a->out = L.out; a->ldo = L.ldo; a->out2 = L.out2; a->ldo2 = L.ldo2;
   a->row_exp = L.row_exp;
   a->wmax = L.wmax;
+  a->nwpart = L.nwpart;
   a->dep = L.dep;
   a->status = device_status_ptr();
   return QL_OK;

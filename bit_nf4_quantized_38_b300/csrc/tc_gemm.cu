@@ -59,10 +59,12 @@ struct GemmArgs {
   int early_main;
   float *part;  // single-CTA kernel split over K (gridDim.z > 1): fp32 partials [splits][M][ldo]
   // E4M3 main steps (CTA-pair kernel, kFp8): per X row its exponent E_m; the
-  // largest |m_hat| of the weight, from which the converters take the
-  // weight's exponent E; the epilogue multiplies row m by 2^(-E_m - E)
+  // partial maxima of |m_hat| (the weight's maximum is the largest of the
+  // nwpart), from which the converters take the weight's exponent E; the
+  // epilogue multiplies row m by 2^(-E_m - E)
   const int *row_exp;
   const float *wmax;
+  int nwpart;
   float q[16];
 };
 
@@ -402,6 +404,7 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * PSTAGES + 2);
   volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *dep_seen = reinterpret_cast<volatile int *>(tmem_slot + 2);  // gate CTA: predecessor done
+  float *wmax_s = reinterpret_cast<float *>(tmem_slot + 3);                  // E4M3: max |m_hat|
   auto full = [&](int s) { return ptx::smem_u32(&bars[s]); };
   auto empty = [&](int s) { return ptx::smem_u32(&bars[PSTAGES + s]); };
   const uint32_t accf = ptx::smem_u32(&bars[2 * PSTAGES]);
@@ -432,6 +435,15 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   if (warp == 1) {
     ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), G::TMEM_COLS);
     ptx::tmem_relinquish_pair();
+  }
+  if constexpr (kFp8) {
+    // max |m_hat| from the operand kernel's partials: that kernel completed
+    // before this grid could launch (its dependent, the LoRA kernel, waits
+    // for it before letting this GEMM start), so they may be read here
+    if (warp == 2) {
+      const float m = wmax_of_warp(p.wmax, p.nwpart);
+      if (lane == 0) *wmax_s = m;
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -588,7 +600,7 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
     // E4M3: the weight's power-of-two scale 2^E (the largest with
     // max |m_hat| 2^E <= 448), applied exactly to every block constant
-    const float s2e = kFp8 ? e4m3_weight_scale(__ldg(p.wmax)) : 1.0f;
+    const float s2e = kFp8 ? e4m3_weight_scale(*wmax_s) : 1.0f;
     constexpr int RB = kFp8 ? 2 : 1;  // row-blocks per thread per step (K = 128 per E4M3 step)
     const float mean = p.w.dq ? __ldg(p.w.mean) : 0.0f;
     auto fetch = [&](int ks, RowBlockSrc (&r)[RB]) {
@@ -658,7 +670,7 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       const int c_begin = NACC == 2 ? 0 : grp * 4, c_end = NACC == 2 ? 8 : grp * 4 + 4;
       const int row = mrow0 + acc * 256 + (int)crank * BMH + qd * 32 + lane;
       uint16_t *orow = p.out + (int64_t)row * p.ldo;
-      const float rs = kFp8 && row < p.M ? e4m3_row_factor(__ldg(p.row_exp + row), __ldg(p.wmax)) : 1.0f;
+      const float rs = kFp8 && row < p.M ? e4m3_row_factor(__ldg(p.row_exp + row), *wmax_s) : 1.0f;
 #pragma unroll 1
       for (int c = c_begin; c < c_end; ++c) {
         uint32_t r[32];
@@ -789,6 +801,7 @@ int launch_pair(const GemmProblem &g, unsigned long long *span, cudaStream_t st)
   a.early_main = g.early_main ? 1 : 0;
   a.row_exp = g.row_exp;
   a.wmax = g.wmax;
+  a.nwpart = g.nwpart;
   const Codebook &cb = codebook(g.w.qt);
   for (int i = 0; i < 16; ++i) a.q[i] = cb.q[i];
   dim3 grid((unsigned)(2 * ((g.Nout + 255) / 256)), (unsigned)((g.M + NACC * 256 - 1) / (NACC * 256)));
@@ -894,7 +907,7 @@ int launch_nf4_gemm(const GemmProblem &g, cudaStream_t st) {
   unsigned long long *span = (sp.on && sp.used < sp.capacity) ? sp.buf + 2 * sp.used : nullptr;
   int rc;
   if (g.fp8) {
-    if (!g.row_exp || !g.wmax) return set_error(QL_ERR_INVALID, "E4M3 GEMM: scales missing");
+    if (!g.row_exp || !g.wmax || g.nwpart < 1) return set_error(QL_ERR_INVALID, "E4M3 GEMM: scales missing");
     if (g.trans)
       rc = g.M <= 256 ? launch_pair<true, 1, true>(g, span, st) : launch_pair<true, 2, true>(g, span, st);
     else

@@ -53,11 +53,12 @@ struct GemmProblem {
   // E4M3 main steps (forward form; CTA-pair kernel): A holds the E4M3 codes
   // of X [M][Kred] bytes (row m scaled by 2^row_exp[m]), A2 the LoRA operand
   // already multiplied by 2^(row_exp[m] + E), and the output row m is
-  // multiplied by 2^(-row_exp[m] - E); wmax points at the largest |m_hat| of
-  // the weight, E = e4m3_weight_exponent(*wmax).
+  // multiplied by 2^(-row_exp[m] - E); wmax points at nwpart partial maxima
+  // of |m_hat| whose largest is the weight's, E = e4m3_weight_exponent(it).
   bool fp8 = false;
   const int *row_exp = nullptr;
   const float *wmax = nullptr;
+  int nwpart = 0;
 };
 int launch_nf4_gemm(const GemmProblem &g, cudaStream_t st);
 // Splits over the reduction of a GEMM with M <= 128 tokens (1 otherwise): as
@@ -104,9 +105,11 @@ struct LoraProblem {
   uint16_t *out2;
   int64_t ldo2;
   // mode 0 only: multiply row p of `out` by 2^(row_exp[p] + E), E =
-  // e4m3_weight_exponent(*wmax) (after the scale; exact)
+  // e4m3_weight_exponent of the largest of the nwpart partial maxima at wmax
+  // (after the scale; exact)
   const int *row_exp = nullptr;
   const float *wmax = nullptr;
+  int nwpart = 0;
   // Ordering against the previous kernel in the stream (programmatic
   // dependent launch):
   //   kDepStart  wait for it before reading anything (the default);

@@ -181,3 +181,44 @@ def test_backward_llama7b_q_proj_full_size_sampled(ql):
     qt = nf4.quantize(bits(W))
     dXr, _ = fp8.lora_backward_e4m3(bits(dY)[rows], qt, bits(A), bits(B), case.scale)
     assert_close("dX e4m3 llama7b q_proj rows", f64(dX)[rows], dXr)
+
+
+def test_back_to_back_calls_equal_synchronised_calls(ql):
+    """E4M3 forwards issued back to back on one stream with one workspace
+    (the operand and LoRA kernels of a call may run alongside the previous
+    call's GEMM) give bit-identical results to calls separated by a
+    synchronisation; so does a chain where a call's X is the previous call's
+    Y (which must wait for it), and a bf16 forward in between."""
+    dev = torch.device("cuda")
+    shapes = [(1024, 1024, 512, 32), (1024, 1024, 512, 32), (2048, 1024, 512, 16)]
+    cases = [make(N, K, M, r, seed=60 + i) for i, (N, K, M, r) in enumerate(shapes)]
+    qs = [ql.nf4_quantize(W.to(dev)) for W, *_ in cases]
+    ins = [(X.to(dev), A.to(dev), B.to(dev), s) for _, X, A, B, s in cases]
+    ws = torch.empty(max(ql.workspace_size(op, 512, 2048, 1024, 32) for op in (ql.OP_LINEAR_FWD_FP8, ql.OP_LINEAR_FWD)),
+                     dtype=torch.uint8, device=dev)
+    ref = []
+    for q, (X, A, B, s) in zip(qs, ins):
+        Y, XA = ql.qlora_linear_fwd_fp8(X, q, A, B, s, ws=ws)
+        torch.cuda.synchronize()
+        ref.append((Y.clone(), XA.clone()))
+    outs = [(torch.empty_like(y), torch.empty_like(xa)) for y, xa in ref]
+    for _ in range(3):
+        for q, (X, A, B, s), (Y, XA) in zip(qs, ins, outs):
+            ql.qlora_linear_fwd_fp8(X, q, A, B, s, Y=Y, XA=XA, ws=ws)
+        # a bf16 forward on the same workspace between the E4M3 calls
+        ql.qlora_linear_fwd(ins[0][0], qs[0], ins[0][1], ins[0][2], ins[0][3], ws=ws)
+    torch.cuda.synchronize()
+    ql.device_status()
+    for (a, xa), (b, xb) in zip(ref, outs):
+        assert torch.equal(a, b) and torch.equal(xa, xb)
+    # chain: layer 2's input is layer 1's output (1024 -> 1024 -> 2048)
+    X0, A0, B0, s0 = ins[0]
+    A1, B1, s1 = ins[1][1], ins[1][2], ins[1][3]
+    Y1s, _ = ql.qlora_linear_fwd_fp8(X0, qs[0], A0, B0, s0, ws=ws)
+    torch.cuda.synchronize()
+    Y2s, _ = ql.qlora_linear_fwd_fp8(Y1s, qs[1], A1, B1, s1, ws=ws)
+    torch.cuda.synchronize()
+    Y1, _ = ql.qlora_linear_fwd_fp8(X0, qs[0], A0, B0, s0, ws=ws)
+    Y2, _ = ql.qlora_linear_fwd_fp8(Y1, qs[1], A1, B1, s1, ws=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(Y2, Y2s)
