@@ -70,6 +70,12 @@ int check_common(const LinearArgs &a, const char *fn, size_t need) {
   } while (0)
 
 constexpr int64_t kDecodeMaxM = 16;  // M at or below this takes the decode path
+// 17 to kSliceMaxM tokens run as slices of kDecodeMaxM tokens through the
+// decode path (one weight stream per slice): measured faster than the
+// few-token tensor-core kernel there (LLaMA-13B shapes, M = 32: 24.7 / 36.2 /
+// 44.6 us for two slices against 28.3 / 56.3 / 59.1 us); above it the
+// few-token kernel is faster
+constexpr int64_t kSliceMaxM = 32;
 
 // ---------------------------------------------------------------------------
 // What the previous library call on a stream may still be reading or writing.
@@ -194,7 +200,7 @@ void note_other_call(cudaStream_t st) { note_call(st, false, {}); }
 
 size_t linear_fwd_ws(int64_t M, int64_t N, int64_t K, int32_t r) {
   if (M <= 0 || N <= 0 || K <= 0 || !rank_ok(r)) return 0;
-  if (M <= kDecodeMaxM) return decode_ws(N, K, r);
+  if (M <= kSliceMaxM) return decode_ws(N, K, r);
   return fwd_ws(M, N, K, r);
 }
 
@@ -210,6 +216,18 @@ int linear_fwd(const LinearArgs &a) {
     return set_error(QL_ERR_MISALIGNED, "%s: operand not 16-byte aligned", fn);
   const int64_t M = a.M, N = a.W.rows, K = a.W.cols;
   const int r = a.r;
+  if (M > kDecodeMaxM && M <= kSliceMaxM) {  // token slices through the decode path
+    QL_TRY(check_common(a, fn, decode_ws(N, K, r)));
+    for (int64_t m0 = 0; m0 < M; m0 += kDecodeMaxM) {
+      LinearArgs sl = a;
+      sl.M = std::min(kDecodeMaxM, M - m0);
+      sl.X = a.X + m0 * K;
+      sl.Y = a.Y + m0 * N;
+      sl.XA = a.XA ? a.XA + m0 * r : nullptr;
+      QL_TRY(linear_fwd(sl));
+    }
+    return QL_OK;
+  }
   if (M >= 1 && M <= kDecodeMaxM) {
     QL_TRY(check_common(a, fn, decode_ws(N, K, r)));
     DecodeProblem d{};

@@ -70,7 +70,8 @@ SHAPES = [
     (328, 320, 600, 16),    # CTA-pair tiles, ragged
     (1032, 576, 1100, 32),  # CTA-pair tiles, partial pair in N and M
     (520, 448, 300, 8),     # rank 8 on the tensor-core forward path
-    (264, 640, 17, 64),     # one token past the decode path's limit
+    (264, 640, 17, 64),     # 17 tokens: decode slices of 16 and 1 (forward)
+    (264, 640, 33, 64),     # one token past the slice limit: the few-token kernel
 ]
 
 

@@ -1,6 +1,6 @@
-"""GPU parity of the few-token forward (16 < M <= 128 tokens: the transposed
-tensor-core product split over all SMs, csrc/skinny.cu) against the fp64
-oracle.
+"""GPU parity of the few-token forward (32 < M <= 128 tokens: the transposed
+tensor-core product split over all SMs, csrc/skinny.cu; and 17-32 tokens, run
+as 16-token slices through the decode path) against the fp64 oracle.
 
 Same tolerance as the other GEMM results (relative Frobenius <= 5e-3,
 |err| <= 1e-2 (|ref| + rms(ref)) per element, fp32 accumulation on the same
@@ -47,11 +47,13 @@ SHAPES = [
     (1032, 576, 33, 128, 256, 0),   # ragged N tile, two LoRA steps, Mp = 64
     (5120, 1024, 128, 64, 256, 0),  # full 128-token tile
     (328, 320, 100, 16, 256, 0),    # ragged N, Mp = 128 with 28 padding tokens
-    (4096, 4096, 32, 64, 256, 0),   # LLaMA-7B attention shape, 32 tokens
+    (4096, 4096, 40, 64, 256, 0),   # LLaMA-7B attention shape, 40 tokens
     (256, 64, 128, 8, 256, 0),      # one main K-step per tile
     (776, 1088, 64, 32, 0, 0),      # double quantization off
     (520, 1088, 48, 16, 256, 1),    # FP4 code table, Mp = 64
-    (136, 4160, 17, 64, 256, 0),    # two tiles, long reduction: many CTAs share each tile
+    (136, 4160, 34, 64, 256, 0),    # two tiles, long reduction: many CTAs share each tile
+    (1032, 576, 17, 128, 256, 0),   # 17 tokens: a 16-token and a 1-token slice (decode path)
+    (776, 1088, 32, 32, 0, 0),      # 32 tokens: two 16-token slices, double quantization off
 ]
 
 
@@ -83,8 +85,8 @@ def test_in_kernel_dequant_is_bit_exact(ql, N, K, M):
     A = torch.randn(K, r).to(torch.bfloat16).to(dev)
     Bz = torch.zeros(r, N, dtype=torch.bfloat16, device=dev)
     for k0 in range(0, K, M):
-        # every batch stays above 16 tokens (M <= 16 takes the decode path)
-        ks = np.arange(min(k0, K - 17), min(K, k0 + M))
+        # every batch stays above 32 tokens (M <= 32 takes the decode path)
+        ks = np.arange(min(k0, K - 33), min(K, k0 + M))
         X = torch.zeros(len(ks), K, dtype=torch.bfloat16)
         X[torch.arange(len(ks)), torch.from_numpy(ks)] = 1.0
         Y, _ = ql.qlora_linear_fwd(X.to(dev), q, A, Bz, 2.0)
@@ -92,10 +94,10 @@ def test_in_kernel_dequant_is_bit_exact(ql, N, K, M):
         assert np.array_equal(bits(Y), Wh.T[ks]), f"tokens {k0}..{ks[-1]}"
 
 
-@pytest.mark.parametrize("idx,M", [(0, 128), (1, 128), (2, 128), (1, 32)])
+@pytest.mark.parametrize("idx,M", [(0, 128), (1, 128), (2, 128), (1, 48), (1, 32)])
 def test_llama13b_full_size(ql, idx, M):
     """LLaMA-13B shapes (5120^2, 13824x5120, 5120x13824), r = 64, checked in
-    full against the oracle."""
+    full against the oracle (M = 32: two decode slices)."""
     from bit_nf4_quantized_38_b300.workloads import case_inputs, case_weight, llama13b_decode
     case = llama13b_decode(M=M).cases[idx]
     W = case_weight(case)
