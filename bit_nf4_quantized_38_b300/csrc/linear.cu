@@ -373,12 +373,16 @@ int linear_fwd_fp8(const LinearArgs &a) {
   return launch_nf4_gemm(g, st);
 }
 
-// E4M3 backward workspace: [partial maxima of |m_hat| | pad to 1 KB][row exponents of dY, M int32]
+// E4M3 backward workspace: two halves (calls on a stream alternate), each
+// [partial maxima of |m_hat| | pad to 1 KB][row exponents of dY, M int32]
 // [dY codes M x N bytes][Gs' M x r bf16][G M x r bf16][XA M x r bf16 (recomputed
 // when the caller passes none)]
+size_t fp8_bwd_half(int64_t M, int64_t N, int32_t r) {
+  return 1024 + up256((size_t)M * 4) + up256((size_t)M * N) + 3 * up256((size_t)M * r * 2);
+}
 size_t linear_bwd_fp8_ws(int64_t M, int64_t N, int64_t K, int32_t r) {
   if (M <= 0 || N <= 0 || K <= 0 || !rank_ok(r)) return 0;
-  return 1024 + up256((size_t)M * 4) + up256((size_t)M * N) + 3 * up256((size_t)M * r * 2);
+  return 2 * fp8_bwd_half(M, N, r);
 }
 
 // Backward with E4M3 main steps in dX (5 or 6 launches, in stream order):
@@ -387,6 +391,9 @@ size_t linear_bwd_fp8_ws(int64_t M, int64_t N, int64_t K, int32_t r) {
 //   2. G = dY B^T -> G16 = bf16(G) and Gs' = bf16(fl32(s G) 2^(E_m + E)) LoRA kernel
 //   3. dX = 2^(-E_m - E) (dY_e4m3 . W_e4m3 + Gs' A^T)                     CTA-pair GEMM
 //   4. dA = s X^T G16 and dB = s XA^T dY (as in the bf16 backward)       one LoRA launch
+// As in the E4M3 forward, the kernels before the GEMM read and compute
+// alongside the previous call's last kernels when their inputs and this
+// call's workspace half are clear of that call.
 int linear_bwd_fp8(const LinearArgs &a) {
   const char *fn = "qlora_linear_bwd_fp8";
   if (!a.dY || !a.X || !a.A || !a.B || !a.dX || !a.dA || !a.dB)
@@ -400,8 +407,21 @@ int linear_bwd_fp8(const LinearArgs &a) {
   if (N % 16)  // rows of dY codes are TMA rows: a multiple of 16 bytes
     return set_error(QL_ERR_UNSUPPORTED, "%s: N = %lld not a multiple of 16", fn, (long long)N);
   cudaStream_t st = a.stream;
-  note_other_call(st);  // the next call waits for this one in full
-  char *ws = static_cast<char *>(a.ws);
+  const size_t half = fp8_bwd_half(M, N, r);
+  char *ws = static_cast<char *>(a.ws) + (next_ws_half(st) ? half : 0);
+  std::vector<Range> prep_reads = {range(a.dY, (size_t)(M * N * 2))};
+  weight_ranges(a.W, prep_reads);
+  const bool prep_free = reads_clear_of_previous(st, prep_reads) && writes_clear_of_previous(st, {range(ws, half)});
+  std::vector<Range> lora_reads = {range(a.dY, (size_t)(M * N * 2)), range(a.X, (size_t)(M * K * 2)),
+                                   range(a.A, (size_t)(K * r * 2)), range(a.B, (size_t)(r * N * 2))};
+  if (a.XA_in) lora_reads.push_back(range(a.XA_in, (size_t)(M * r * 2)));
+  const bool lora_early = prep_free && reads_clear_of_previous(st, lora_reads);
+  std::vector<Range> reads = lora_reads;
+  weight_ranges(a.W, reads);
+  note_call(st, true,
+            {range(a.dX, (size_t)(M * K * 2)), range(a.dA, (size_t)(K * r * 4)), range(a.dB, (size_t)(r * N * 4)),
+             range(ws, half)},
+            std::move(reads));
   float *wpart = reinterpret_cast<float *>(ws);
   int *rows = reinterpret_cast<int *>(ws + 1024);
   uint8_t *dyq = reinterpret_cast<uint8_t *>(ws + 1024 + up256((size_t)M * 4));
@@ -410,14 +430,18 @@ int linear_bwd_fp8(const LinearArgs &a) {
   uint16_t *xa_tmp = reinterpret_cast<uint16_t *>(reinterpret_cast<char *>(g16) + up256((size_t)M * r * 2));
   const NF4View w = nf4_view(a.W);
   int nwpart = 0;
-  QL_TRY(check_cuda(launch_prep_e4m3(a.dY, M, N, w, dyq, rows, wpart, &nwpart, false, st),
+  QL_TRY(check_cuda(launch_prep_e4m3(a.dY, M, N, w, dyq, rows, wpart, &nwpart, prep_free, st),
                     "qlora_linear_bwd_fp8: operand codes"));
+  // the LoRA kernels before the GEMM read inputs only and store after their
+  // predecessor completes (the operand kernel, whose completion implies the
+  // previous call's)
+  const int lora_dep = lora_early ? kDepStores : kDepStart;
   const uint16_t *xa = a.XA_in;
   if (!xa) {  // XA = X A (fp32 accumulation, bf16)
     LoraProblem L{};
     L.A = a.X; L.a_mn = false; L.B = a.A; L.b_mn = true;
     L.P = M; L.Q = r; L.T = K; L.mode = 0; L.scale = 1.0f; L.out = xa_tmp; L.ldo = r;
-    L.dep = kDepStart;
+    L.dep = lora_dep;
     QL_TRY(launch_lora(L, st));
     xa = xa_tmp;
   }
@@ -429,7 +453,7 @@ int linear_bwd_fp8(const LinearArgs &a) {
     L.row_exp = rows;
     L.wmax = wpart;
     L.nwpart = nwpart;
-    L.dep = kDepStart;
+    L.dep = lora_dep;
     QL_TRY(launch_lora(L, st));
   }
   {  // dX = 2^(-E_m - E) (dY_e4m3 W_e4m3 + Gs' A^T)

@@ -222,3 +222,37 @@ def test_back_to_back_calls_equal_synchronised_calls(ql):
     Y2, _ = ql.qlora_linear_fwd_fp8(Y1, qs[1], A1, B1, s1, ws=ws)
     torch.cuda.synchronize()
     assert torch.equal(Y2, Y2s)
+
+
+def test_back_to_back_backward_calls_equal_synchronised_calls(ql):
+    """E4M3 backward calls issued back to back on one stream and workspace,
+    interleaved with E4M3 forwards (saved XA and recomputed XA), give
+    bit-identical dX, dA, dB to calls separated by a synchronisation."""
+    from bit_nf4_quantized_38_b300.workloads import normal_bf16
+    dev = torch.device("cuda")
+    shapes = [(1024, 1024, 512, 32), (2048, 1024, 512, 16), (1024, 2048, 512, 64)]
+    cases = [make(N, K, M, r, seed=80 + i) for i, (N, K, M, r) in enumerate(shapes)]
+    qs = [ql.nf4_quantize(W.to(dev)) for W, *_ in cases]
+    ins = [(X.to(dev), A.to(dev), B.to(dev), normal_bf16((M, N), 1.0, 90 + i).to(dev), s)
+           for i, ((_, X, A, B, s), (N, K, M, r)) in enumerate(zip(cases, shapes))]
+    ws = torch.empty(max(ql.workspace_size(op, 512, 2048, 2048, 64)
+                         for op in (ql.OP_LINEAR_FWD_FP8, ql.OP_LINEAR_BWD_FP8)), dtype=torch.uint8, device=dev)
+    xas = [ql.qlora_linear_fwd_fp8(X, q, A, B, s)[1] for q, (X, A, B, dY, s) in zip(qs, ins)]
+    torch.cuda.synchronize()
+    ref = []
+    for i, (q, (X, A, B, dY, s)) in enumerate(zip(qs, ins)):
+        out = ql.qlora_linear_bwd_fp8(dY, X, xas[i] if i % 2 == 0 else None, q, A, B, s, ws=ws)
+        torch.cuda.synchronize()
+        ref.append(tuple(t.clone() for t in out))
+    outs = [tuple(torch.empty_like(t) for t in r) for r in ref]
+    Y = [torch.empty(X.shape[0], q.rows, dtype=torch.bfloat16, device=dev) for q, (X, *_) in zip(qs, ins)]
+    for _ in range(3):
+        for i, (q, (X, A, B, dY, s)) in enumerate(zip(qs, ins)):
+            ql.qlora_linear_fwd_fp8(X, q, A, B, s, Y=Y[i], ws=ws)
+            dX, dA, dB = outs[i]
+            ql.qlora_linear_bwd_fp8(dY, X, xas[i] if i % 2 == 0 else None, q, A, B, s, dX=dX, dA=dA, dB=dB, ws=ws)
+    torch.cuda.synchronize()
+    ql.device_status()
+    for r, o in zip(ref, outs):
+        for a, b in zip(r, o):
+            assert torch.equal(a, b)
