@@ -291,8 +291,10 @@ QL_API int qlora_linear_fwd(const uint16_t *X, int64_t M, const ql_nf4_tensor *W
  * products accumulate in fp32.  Arguments, layouts and XA_out as for
  * qlora_linear_fwd; K % 8 == 0 (always, as K % 64 == 0).
  *   ws : ql_workspace_size(QL_OP_LINEAR_FWD_FP8, M, N, K, r) bytes.
- * Every M takes the tensor-core path (tiles of 256 tokens).  The next call on
- * the stream waits for this one to complete.
+ * Every M takes the tensor-core path (tiles of 256 tokens).  Successive calls
+ * on a stream alternate between the two halves of `ws` (any initial
+ * contents work), so a call's first kernels may run while the previous
+ * call's GEMM finishes when they read nothing it writes.
  */
 QL_API int qlora_linear_fwd_fp8(const uint16_t *X, int64_t M, const ql_nf4_tensor *W,
                          const uint16_t *A, const uint16_t *B, int32_t r,
@@ -328,8 +330,10 @@ QL_API int qlora_linear_bwd(const uint16_t *dY, const uint16_t *X, const uint16_
  * Arguments and layouts as for qlora_linear_bwd; N % 16 == 0 (the rows of
  * the dY codes are TMA rows), else QL_ERR_UNSUPPORTED.
  *   ws : ql_workspace_size(QL_OP_LINEAR_BWD_FP8, M, N, K, r) bytes.
- * Every M takes the tensor-core path (tiles of 256 tokens).  The next call on
- * the stream waits for this one to complete.
+ * Every M takes the tensor-core path (tiles of 256 tokens).  Successive calls
+ * on a stream alternate between the two halves of `ws` (any initial
+ * contents work), so a call's first kernels may run while the previous
+ * call's GEMM finishes when they read nothing it writes.
  */
 QL_API int qlora_linear_bwd_fp8(const uint16_t *dY, const uint16_t *X, const uint16_t *XA,
                          int64_t M, const ql_nf4_tensor *W, const uint16_t *A,
