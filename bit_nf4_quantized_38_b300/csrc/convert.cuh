@@ -102,7 +102,11 @@ __device__ __forceinline__ uint32_t lut4_e4m3(uint32_t s, const uint32_t (&T)[4]
 // becomes e4m3(fl32(q[c] * m_hat) * 2^E); its 64 bytes are 16-byte pieces
 // 4h .. 4h + 3 of the 128-byte swizzled row at `row_addr` (piece j stored at
 // j ^ swz): h = 0 for the first 64 K-elements of a 128-wide step, 1 for the
-// second.
+// second.  kInOrder: byte i holds element i; otherwise the bytes of each pair
+// come out swapped (element 2j + 1 at byte 2j), which saves the nibble swap
+// and is exact wherever the other operand carries the same order along the
+// reduction (a dot product does not depend on the order of its terms).
+template <bool kInOrder>
 __device__ __forceinline__ void convert_rowblock_e4m3(const uint4 &p0, const uint4 &p1, float mE,
                                                       const float (&q)[16], uint32_t row_addr, int h, uint32_t swz) {
   uint32_t T[4];
@@ -117,9 +121,9 @@ __device__ __forceinline__ void convert_rowblock_e4m3(const uint4 &p0, const uin
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const uint32_t w = words[2 * jj + t];
-      // byte j of w holds element 2j (high nibble) and 2j + 1 (low): swap so
-      // that nibble i holds element i
-      const uint32_t sw = ((w >> 4) & 0x0F0F0F0Fu) | ((w << 4) & 0xF0F0F0F0u);
+      // byte j of w holds element 2j (high nibble) and 2j + 1 (low): swapped,
+      // nibble i holds element i
+      const uint32_t sw = kInOrder ? (((w >> 4) & 0x0F0F0F0Fu) | ((w << 4) & 0xF0F0F0F0u)) : w;
       o[2 * t] = lut4_e4m3(sw, T);
       o[2 * t + 1] = lut4_e4m3(sw >> 16, T);
     }

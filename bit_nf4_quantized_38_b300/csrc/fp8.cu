@@ -34,15 +34,19 @@ __device__ __forceinline__ float absmax8(const uint4 v) {
   return a;
 }
 
-// Eight codes e4m3(x 2^E_m) (the scaling is exact), element 2j in the low byte
-// of pair j: the hardware conversion (round to nearest even, saturating at
-// +-448), which equals e4m3_code for every finite input.
-__device__ __forceinline__ uint2 codes8(const uint4 v, float sc) {
+// Eight codes e4m3(x 2^E_m) (the scaling is exact): the hardware conversion
+// (round to nearest even, saturating at +-448), which equals e4m3_code for
+// every finite input.  Element 2j in the low byte of pair j, or, with
+// `swapped`, in the high byte (the pair order of the forward GEMM's weight
+// rows).
+__device__ __forceinline__ uint2 codes8(const uint4 v, float sc, bool swapped) {
   const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
   uint32_t h[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    h[j] = ptx::cvt_e4m3x2(__fmul_rn(bf16lo_to_f32(wd[j]), sc), __fmul_rn(bf16hi_to_f32(wd[j]), sc));
+  for (int j = 0; j < 4; ++j) {
+    const float lo = __fmul_rn(bf16lo_to_f32(wd[j]), sc), hi = __fmul_rn(bf16hi_to_f32(wd[j]), sc);
+    h[j] = swapped ? ptx::cvt_e4m3x2(hi, lo) : ptx::cvt_e4m3x2(lo, hi);
+  }
   return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
 }
 
@@ -68,7 +72,7 @@ template <int R>
 __global__ void __launch_bounds__(R == 4 ? 128 : 256, R == 4 ? 8 : 3) k_prep_e4m3(const uint4 *__restrict__ X, int64_t M, int64_t K,
                                                                   uint2 *__restrict__ codes, int *__restrict__ row_exp,
                                                                   NF4View w, float *__restrict__ wpart, int gw,
-                                                                  int free_) {
+                                                                  int free_, int swapped) {
   __shared__ float red[2][8];
   if (!free_) ptx::griddep_wait();
   ptx::griddep_launch();  // the dependents wait for this grid before reading its output
@@ -149,7 +153,7 @@ __global__ void __launch_bounds__(R == 4 ? 128 : 256, R == 4 ? 8 : 3) k_prep_e4m
 #pragma unroll
       for (int j = 0; j < R; ++j) {
         const int64_t i = threadIdx.x + (int64_t)j * nt;
-        if (i < n8) codes[r * n8 + i] = codes8(v[j], sc);
+        if (i < n8) codes[r * n8 + i] = codes8(v[j], sc, swapped != 0);
       }
     };
     uint4 va[R], vb[R];
@@ -170,7 +174,7 @@ __global__ void __launch_bounds__(R == 4 ? 128 : 256, R == 4 ? 8 : 3) k_prep_e4m
       float a = 0.0f;
       for (int64_t i = threadIdx.x; i < n8; i += nt) a = fmaxf(a, absmax8(__ldg(x + i)));
       const float sc = row_scale(a, red[par], row, row_exp);
-      for (int64_t i = threadIdx.x; i < n8; i += nt) codes[row * n8 + i] = codes8(__ldg(x + i), sc);
+      for (int64_t i = threadIdx.x; i < n8; i += nt) codes[row * n8 + i] = codes8(__ldg(x + i), sc, swapped != 0);
     }
   }
   if (waiter) ptx::griddep_wait();  // this grid completes after its predecessor
@@ -206,7 +210,7 @@ int sm_count() {
 }  // namespace
 
 cudaError_t launch_prep_e4m3(const uint16_t *X, int64_t M, int64_t K, const NF4View &w, uint8_t *codes, int *row_exp,
-                             float *wpart, int *n_wpart, bool free_, cudaStream_t st) {
+                             float *wpart, int *n_wpart, bool free_, bool swapped, cudaStream_t st) {
   const int64_t n_b = w.rows * w.cols / 64;
   const bool small = K <= 4 * 128 * 8;  // rows of up to 4096 elements: 128 threads x 4 pieces
   const int nt = small ? 128 : 256;
@@ -226,9 +230,9 @@ cudaError_t launch_prep_e4m3(const uint16_t *X, int64_t M, int64_t K, const NF4V
   cfg.numAttrs = 1;
   const uint4 *x4 = reinterpret_cast<const uint4 *>(X);
   uint2 *c2 = reinterpret_cast<uint2 *>(codes);
-  const int fr = free_ ? 1 : 0;
-  cudaError_t e = small ? cudaLaunchKernelEx(&cfg, k_prep_e4m3<4>, x4, M, K, c2, row_exp, w, wpart, gw, fr)
-                        : cudaLaunchKernelEx(&cfg, k_prep_e4m3<6>, x4, M, K, c2, row_exp, w, wpart, gw, fr);
+  const int fr = free_ ? 1 : 0, sw = swapped ? 1 : 0;
+  cudaError_t e = small ? cudaLaunchKernelEx(&cfg, k_prep_e4m3<4>, x4, M, K, c2, row_exp, w, wpart, gw, fr, sw)
+                        : cudaLaunchKernelEx(&cfg, k_prep_e4m3<6>, x4, M, K, c2, row_exp, w, wpart, gw, fr, sw);
   count_launch();
   return e;
 }

@@ -11,9 +11,11 @@ namespace ql {
 // == 0; X 16- and codes 8-byte aligned.  free_: X and the weight are not
 // written, and codes, row_exp and wpart not read or written, by any kernel
 // that may still be running (the kernel then runs alongside its predecessor).
+// swapped: each pair of codes stored in swapped order (element 2j + 1 at byte
+// 2j), the order of the forward GEMM's E4M3 weight rows along the reduction.
 constexpr int kWmaxParts = 148;
 cudaError_t launch_prep_e4m3(const uint16_t *X, int64_t M, int64_t K, const NF4View &w, uint8_t *codes, int *row_exp,
-                             float *wpart, int *n_wpart, bool free_, cudaStream_t st);
+                             float *wpart, int *n_wpart, bool free_, bool swapped, cudaStream_t st);
 
 // max |m_hat| from the partial maxima, by one warp (every lane gets it).
 __device__ __forceinline__ float wmax_of_warp(const float *wpart, int n) {

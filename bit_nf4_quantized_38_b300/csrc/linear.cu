@@ -341,7 +341,8 @@ int linear_fwd_fp8(const LinearArgs &a) {
   note_call(st, true, std::move(writes), reads);
 
   int nwpart = 0;
-  QL_TRY(check_cuda(launch_prep_e4m3(a.X, M, K, w, xq, rows, wpart, &nwpart, prep_free, st),
+  // the codes in pair-swapped order, matching the GEMM's weight rows
+  QL_TRY(check_cuda(launch_prep_e4m3(a.X, M, K, w, xq, rows, wpart, &nwpart, prep_free, true, st),
                     "qlora_linear_fwd_fp8: operand codes"));
   LoraProblem L{};
   L.A = a.X; L.a_mn = false; L.B = a.A; L.b_mn = true;  // X [M][K], A [K][r]
@@ -430,7 +431,7 @@ int linear_bwd_fp8(const LinearArgs &a) {
   uint16_t *xa_tmp = reinterpret_cast<uint16_t *>(reinterpret_cast<char *>(g16) + up256((size_t)M * r * 2));
   const NF4View w = nf4_view(a.W);
   int nwpart = 0;
-  QL_TRY(check_cuda(launch_prep_e4m3(a.dY, M, N, w, dyq, rows, wpart, &nwpart, prep_free, st),
+  QL_TRY(check_cuda(launch_prep_e4m3(a.dY, M, N, w, dyq, rows, wpart, &nwpart, prep_free, false, st),
                     "qlora_linear_bwd_fp8: operand codes"));
   // the LoRA kernels before the GEMM read inputs only and store after their
   // predecessor completes (the operand kernel, whose completion implies the

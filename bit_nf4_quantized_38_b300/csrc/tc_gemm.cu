@@ -620,7 +620,10 @@ k_nf4_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (kFp8) {
 #pragma unroll
           for (int h = 0; h < RB; ++h)  // an invalid row-block has zero codes and constant: zero bytes
-            convert_rowblock_e4m3(cur[h].p0, cur[h].p1, __fmul_rn(rowblock_mhat(cur[h], p.w, mean), s2e), q,
+            // forward: the reduction runs along the row, and the X codes
+            // carry the same pair order, so the pairs may stay swapped; dX:
+            // the row runs along the output columns, so in order
+            convert_rowblock_e4m3<kTrans>(cur[h].p0, cur[h].p1, __fmul_rn(rowblock_mhat(cur[h], p.w, mean), s2e), q,
                                   b_addr + rb_dst, h, rb_swz);
         } else {
           if (cur[0].valid) convert_rowblock(cur[0].p0, cur[0].p1, rowblock_mhat(cur[0], p.w, mean), q, b_addr + rb_dst, rb_swz);

@@ -256,3 +256,27 @@ def test_back_to_back_backward_calls_equal_synchronised_calls(ql):
     for r, o in zip(ref, outs):
         for a, b in zip(r, o):
             assert torch.equal(a, b)
+
+
+def test_fp4_weights_forward_and_backward(ql):
+    """The E4M3 forward and backward on FP4-coded weights (the comparison code
+    table): the weight's E4M3 values come from the FP4 levels."""
+    from bit_nf4_quantized_38_b300.workloads import normal_bf16
+    N, K, M, r = 528, 640, 300, 16
+    W, X, A, B, s = make(N, K, M, r, seed=101)
+    dY = normal_bf16((M, N), 1.0, 102)
+    dev = torch.device("cuda")
+    q = ql.nf4_quantize(W.to(dev), quant_type=ql.QL_FP4)
+    Xd, Ad, Bd, dYd = X.to(dev), A.to(dev), B.to(dev), dY.to(dev)
+    Y, XA = ql.qlora_linear_fwd_fp8(Xd, q, Ad, Bd, s)
+    dX, dA, dB = ql.qlora_linear_bwd_fp8(dYd, Xd, XA, q, Ad, Bd, s)
+    torch.cuda.synchronize()
+    ql.device_status()
+    qt = nf4.quantize(bits(W), quant_type=nf4.QT_FP4)
+    Yr, _ = fp8.lora_forward_e4m3(bits(X), qt, bits(A), bits(B), s)
+    dXr, _ = fp8.lora_backward_e4m3(bits(dY), qt, bits(A), bits(B), s)
+    dAr, dBr, _ = linear.lora_adapter_grads(bits(dY), bits(X), bits(A), bits(B), s)
+    assert_close("Y e4m3 fp4 weights", f64(Y), Yr)
+    assert_close("dX e4m3 fp4 weights", f64(dX), dXr)
+    assert_close("dA e4m3 fp4 weights", dA.double().cpu().numpy(), dAr)
+    assert_close("dB e4m3 fp4 weights", dB.double().cpu().numpy(), dBr)
