@@ -88,13 +88,18 @@ __device__ __forceinline__ void convert_rowblock2(const uint4 &a0, const uint4 &
   }
 }
 
-// 4 E4M3 bytes (elements i = 0..3 in bytes 0..3) from the 4 codes in
-// nibbles 0..3 of `s`, through the 16-byte table T (entry c in byte c % 4 of
-// T[c / 4]): bits 0-2 of a code pick a byte among 8, bit 3 the table half.
-__device__ __forceinline__ uint32_t lut4_e4m3(uint32_t s, const uint32_t (&T)[4]) {
+// 8 E4M3 bytes (elements i = 0..7 in bytes 0..7 of lo, hi) from the 8 codes
+// in nibbles 0..7 of `s`, through the 16-byte table T (entry c in byte c % 4
+// of T[c / 4]): bits 0-2 of a code pick a byte among 8, bit 3 the table half.
+// A byte permute reads only the low 16 bits (4 selectors) of its selector
+// word, so both halves share one masked word and one final-selector word.
+__device__ __forceinline__ void lut8_e4m3(uint32_t s, const uint32_t (&T)[4], uint32_t &lo, uint32_t &hi) {
   using ptx::prmt;
-  const uint32_t sel = s & 0x7777u;
-  return prmt(prmt(T[0], T[1], sel), prmt(T[2], T[3], sel), ((s >> 1) & 0x4444u) | 0x3210u);
+  const uint32_t sel = s & 0x77777777u;                      // byte index within a table half
+  const uint32_t fin = ((s >> 1) & 0x44444444u) | 0x32103210u;  // which half, per element
+  const uint32_t sel_h = sel >> 16, fin_h = fin >> 16;
+  lo = prmt(prmt(T[0], T[1], sel), prmt(T[2], T[3], sel), fin);
+  hi = prmt(prmt(T[0], T[1], sel_h), prmt(T[2], T[3], sel_h), fin_h);
 }
 
 // One 64-element row-block to E4M3: the block's table holds
@@ -124,8 +129,7 @@ __device__ __forceinline__ void convert_rowblock_e4m3(const uint4 &p0, const uin
       // byte j of w holds element 2j (high nibble) and 2j + 1 (low): swapped,
       // nibble i holds element i
       const uint32_t sw = kInOrder ? (((w >> 4) & 0x0F0F0F0Fu) | ((w << 4) & 0xF0F0F0F0u)) : w;
-      o[2 * t] = lut4_e4m3(sw, T);
-      o[2 * t + 1] = lut4_e4m3(sw >> 16, T);
+      lut8_e4m3(sw, T, o[2 * t], o[2 * t + 1]);
     }
     ptx::sts128(row_addr + ((((uint32_t)(4 * h + jj)) ^ swz) << 4), o[0], o[1], o[2], o[3]);
   }
