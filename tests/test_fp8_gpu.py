@@ -47,6 +47,7 @@ def make(N, K, M, r, seed):
     (264, 640, 17, 64, 256, 0),      # few tokens, mostly padding
     (1024, 1024, 300, 128, 256, 1),  # rank 128; E4M3 second-level codes
     (776, 1088, 513, 8, 0, 0),       # double quantization off
+    (520, 576, 1, 16, 256, 0),       # one token in a 256-row tile
 ])
 def test_forward_matches_the_e4m3_oracle(ql, N, K, M, r, dq, dqt):
     W, X, A, B, s = make(N, K, M, r, seed=N + K + M + r)
@@ -118,6 +119,7 @@ def test_llama7b_q_proj_full_size_sampled(ql):
     (272, 640, 17, 64, 256, 0, True),      # few tokens
     (1024, 1024, 300, 128, 256, 1, True),  # rank 128; E4M3 second-level codes
     (784, 1088, 513, 8, 0, 0, False),      # double quantization off
+    (528, 576, 3, 16, 256, 0, False),      # three tokens in a 256-row tile
 ])
 def test_backward_matches_the_e4m3_oracle(ql, N, K, M, r, dq, dqt, saved_xa):
     W, X, A, B, s = make(N, K, M, r, seed=N + 2 * K + M + r)
