@@ -530,12 +530,15 @@ def run_only(args):
     print(json.dumps({"only": args.only, "results": res}), flush=True)
 
 
-def bench_forward_fp8(ql, dev, peaks, steps=20, warmup=5):
+def bench_forward_fp8(ql, dev, peaks, steps=20, warmup=5, rounds=3):
     """The LLaMA-7B linears (M = 4096 tokens, r = 64): the bf16 and the E4M3
     forward, and the bf16 and the E4M3 backward (dX main product on E4M3),
     each timed over `steps` passes of the 7 calls with CUDA events; flops
     counted as 2 M N K + 2 M r (N + K) per linear forward and
-    2 M N K + 4 M r (N + K) per linear backward for both."""
+    2 M N K + 4 M r (N + K) per linear backward for both.  The two variants
+    alternate over `rounds` rounds (the order flipped each round, so that a
+    drifting clock under the power cap favours neither) and each reports its
+    median."""
     import torch
     wl = workload_of("llama7b")
     layers = build_layers(ql, dev, wl)
@@ -576,11 +579,19 @@ def bench_forward_fp8(ql, dev, peaks, steps=20, warmup=5):
         ms = e0.elapsed_time(e1) / steps
         return {"ms_per_pass": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12}
 
-    out["bf16"] = timed(fwd(ql.qlora_linear_fwd), fwd_flops)
-    out["e4m3"] = timed(fwd(ql.qlora_linear_fwd_fp8), fwd_flops)
+    def alternate(name_a, pass_a, name_b, pass_b, flops):
+        ms = {name_a: [], name_b: []}
+        for rd in range(rounds):
+            order = ((name_a, pass_a), (name_b, pass_b)) if rd % 2 == 0 else ((name_b, pass_b), (name_a, pass_a))
+            for name, one_pass in order:
+                ms[name].append(timed(one_pass, flops)["ms_per_pass"])
+        for name in (name_a, name_b):
+            med = sorted(ms[name])[len(ms[name]) // 2]
+            out[name] = {"ms_per_pass": med, "TFLOP/s": flops / (med * 1e-3) / 1e12, "rounds_ms": ms[name]}
+
+    alternate("bf16", fwd(ql.qlora_linear_fwd), "e4m3", fwd(ql.qlora_linear_fwd_fp8), fwd_flops)
     out["speedup_e4m3_over_bf16"] = out["bf16"]["ms_per_pass"] / out["e4m3"]["ms_per_pass"]
-    out["bwd_bf16"] = timed(bwd(ql.qlora_linear_bwd), bwd_flops)
-    out["bwd_e4m3"] = timed(bwd(ql.qlora_linear_bwd_fp8), bwd_flops)
+    alternate("bwd_bf16", bwd(ql.qlora_linear_bwd), "bwd_e4m3", bwd(ql.qlora_linear_bwd_fp8), bwd_flops)
     out["bwd_speedup_e4m3_over_bf16"] = out["bwd_bf16"]["ms_per_pass"] / out["bwd_e4m3"]["ms_per_pass"]
     out["peak_e4m3_tflops"] = 2.0 * peaks["bf16_tflops"]
     out["peak_note"] = "E4M3 dense peak taken as 2x the measured bf16 burst peak (nominal ratio)"
