@@ -48,6 +48,13 @@ def test_workspace_sizes(ql):
     assert ql.workspace_size(ql.OP_QUANTIZE, 0, 4096, 4096, 0) >= 4096 * 4096 // 64 * 4
     assert ql.workspace_size(ql.OP_DEQUANTIZE, 0, 4096, 4096, 0) == 0
     assert ql.workspace_size(99) == 2 ** 64 - 1
+    # 17-32 tokens run as 16-token decode slices: the decode workspace
+    fwd = lambda M: ql.workspace_size(ql.OP_LINEAR_FWD, M, 5120, 5120, 64)
+    assert fwd(17) == fwd(32) == fwd(16) == fwd(1) and fwd(33) != fwd(32)
+    # the E4M3 calls keep two halves, each holding the M x K (forward) or
+    # M x N (backward) codes
+    assert ql.workspace_size(ql.OP_LINEAR_FWD_FP8, 4096, 1024, 4096, 64) >= 2 * 4096 * 4096
+    assert ql.workspace_size(ql.OP_LINEAR_BWD_FP8, 4096, 1024, 4096, 64) >= 2 * 4096 * 1024
 
 
 def test_quantize_rejects_bad_arguments_on_host(ql):
