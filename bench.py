@@ -876,8 +876,8 @@ def main():
                          "results": bench_decode(ql, dev, peaks["hbm_gbs"], args.decode_calls,
                                                  tuple(int(m) for m in args.decode_m.split(",")),
                                                  tuple(int(i) for i in args.decode_shapes.split(",")))}
-        out["prefill"] = {"workload": "llama13b shapes, M in {32,48,64,128} tokens (32: two 16-token slices "
-                                      "through the weight-streaming kernel; 48-128: the few-token tensor-core "
+        out["prefill"] = {"workload": "llama13b shapes, M in {32,48,64,128} tokens (32: one 32-token pass "
+                                      "of the weight-streaming kernel; 48-128: the few-token tensor-core "
                                       "kernel), r=64, fwd, CUDA graph over weight copies > 3x L2",
                           "peak_hbm_gbs": peaks["hbm_gbs"],
                           "results": bench_decode(ql, dev, peaks["hbm_gbs"], 120, (32, 48, 64, 128), (0, 1, 2))}

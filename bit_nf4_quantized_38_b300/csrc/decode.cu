@@ -1,4 +1,4 @@
-// Decode-sized forward (M <= 16 tokens) of the frozen-NF4 linear with LoRA:
+// Decode-sized forward (M <= 32 tokens) of the frozen-NF4 linear with LoRA:
 //   Y = X W_hat^T + s (X A) B
 // At decode batch sizes the layer is bound by HBM traffic on the packed 4-bit
 // weights (0.5 B/param + 1/64 B/param of block codes), so this is a streaming
@@ -7,18 +7,19 @@
 //   k_decode_stream  one persistent CTA per SM (at most), 16 warps.  The
 //                    units (256-row group x 256-wide K box) are taken in
 //                    row-group-major order and split evenly over the CTAs.  A
-//                    3-stage shared-memory ring is filled by TMA: per unit a
-//                    256 x 128 B box of packed nibbles (128-byte swizzle) and
-//                    four 64-wide boxes of X (rows past M zero filled).  The
-//                    first three units are loaded at the start, each later one
-//                    by the last warp to finish with a stage.  Warp w owns rows 16 w ..
-//                    16 w + 15 of the unit: every packed byte (two codes) is
-//                    looked up in a 256-entry table of bf16 level pairs kept
-//                    once per lane in shared memory (one byte permute forms
-//                    the lookup address, and lookups never conflict on a
-//                    bank); warp MMAs m16n8k16 with weight rows as M and
-//                    tokens as N accumulate each 64-block in a fresh fp32
-//                    tile that is then scaled by the block constant.  When a
+//                    3-stage (2-stage with 32 tokens) shared-memory ring is
+//                    filled by TMA: per unit a 256 x 128 B box of packed
+//                    nibbles (128-byte swizzle) and four 64-wide boxes of X
+//                    (rows past M zero filled).  The first units are loaded
+//                    at the start, each later one by the last warp to finish
+//                    with a stage.  Warp w owns rows 16 w .. 16 w + 15 of the
+//                    unit: every packed byte (two codes) is looked up in a
+//                    256-entry table of fp32 level pairs kept once per lane
+//                    in shared memory (one byte permute forms the lookup
+//                    address, and lookups never conflict on a bank); each
+//                    level times the block constant, rounded to bf16, is the
+//                    dequantized weight, and warp MMAs m16n8k16 with weight
+//                    rows as M and tokens as N accumulate in fp32.  When a
 //                    CTA leaves a row group it stores its partial tile to the
 //                    group's slot for that CTA.  Before streaming, the first
 //                    NX CTAs stage their share of the K rows of A and X (bulk
@@ -40,12 +41,10 @@
 // kernel that has waited for its stream kernel has also seen every earlier
 // call complete.
 //
-// Numerics: the block constant multiplies fp32 partial sums of x * bf16(q[c]),
-// so the weight used is q[c] (rounded once to bf16) times the fp32 constant,
-// not bf16(q[c] * constant) as in the dequantized matrix; the two differ by
-// one bf16 rounding per weight, inside the path's stated tolerance.  XA enters
-// the LoRA product as a bf16 high part plus a bf16 low part (about 16
-// significant bits).  Results are deterministic (fixed reduction orders).
+// Numerics: every weight is the dequantized value bf16(fl32(q[c] * m_hat)) bit
+// for bit, and products accumulate in fp32 (the MMA's order).  XA enters the
+// LoRA product as a bf16 high part plus a bf16 low part (about 16 significant
+// bits).  Results are deterministic (fixed reduction orders).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -60,14 +59,14 @@ namespace {
 
 constexpr int CONS = 16;                      // warps of the stream kernel, 16 weight rows each
 constexpr int THREADS = CONS * 32;
-constexpr int ST_STAGES = 3;
+constexpr int ST_STAGES = 3;                  // ring stages (two with 32 tokens: st_stages<4>)
 constexpr int UNIT_ROWS = 256;                // rows per unit
 constexpr int UNIT_K = 256;                   // K values per unit (128 packed bytes per row)
 constexpr int W_BYTES = UNIT_ROWS * 128;      // packed box of a unit
-constexpr int TAB_BYTES = 256 * 256;          // 256 entries x 256 B stride (32 lanes x 4 B used)
+constexpr int TAB_BYTES = 256 * 256;          // 256 entries x 256 B (32 lanes x an fp32 pair)
 constexpr int PD = 2;                         // units of block constants loaded ahead
 constexpr int G_MAX = 160;                    // persistent CTAs at most (one per SM)
-constexpr int SLOT_FLOATS = UNIT_ROWS * 16;   // partial tile of a row group: 256 rows x 16 tokens
+constexpr int MAX_TOKS = 32;                  // tokens of the largest variant (MT = 4)
 constexpr int XA_A_BYTES = 16384;             // staged rows of A per chunk, at most
 constexpr int XA_KC_MAX = 256;
 constexpr int FIN_WARPS = 4;                  // finishing kernel: 4 warps x 32 rows
@@ -75,21 +74,29 @@ constexpr int FIN_ROWS = FIN_WARPS * 32;
 
 template <int MT>
 constexpr int stage_bytes() { return W_BYTES + 4 * (MT * 8) * 128; }
+template <int MT>
+constexpr int st_stages() { return MT == 4 ? 2 : ST_STAGES; }
+// token columns of a partial tile (slot) and of a partial XA tile: 16, or 32 with MT = 4
+template <int MT>
+constexpr int toks() { return MT == 4 ? 32 : 16; }
+template <int MT>
+constexpr int slot_floats() { return UNIT_ROWS * toks<MT>(); }
 template <int NT>
 constexpr int xa_kc() {
   return (XA_A_BYTES / (NT * 8 * 2) < XA_KC_MAX ? XA_A_BYTES / (NT * 8 * 2) : XA_KC_MAX) / 16 * 16;
 }
-template <int NT>
-constexpr int xa_smem() {  // A chunk, X chunk (16 rows)
-  return xa_kc<NT>() * NT * 8 * 2 + 16 * xa_kc<NT>() * 2;
+template <int MT, int NT>
+constexpr int xa_smem() {  // A chunk, X chunk (toks<MT> rows)
+  return xa_kc<NT>() * NT * 8 * 2 + toks<MT>() * xa_kc<NT>() * 2;
 }
 template <int MT, int NT>
 constexpr size_t dec_smem() {
-  return (size_t)TAB_BYTES + 1024 + (size_t)ST_STAGES * stage_bytes<MT>() + (size_t)xa_smem<NT>();
+  return (size_t)TAB_BYTES + 1024 + (size_t)st_stages<MT>() * stage_bytes<MT>() + (size_t)xa_smem<MT, NT>();
 }
 // room for a finishing CTA (8 KB of XA, 1 KB reserved) beside a stream CTA in 228 KB
 static_assert(dec_smem<2, 16>() + 1024 + 8192 + 1024 <= 228 * 1024, "decode shared memory");
 static_assert(dec_smem<2, 1>() + 1024 + 8192 + 1024 <= 228 * 1024, "decode shared memory");
+static_assert(dec_smem<4, 16>() + 1024 + 16384 + 1024 <= 228 * 1024, "decode shared memory");
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -121,6 +128,13 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
   return v;
+}
+// The dequantized weights of one packed byte's two codes in a row with block
+// constant m: bf16(fl32(q[c] * m)) each, from the fp32 level pair at addr
+// (element 2j in the low half).
+__device__ __forceinline__ uint32_t w_hat_pair(uint32_t addr, float m) {
+  const uint2 v = lds64(addr);
+  return pack_bf16x2(__fmul_rn(__uint_as_float(v.x), m), __fmul_rn(__uint_as_float(v.y), m));
 }
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
@@ -162,8 +176,8 @@ struct StreamArgs {  // N K / 64 < 2^31 and units < 2^31 (checked on the host)
   const float *absmax;
   const uint16_t *X;   // [M][K]
   const uint16_t *A;   // [K][R]
-  float *xap;          // [nx][16][R] partial XA tiles
-  float *slots;        // [groups + G][256 rows][16 tokens]
+  float *xap;          // [nx][toks][R] partial XA tiles
+  float *slots;        // [groups + G][256 rows][toks tokens]
   int *status;
   float q[16];
 };
@@ -192,20 +206,25 @@ __device__ __forceinline__ void xa_issue(const StreamArgs &a, uint32_t xa_base, 
 }
 
 // Warp w < NT: rank tile w (columns 8 w .. 8 w + 7) of this CTA's share of XA,
-// X as the A fragments (16 tokens, rows M..15 zero) and A as the B fragments
+// X as the A fragments (16 tokens per MMA, rows past M zero; with 32 tokens
+// two such halves share each A fragment load) and A as the B fragments
 // (n = j) through transposing loads; stored (rows < M) to the CTA's partial
 // tile.  A chunk after the first is issued once every XA warp has arrived
 // at `empty` for the one before.  Returns the number of chunks that landed.
-template <int NT>
+template <int MT, int NT>
 __device__ __forceinline__ int xa_share(const StreamArgs &a, uint32_t xa_base, uint32_t bar, uint32_t empty,
                                         volatile int *abort_v) {
-  constexpr int R = NT * 8;
+  constexpr int R = NT * 8, TH = MT == 4 ? 2 : 1;  // 16-token halves
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int c = blockIdx.x, M = a.M, KC = a.kc, NX = a.nx;
   const int64_t KS = a.K / 16;
   const int64_t k0 = (int64_t)c * KS / NX * 16, k1 = (int64_t)(c + 1) * KS / NX * 16;
   const uint32_t xa_a = xa_base, xa_x = xa_base + (uint32_t)(KC * R * 2);
-  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  float acc[TH][4];
+#pragma unroll
+  for (int h = 0; h < TH; ++h)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[h][e] = 0.0f;
   int landed_chunks = 0;
 #pragma unroll 1
   for (int64_t k = k0; k < k1; k += KC) {
@@ -218,22 +237,30 @@ __device__ __forceinline__ int xa_share(const StreamArgs &a, uint32_t xa_base, u
     ++landed_chunks;
 #pragma unroll 1
     for (int ks = 0; ks < n / 16; ++ks) {
-      const uint32_t xr = xa_x + (uint32_t)((g * KC + ks * 16 + 2 * t) * 2);
-      const uint32_t a0 = g < M ? lds32(xr) : 0u;
-      const uint32_t a2 = g < M ? lds32(xr + 16) : 0u;
-      const uint32_t a1 = g + 8 < M ? lds32(xr + (uint32_t)(8 * KC * 2)) : 0u;
-      const uint32_t a3 = g + 8 < M ? lds32(xr + (uint32_t)(8 * KC * 2) + 16) : 0u;
       uint32_t b0, b1;
       ldsm_x2_t(xa_a + (uint32_t)((ks * 16 + (lane & 15)) * R * 2 + warp * 16), b0, b1);
-      mma16816(acc, a0, a1, a2, a3, b0, b1);
+#pragma unroll
+      for (int h = 0; h < TH; ++h) {
+        const int r0 = 16 * h + g;
+        const uint32_t xr = xa_x + (uint32_t)((r0 * KC + ks * 16 + 2 * t) * 2);
+        const uint32_t a0 = r0 < M ? lds32(xr) : 0u;
+        const uint32_t a2 = r0 < M ? lds32(xr + 16) : 0u;
+        const uint32_t a1 = r0 + 8 < M ? lds32(xr + (uint32_t)(8 * KC * 2)) : 0u;
+        const uint32_t a3 = r0 + 8 < M ? lds32(xr + (uint32_t)(8 * KC * 2) + 16) : 0u;
+        mma16816(acc[h], a0, a1, a2, a3, b0, b1);
+      }
     }
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(empty);  // this warp has read the chunk
   }
   if (!a.ws_early) ptx::griddep_wait();  // before the first store to the workspace
-  float *mine = a.xap + (int64_t)c * 16 * R + warp * 8 + 2 * t;
-  if (g < M) __stcg(reinterpret_cast<float2 *>(mine + g * R), make_float2(acc[0], acc[1]));
-  if (g + 8 < M) __stcg(reinterpret_cast<float2 *>(mine + (g + 8) * R), make_float2(acc[2], acc[3]));
+  float *mine = a.xap + (int64_t)c * toks<MT>() * R + warp * 8 + 2 * t;
+#pragma unroll
+  for (int h = 0; h < TH; ++h) {
+    const int r0 = 16 * h + g;
+    if (r0 < M) __stcg(reinterpret_cast<float2 *>(mine + r0 * R), make_float2(acc[h][0], acc[h][1]));
+    if (r0 + 8 < M) __stcg(reinterpret_cast<float2 *>(mine + (r0 + 8) * R), make_float2(acc[h][2], acc[h][3]));
+  }
   return landed_chunks;
 }
 
@@ -244,7 +271,7 @@ template <int MT, int NT>  // MT token tiles of 8, NT rank tiles of 8
 __global__ void __maxnreg__(96)
 k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                 const __grid_constant__ StreamArgs a) {
-  constexpr int XR = MT * 8, SB = stage_bytes<MT>();
+  constexpr int XR = MT * 8, SB = stage_bytes<MT>(), ST_STAGES = st_stages<MT>(), TSL = toks<MT>();
   // the finishing kernel may be scheduled now: it waits for this grid to complete
   ptx::griddep_launch();
   extern __shared__ __align__(16) uint8_t smem[];
@@ -312,12 +339,13 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     xa_issue<NT>(a, xa_base, ptx::smem_u32(&xa_bar), 0);
   }
   {
-    // entry e (a packed byte), lane l: bf16 pair (q[e >> 4], q[e & 15]); the
-    // high nibble is element 2j, the lower k of the MMA pair, in the low half
-    uint4 *tp = reinterpret_cast<uint4 *>(smem);
-    for (int i = tid; i < 256 * 8; i += THREADS) {
-      const uint32_t v = pack_bf16x2(a.q[(i >> 7) & 15], a.q[(i >> 3) & 15]);
-      tp[(i >> 3) * 16 + (i & 7)] = make_uint4(v, v, v, v);
+    // entry e (a packed byte), lane l: the fp32 levels (q[e >> 4], q[e & 15])
+    // at byte 256 e + 8 l; the high nibble is element 2j, the lower k of the
+    // MMA pair
+    float4 *tp = reinterpret_cast<float4 *>(smem);
+    for (int i = tid; i < 256 * 16; i += THREADS) {
+      const float lo = a.q[(i >> 8) & 15], hi = a.q[(i >> 4) & 15];
+      tp[i] = make_float4(lo, hi, lo, hi);
     }
   }
   if (lane == 0 && warp >= 1 && warp < npre) issue_first(warp);
@@ -325,7 +353,7 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
   if (!a.w_early) ptx::griddep_wait();
 
   if (xa_cta && warp < NT) {
-    const int n = xa_share<NT>(a, xa_base, ptx::smem_u32(&xa_bar), ptx::smem_u32(&xa_empty), abort_v);
+    const int n = xa_share<MT, NT>(a, xa_base, ptx::smem_u32(&xa_bar), ptx::smem_u32(&xa_empty), abort_v);
     if (tid == 0) xa_chunks = n;
   }
 
@@ -341,7 +369,7 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
   // 16-byte load of X takes one shared-memory wavefront (M <= 2) or two
   // (M <= 4) instead of four; the products in those columns are ignored.
   const int xg = MT == 1 ? g % a.M : g;
-  const uint32_t lanebase = (uint32_t)lane * 4u;
+  const uint32_t lanebase = (uint32_t)lane * 8u;
   const float mu = a.dq ? __ldg(a.mean) : 0.0f;
 
   // block constants of block t of a unit for the lane's 2 rows (16 w + 8 k + pg),
@@ -398,12 +426,12 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
       ptx::griddep_wait();
       waited = true;
     }
-    float *slot = a.slots + (int64_t)(rg + c) * SLOT_FLOATS;
+    float *slot = a.slots + (int64_t)(rg + c) * slot_floats<MT>();
     const int rl = warp * 16 + pg;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-      __stcg(reinterpret_cast<float2 *>(slot + rl * 16 + mt * 8 + 2 * t), make_float2(acc[mt][0], acc[mt][1]));
-      __stcg(reinterpret_cast<float2 *>(slot + (rl + 8) * 16 + mt * 8 + 2 * t), make_float2(acc[mt][2], acc[mt][3]));
+      __stcg(reinterpret_cast<float2 *>(slot + rl * TSL + mt * 8 + 2 * t), make_float2(acc[mt][0], acc[mt][1]));
+      __stcg(reinterpret_cast<float2 *>(slot + (rl + 8) * TSL + mt * 8 + 2 * t), make_float2(acc[mt][2], acc[mt][3]));
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[mt][e] = 0.0f;
     }
@@ -429,6 +457,49 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     const bool ok = __all_sync(0xffffffffu, landed);
     if (ok) {
       const uint32_t wsb = stages + (uint32_t)(s * SB), xsb = wsb + W_BYTES;
+      if constexpr (MT == 4) {
+        // 32 tokens: the weights of a block (its 16 A fragments) are formed
+        // once and used for two pairs of token tiles in turn, so their cost is
+        // shared by all four tiles
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) {
+          if (b * 4 + blk >= nb_row) break;
+          const float m0 = __shfl_sync(0xffffffffu, mh[0], (g << 2) | blk);
+          const float m1 = __shfl_sync(0xffffffffu, mh[1], (g << 2) | blk);
+          const uint32_t coff = ((uint32_t)((2 * blk + (t >> 1)) ^ pg) << 4) + (uint32_t)(t & 1) * 8u;
+          const uint32_t r0 = wsb + (uint32_t)(warp * 16 + pg) * 128u + coff;
+          const uint2 wg = lds64(r0), wg8 = lds64(r0 + 8 * 128);
+          uint32_t af[4][4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t wa = (j >> 1) ? wg.y : wg.x, wb = (j >> 1) ? wg8.y : wg8.x;
+            const uint32_t s0 = 0x5504u | ((uint32_t)((j & 1) * 2) << 4), s1 = s0 + 0x10u;
+            af[j][0] = w_hat_pair(tab + prmt(wa, lanebase, s0), m0);
+            af[j][2] = w_hat_pair(tab + prmt(wa, lanebase, s1), m0);
+            af[j][1] = w_hat_pair(tab + prmt(wb, lanebase, s0), m1);
+            af[j][3] = w_hat_pair(tab + prmt(wb, lanebase, s1), m1);
+          }
+#pragma unroll
+          for (int tp = 0; tp < 2; ++tp) {
+            uint32_t xw[2][8];
+#pragma unroll
+            for (int mm = 0; mm < 2; ++mm) {
+              const int mt = 2 * tp + mm;
+              const uint32_t rowa = xsb + (uint32_t)(blk * XR * 128 + (mt * 8 + g) * 128);
+              const uint4 x0 = lds128(rowa + ((uint32_t)((2 * t) ^ g) << 4));
+              const uint4 x1 = lds128(rowa + ((uint32_t)((2 * t + 1) ^ g) << 4));
+              xw[mm][0] = x0.x; xw[mm][1] = x0.y; xw[mm][2] = x0.z; xw[mm][3] = x0.w;
+              xw[mm][4] = x1.x; xw[mm][5] = x1.y; xw[mm][6] = x1.z; xw[mm][7] = x1.w;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+              for (int mm = 0; mm < 2; ++mm)
+                mma16816(acc[2 * tp + mm], af[j][0], af[j][1], af[j][2], af[j][3], xw[mm][2 * j],
+                         xw[mm][2 * j + 1]);
+          }
+        }
+      } else {
 #pragma unroll
       for (int blk = 0; blk < 4; ++blk) {
         if (b * 4 + blk >= nb_row) break;
@@ -450,30 +521,19 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         const uint32_t coff = ((uint32_t)((2 * blk + (t >> 1)) ^ pg) << 4) + (uint32_t)(t & 1) * 8u;
         const uint32_t r0 = wsb + (uint32_t)(warp * 16 + pg) * 128u + coff;
         const uint2 wg = lds64(r0), wg8 = lds64(r0 + 8 * 128);
-        float D[MT][4];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) D[mt][e] = 0.0f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           // MMA j takes k = 16 t + 4 j + [0, 4) of this block: bytes 2j and 2j+1
           const uint32_t wa = (j >> 1) ? wg.y : wg.x, wb = (j >> 1) ? wg8.y : wg8.x;
           const uint32_t s0 = 0x5504u | ((uint32_t)((j & 1) * 2) << 4), s1 = s0 + 0x10u;
-          const uint32_t a0 = lds32(tab + prmt(wa, lanebase, s0));
-          const uint32_t a2 = lds32(tab + prmt(wa, lanebase, s1));
-          const uint32_t a1 = lds32(tab + prmt(wb, lanebase, s0));
-          const uint32_t a3 = lds32(tab + prmt(wb, lanebase, s1));
+          const uint32_t a0 = w_hat_pair(tab + prmt(wa, lanebase, s0), m0);
+          const uint32_t a2 = w_hat_pair(tab + prmt(wa, lanebase, s1), m0);
+          const uint32_t a1 = w_hat_pair(tab + prmt(wb, lanebase, s0), m1);
+          const uint32_t a3 = w_hat_pair(tab + prmt(wb, lanebase, s1), m1);
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) mma16816(D[mt], a0, a1, a2, a3, xw[mt][2 * j], xw[mt][2 * j + 1]);
+          for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt], a0, a1, a2, a3, xw[mt][2 * j], xw[mt][2 * j + 1]);
         }
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          acc[mt][0] = fmaf(D[mt][0], m0, acc[mt][0]);
-          acc[mt][1] = fmaf(D[mt][1], m0, acc[mt][1]);
-          acc[mt][2] = fmaf(D[mt][2], m1, acc[mt][2]);
-          acc[mt][3] = fmaf(D[mt][3], m1, acc[mt][3]);
-        }
+      }
       }
     }
     // stage s has been read by this warp; the last warp to finish with it
@@ -520,7 +580,7 @@ struct FinArgs {
   int nx;               // partial XA tiles
   int x_early;          // B may be read before the stream kernel completes
   int launch_early;     // the stream kernel fills every SM (see k_decode_finish)
-  const float *xap;     // [nx][16][R]
+  const float *xap;     // [nx][toks][R]
   const float *slots;   // the stream's partial tiles
   const uint16_t *B;    // [R][N]
   float scale;
@@ -528,17 +588,19 @@ struct FinArgs {
   uint16_t *XA_out;     // [M][R] bf16 or null
 };
 
-template <int NT>
+template <int MT, int NT>
 struct FinShape {
-  static constexpr int R = NT * 8, KS = (R + 15) / 16, KSC = KS < 4 ? KS : 4;  // k steps, per chunk
+  // k steps, and k steps per chunk of fragments held at once (one with 32
+  // tokens, whose XA fragments take four times the registers)
+  static constexpr int R = NT * 8, KS = (R + 15) / 16, KSC = MT == 4 ? 1 : (KS < 4 ? KS : 4);
 };
 
 // B fragments of k steps [kc0, kc0 + KSC) for the 16 rows from row0 (B is an
 // input): 8 x 8 blocks read row-wise, 4 bytes per lane, transposed later.
-template <int NT>
+template <int MT, int NT>
 __device__ __forceinline__ void load_bfrag(const FinArgs &a, int row0, int kc0,
-                                           uint32_t (&af)[FinShape<NT>::KSC][4]) {
-  constexpr int R = FinShape<NT>::R, KSC = FinShape<NT>::KSC;
+                                           uint32_t (&af)[FinShape<MT, NT>::KSC][4]) {
+  constexpr int R = FinShape<MT, NT>::R, KSC = FinShape<MT, NT>::KSC;
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 #pragma unroll
   for (int kk = 0; kk < KSC; ++kk)
@@ -549,12 +611,12 @@ __device__ __forceinline__ void load_bfrag(const FinArgs &a, int row0, int kc0,
     }
 }
 
-// XA fragments of k steps [kc0, kc0 + KSC) from shared memory ([16][R] fp32):
+// XA fragments of k steps [kc0, kc0 + KSC) from shared memory ([M][R] fp32):
 // token 8 mt + g, k pairs (16 ks + 2t, +1) and (+8, +9).
 template <int MT, int NT>
 __device__ __forceinline__ void load_xfrag(const FinArgs &a, const float *xas, int kc0,
-                                           float2 (&xf)[FinShape<NT>::KSC][MT][2]) {
-  constexpr int R = FinShape<NT>::R, KSC = FinShape<NT>::KSC;
+                                           float2 (&xf)[FinShape<MT, NT>::KSC][MT][2]) {
+  constexpr int R = FinShape<MT, NT>::R, KSC = FinShape<MT, NT>::KSC;
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 #pragma unroll
   for (int kk = 0; kk < KSC; ++kk)
@@ -569,10 +631,10 @@ __device__ __forceinline__ void load_xfrag(const FinArgs &a, const float *xas, i
 }
 
 template <int MT, int NT>
-__device__ __forceinline__ void lora_mma(float (&L)[MT][4], const uint32_t (&af)[FinShape<NT>::KSC][4],
-                                         const float2 (&xf)[FinShape<NT>::KSC][MT][2]) {
+__device__ __forceinline__ void lora_mma(float (&L)[MT][4], const uint32_t (&af)[FinShape<MT, NT>::KSC][4],
+                                         const float2 (&xf)[FinShape<MT, NT>::KSC][MT][2]) {
 #pragma unroll
-  for (int kk = 0; kk < FinShape<NT>::KSC; ++kk) {
+  for (int kk = 0; kk < FinShape<MT, NT>::KSC; ++kk) {
     const uint32_t a0 = movtrans(af[kk][0]), a1 = movtrans(af[kk][1]);
     const uint32_t a2 = movtrans(af[kk][2]), a3 = movtrans(af[kk][3]);
 #pragma unroll
@@ -592,12 +654,12 @@ __device__ __forceinline__ void lora_mma(float (&L)[MT][4], const uint32_t (&af)
 template <int MT, int NT>
 __global__ void __maxnreg__(96)
 k_decode_finish(const __grid_constant__ FinArgs a) {
-  constexpr int R = NT * 8, KS = FinShape<NT>::KS, KSC = FinShape<NT>::KSC;
-  __shared__ __align__(16) float xas[16 * R];
+  constexpr int R = NT * 8, KS = FinShape<MT, NT>::KS, KSC = FinShape<MT, NT>::KSC, TSL = toks<MT>();
+  __shared__ __align__(16) float xas[TSL * R];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int rowc = blockIdx.x * FIN_ROWS + warp * 32;  // this warp's first row
   uint32_t af0[KSC][4];
-  if (a.x_early) load_bfrag<NT>(a, rowc, 0, af0);
+  if (a.x_early) load_bfrag<MT, NT>(a, rowc, 0, af0);
   // The next call may start once this kernel has waited for the stream kernel
   // (and so for every grid before it).  When the stream kernel has a CTA on
   // every SM it may start at once instead: its CTAs (too large to share an SM
@@ -608,7 +670,7 @@ k_decode_finish(const __grid_constant__ FinArgs a) {
   if (a.launch_early) ptx::griddep_launch();
   ptx::griddep_wait();  // the stream kernel, and every grid before it, completed
   if (!a.launch_early) ptx::griddep_launch();
-  if (!a.x_early) load_bfrag<NT>(a, rowc, 0, af0);
+  if (!a.x_early) load_bfrag<MT, NT>(a, rowc, 0, af0);
   {
     // XA = the partial tiles added in tile order, in two steps: thread t adds
     // tiles zc, zc + zg, ... (zc = t / MR4, zg = 128 / MR4 groups) of element
@@ -621,7 +683,7 @@ k_decode_finish(const __grid_constant__ FinArgs a) {
       if (zc < zg) {
 #pragma unroll 8
         for (int z = zc; z < a.nx; z += zg) {
-          const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.xap + (int64_t)z * 16 * R) + i);
+          const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.xap + (int64_t)z * TSL * R) + i);
           sacc.x += v.x;
           sacc.y += v.y;
           sacc.z += v.z;
@@ -646,7 +708,7 @@ k_decode_finish(const __grid_constant__ FinArgs a) {
         float4 s4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll 8
         for (int z = 0; z < a.nx; ++z) {
-          const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.xap + (int64_t)z * 16 * R) + i);
+          const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.xap + (int64_t)z * TSL * R) + i);
           s4.x += v.x;
           s4.y += v.y;
           s4.z += v.z;
@@ -668,17 +730,17 @@ k_decode_finish(const __grid_constant__ FinArgs a) {
   for (int tile = 0; tile < 2; ++tile) {
     const int row0 = rowc + tile * 16;
     if (row0 >= a.N) break;  // N % 8 == 0: rows g of a live tile are valid
-    if (tile) load_bfrag<NT>(a, row0, 0, af0);
+    if (tile) load_bfrag<MT, NT>(a, row0, 0, af0);
     const int rg = row0 / UNIT_ROWS;
     const int rowg = row0 + g, rowg8 = rowg + 8;
     const bool vg8 = rowg8 < a.N;
     const int cf = cta_of((int64_t)rg * a.nbox, a.G, a.W), cl = cta_of((int64_t)(rg + 1) * a.nbox - 1, a.G, a.W);
     const int rl = row0 - rg * UNIT_ROWS + g;
-    const float *base = a.slots + (int64_t)(rg + cf) * SLOT_FLOATS;
+    const float *base = a.slots + (int64_t)(rg + cf) * slot_floats<MT>();
     float2 sm[MT][2];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) sm[mt][0] = sm[mt][1] = make_float2(0.0f, 0.0f);
-    constexpr int ZB = MT == 1 ? 8 : 4;  // partial tiles loaded per batch
+    constexpr int ZB = MT == 1 ? 8 : (MT == 2 ? 4 : 2);  // partial tiles loaded per batch
 #pragma unroll 1
     for (int z0 = 0; z0 <= cl - cf; z0 += ZB) {
       float2 v[ZB][MT][2];
@@ -687,9 +749,9 @@ k_decode_finish(const __grid_constant__ FinArgs a) {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           const bool in = z0 + dz <= cl - cf;
-          const float *pz = base + (int64_t)(z0 + dz) * SLOT_FLOATS + mt * 8 + 2 * t;
-          v[dz][mt][0] = in ? __ldcg(reinterpret_cast<const float2 *>(pz + rl * 16)) : make_float2(0.0f, 0.0f);
-          v[dz][mt][1] = in ? __ldcg(reinterpret_cast<const float2 *>(pz + (rl + 8) * 16)) : make_float2(0.0f, 0.0f);
+          const float *pz = base + (int64_t)(z0 + dz) * slot_floats<MT>() + mt * 8 + 2 * t;
+          v[dz][mt][0] = in ? __ldcg(reinterpret_cast<const float2 *>(pz + rl * TSL)) : make_float2(0.0f, 0.0f);
+          v[dz][mt][1] = in ? __ldcg(reinterpret_cast<const float2 *>(pz + (rl + 8) * TSL)) : make_float2(0.0f, 0.0f);
         }
 #pragma unroll
       for (int dz = 0; dz < ZB; ++dz)
@@ -712,7 +774,7 @@ k_decode_finish(const __grid_constant__ FinArgs a) {
 #pragma unroll
     for (int kc0 = KSC; kc0 < KS; kc0 += KSC) {
       uint32_t af[KSC][4];
-      load_bfrag<NT>(a, row0, kc0, af);
+      load_bfrag<MT, NT>(a, row0, kc0, af);
       load_xfrag<MT, NT>(a, xas, kc0, xf);
       lora_mma<MT, NT>(L, af, xf);
     }
@@ -776,7 +838,7 @@ int make_tmaps(CUtensorMap *tw, CUtensorMap *tx, const uint8_t *packed, int64_t 
 
 struct DevInfo {
   int sms = 0;
-  bool attr[2][5] = {};
+  bool attr[3][5] = {};
 };
 DevInfo &dev_info(int dev) {
   static DevInfo info[64];
@@ -790,8 +852,8 @@ struct WsLayout {
 WsLayout ws_layout(int64_t N, int r) {
   const size_t groups = (size_t)((N + UNIT_ROWS - 1) / UNIT_ROWS);
   WsLayout l{};
-  l.slots = up256((size_t)G_MAX * 16 * r * 4);
-  l.total = l.slots + (groups + G_MAX) * SLOT_FLOATS * 4;
+  l.slots = up256((size_t)G_MAX * MAX_TOKS * r * 4);
+  l.total = l.slots + (groups + G_MAX) * (size_t)UNIT_ROWS * MAX_TOKS * 4;
   return l;
 }
 
@@ -804,7 +866,8 @@ int max_carveout(F *fn) {
 
 template <int MT, int NT>
 int launch_t(const DecodeProblem &p, StreamArgs &a, FinArgs &f, int G, DevInfo &di, int ti, cudaStream_t st) {
-  if (!di.attr[MT - 1][ti]) {
+  constexpr int mi = MT == 4 ? 2 : MT - 1;
+  if (!di.attr[mi][ti]) {
     int rc = check_cuda(cudaFuncSetAttribute(k_decode_stream<MT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)dec_smem<MT, NT>()),
                         "decode: shared-memory attribute");
@@ -812,7 +875,7 @@ int launch_t(const DecodeProblem &p, StreamArgs &a, FinArgs &f, int G, DevInfo &
     if (!rc) rc = max_carveout(k_decode_stream<MT, NT>);
     if (!rc) rc = max_carveout(k_decode_finish<MT, NT>);
     if (rc) return rc;
-    di.attr[MT - 1][ti] = true;
+    di.attr[mi][ti] = true;
   }
   a.kc = xa_kc<NT>();
   // CTAs computing partial XA tiles: enough that each stages one chunk, at least 32
@@ -896,11 +959,12 @@ int launch_decode(const DecodeProblem &p, cudaStream_t st, bool *early_dependent
   *early_dependents = f.launch_early;
   f.xap = a.xap; f.slots = a.slots;
   f.B = p.B; f.scale = p.scale; f.Y = p.Y; f.XA_out = p.XA_out;
-  const bool mt2 = p.M > 8;
-  switch (p.r * 4 + (mt2 ? 2 : 1)) {
+  const int mt = p.M <= 8 ? 1 : (p.M <= 16 ? 2 : 4);  // token tiles of 8
+  switch (p.r * 8 + mt) {
 #define QL_DEC(R_, TI_)                                                 \
-  case R_ * 4 + 1: return launch_t<1, R_ / 8>(p, a, f, G, di, TI_, st); \
-  case R_ * 4 + 2: return launch_t<2, R_ / 8>(p, a, f, G, di, TI_, st);
+  case R_ * 8 + 1: return launch_t<1, R_ / 8>(p, a, f, G, di, TI_, st); \
+  case R_ * 8 + 2: return launch_t<2, R_ / 8>(p, a, f, G, di, TI_, st); \
+  case R_ * 8 + 4: return launch_t<4, R_ / 8>(p, a, f, G, di, TI_, st);
     QL_DEC(8, 0) QL_DEC(16, 1) QL_DEC(32, 2) QL_DEC(64, 3) QL_DEC(128, 4)
 #undef QL_DEC
     default: return set_error(QL_ERR_UNSUPPORTED, "decode: rank %d", p.r);

@@ -5,7 +5,7 @@
 namespace ql {
 
 struct DecodeProblem {
-  const uint16_t *X;  // M x K bf16, M <= 16
+  const uint16_t *X;  // M x K bf16, M <= 32
   int64_t M, K, N;
   NF4View w;          // N x K
   const uint16_t *A;  // K x r

@@ -1,12 +1,12 @@
 // Forward and backward of the frozen-NF4 linear with a LoRA adapter:
 // argument checks, workspace layout and the launch sequence on one stream.
 //
-// forward, M > 16 tokens (2 launches; 3 for M <= 128):
+// forward, M > 32 tokens (2 launches; 3 for M <= 128):
 //   1. XA = X A  -> XA_out (bf16) and XAs = bf16(s XA)     LoRA kernel
 //   2. Y  = X W_hat^T + XAs B                             tensor-core GEMM,
 //                                                          LoRA as extra K-steps
 //      (M <= 128: the few-token kernel, skinny.cu, and its fixup kernel)
-// forward, M <= 16: the decode path (decode.cu).
+// forward, M <= 32: the decode path (decode.cu).
 // backward (4 launches, 5 when XA must be recomputed):
 //   0. XA = X A                                            (only without XA)
 //   1. Gs = bf16(s dY B^T)                                  LoRA kernel
@@ -69,13 +69,9 @@ int check_common(const LinearArgs &a, const char *fn, size_t need) {
     if (rc_) return rc_;     \
   } while (0)
 
-constexpr int64_t kDecodeMaxM = 16;  // M at or below this takes the decode path
-// 17 to kSliceMaxM tokens run as slices of kDecodeMaxM tokens through the
-// decode path (one weight stream per slice): measured faster than the
-// few-token tensor-core kernel there (LLaMA-13B shapes, M = 32: 24.7 / 36.2 /
-// 44.6 us for two slices against 28.3 / 56.3 / 59.1 us); above it the
-// few-token kernel is faster
-constexpr int64_t kSliceMaxM = 32;
+// M at or below this takes the decode path (the weight-streaming kernel with
+// 8, 16 or 32 token columns); above it the few-token tensor-core kernel
+constexpr int64_t kDecodeMaxM = 32;
 
 // ---------------------------------------------------------------------------
 // What the previous library call on a stream may still be reading or writing.
@@ -200,7 +196,7 @@ void note_other_call(cudaStream_t st) { note_call(st, false, {}); }
 
 size_t linear_fwd_ws(int64_t M, int64_t N, int64_t K, int32_t r) {
   if (M <= 0 || N <= 0 || K <= 0 || !rank_ok(r)) return 0;
-  if (M <= kSliceMaxM) return decode_ws(N, K, r);
+  if (M <= kDecodeMaxM) return decode_ws(N, K, r);
   return fwd_ws(M, N, K, r);
 }
 
@@ -216,18 +212,6 @@ int linear_fwd(const LinearArgs &a) {
     return set_error(QL_ERR_MISALIGNED, "%s: operand not 16-byte aligned", fn);
   const int64_t M = a.M, N = a.W.rows, K = a.W.cols;
   const int r = a.r;
-  if (M > kDecodeMaxM && M <= kSliceMaxM) {  // token slices through the decode path
-    QL_TRY(check_common(a, fn, decode_ws(N, K, r)));
-    for (int64_t m0 = 0; m0 < M; m0 += kDecodeMaxM) {
-      LinearArgs sl = a;
-      sl.M = std::min(kDecodeMaxM, M - m0);
-      sl.X = a.X + m0 * K;
-      sl.Y = a.Y + m0 * N;
-      sl.XA = a.XA ? a.XA + m0 * r : nullptr;
-      QL_TRY(linear_fwd(sl));
-    }
-    return QL_OK;
-  }
   if (M >= 1 && M <= kDecodeMaxM) {
     QL_TRY(check_common(a, fn, decode_ws(N, K, r)));
     DecodeProblem d{};

@@ -262,9 +262,10 @@ QL_API int nf4_dequantize(const ql_nf4_tensor *q, uint16_t *W_out, ql_stream_t s
  *            backward pass.
  *   scale  : s = alpha / r.
  *   ws     : ql_workspace_size(QL_OP_LINEAR_FWD, M, N, K, r) bytes.
- * M >= 1.  M <= 16 takes the decode (weight-streaming) path, 17 <= M <= 32
- * runs as 16-token slices through it, larger M the tensor-core path (the
- * few-token kernel up to 128 tokens, the CTA-pair kernel above).
+ * M >= 1.  M <= 32 takes the decode (weight-streaming) path, larger M the
+ * tensor-core path (the few-token kernel up to 128 tokens, the CTA-pair
+ * kernel above).  Every path multiplies by the dequantized weight W_hat bit
+ * for bit; results differ only in the order of the fp32 sums.
  * The decode path keeps partial results in `ws` (any initial contents work);
  * successive decode calls on a stream alternate between its two halves, so a
  * call may start while the previous one finishes.

@@ -48,7 +48,7 @@ def test_workspace_sizes(ql):
     assert ql.workspace_size(ql.OP_QUANTIZE, 0, 4096, 4096, 0) >= 4096 * 4096 // 64 * 4
     assert ql.workspace_size(ql.OP_DEQUANTIZE, 0, 4096, 4096, 0) == 0
     assert ql.workspace_size(99) == 2 ** 64 - 1
-    # 17-32 tokens run as 16-token decode slices: the decode workspace
+    # up to 32 tokens take the decode path and its workspace
     fwd = lambda M: ql.workspace_size(ql.OP_LINEAR_FWD, M, 5120, 5120, 64)
     assert fwd(17) == fwd(32) == fwd(16) == fwd(1) and fwd(33) != fwd(32)
     # the E4M3 calls keep two halves, each holding the M x K (forward) or

@@ -1,16 +1,14 @@
-"""GPU parity of the decode-sized forward (M <= 16 tokens) against the fp64
-oracle.  The decode path applies each block constant to fp32 partial sums of
-x * bf16(q[code]) instead of using bf16(q[code] * constant) per weight; the
-difference is at most one bf16 step per weight (pinned bit for bit by one-hot
-tokens below) and the outputs stay inside the path's tolerance against the
-oracle on w_hat (relative Frobenius error <= 5e-3,
-|err| <= 1e-2 (|ref| + rms(ref)))."""
+"""GPU parity of the decode-sized forward (M <= 32 tokens) against the fp64
+oracle.  The decode path forms every weight as the dequantized value
+w_hat = bf16(fl32(q[c] * m_hat)) (pinned bit for bit by one-hot tokens below)
+and accumulates in fp32, so its outputs differ from the oracle's only by the
+order of the fp32 sums and the bf16 rounding of Y; the bar is the path's
+tolerance (relative Frobenius error <= 5e-3, |err| <= 1e-2 (|ref| + rms(ref)))."""
 import numpy as np
 import pytest
 import torch
 
 from oracle import linear, nf4
-from oracle.bf16 import bf16_bits_to_f32, f32_to_bf16_bits
 from parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -47,6 +45,9 @@ def reference(W, X, A, B, s, dq=256):
     (4096, 128, 7, 64), (256, 8192, 12, 64), (1536, 2048, 2, 16), (776, 1088, 5, 64), (512, 768, 8, 8),
     # K long enough that each XA CTA stages its slice of A in several chunks
     (256, 19968, 3, 64), (256, 20032, 1, 64), (512, 10240, 16, 128), (512, 40960, 4, 64),
+    # 17-32 tokens: four 8-token tiles per pass, ragged last tile
+    (1032, 576, 17, 128), (520, 4160, 32, 32), (776, 1088, 25, 64), (4096, 128, 24, 64),
+    (256, 20032, 32, 64), (64, 64, 31, 16), (1536, 2048, 20, 8),
 ])
 def test_decode_ragged_shapes(ql, N, K, M, r):
     from bit_nf4_quantized_38_b300.workloads import normal_bf16, normal_with_outliers_bf16
@@ -73,7 +74,7 @@ def test_decode_double_quant_off(ql):
     assert_close("decode Y dq off", Y.float().cpu().numpy(), Yr)
 
 
-@pytest.mark.parametrize("M", [1, 4, 16])
+@pytest.mark.parametrize("M", [1, 4, 16, 32])
 @pytest.mark.parametrize("idx", [0, 1, 2])
 def test_decode_llama13b_full_size(ql, idx, M):
     """LLaMA-13B shapes (5120x5120, 13824x5120, 5120x13824), r = 64: every output checked."""
@@ -169,27 +170,20 @@ def test_decode_graph_replays_reuse_the_workspace(ql):
 
 
 @pytest.mark.parametrize("dq", [256, 0])
-@pytest.mark.parametrize("M", [16, 1])
+@pytest.mark.parametrize("M", [32, 16, 1])
 def test_decode_weight_values_one_hot(ql, M, dq):
     """The decode path's per-weight value, read out bit for bit: with B = 0 and
-    one-hot token rows, Y[m, n] is the decode weight of (n, k_m), i.e.
-    bf16(fl32(bf16(q[c]) * m_hat)) -- the block constant applied in fp32 to
-    the bf16-rounded level -- and it lies within one bf16 step of the
-    oracle's w_hat = bf16(fl32(q[c] * m_hat))."""
+    one-hot token rows, Y[m, n] is the weight of (n, k_m) that the path used,
+    which must be the oracle's dequantized w_hat = bf16(fl32(q[c] * m_hat))."""
     from bit_nf4_quantized_38_b300.workloads import normal_with_outliers_bf16
     dev = torch.device("cuda")
     N, K, r = 264, 512, 8
     W = normal_with_outliers_bf16((N, K), 0.02, 0.001, 20.0, 81 + dq)
-    ref = nf4.quantize(bits(W), dq_blocksize=dq)
-    Wh = nf4.dequantize(ref)
-    codes = nf4.unpack_nibbles(ref["packed"]).reshape(N, K)
-    mh = np.repeat(nf4.absmax_hat(ref).reshape(N, K // 64), 64, axis=1)
-    lv = bf16_bits_to_f32(f32_to_bf16_bits(nf4.nf4_levels()))
-    expect = f32_to_bf16_bits((lv[codes] * mh).astype(np.float32))
+    Wh = nf4.dequantize(nf4.quantize(bits(W), dq_blocksize=dq))
     q = ql.nf4_quantize(W.to(dev), dq_blocksize=dq)
     A = torch.randn(K, r, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16).to(dev)
     Bz = torch.zeros(r, N, dtype=torch.bfloat16, device=dev)
-    ks = np.arange(K) if M == 16 else np.array([0, 1, 63, 64, 200, 255, 256, 511])
+    ks = np.arange(K) if M > 1 else np.array([0, 1, 63, 64, 200, 255, 256, 511])
     got = np.empty((ks.size, N), dtype=np.uint16)
     for i0 in range(0, ks.size, M):
         sel = ks[i0:i0 + M]
@@ -199,11 +193,4 @@ def test_decode_weight_values_one_hot(ql, M, dq):
         got[i0:i0 + sel.size] = bits(Y)[:sel.size]
     torch.cuda.synchronize()
     ql.device_status()
-    assert np.array_equal(got, expect.T[ks])
-    # adjacent or equal bf16 values of one sign: bit patterns at most 1 apart
-    wh = Wh.T[ks].astype(np.int32)
-    g = got.astype(np.int32)
-    assert np.all((g >> 15) == (wh >> 15))
-    steps = np.abs(g - wh)
-    assert steps.max() <= 1
-    print(f"decode weights one bf16 step from w_hat: {np.mean(steps):.4f} of {steps.size}")
+    assert np.array_equal(got, Wh.T[ks])

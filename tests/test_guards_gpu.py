@@ -67,8 +67,8 @@ def guarded_nf4(ql, g, rows, cols, dq):
 @pytest.mark.parametrize("N,K,M,r,dq", [
     (328, 320, 200, 16, 256),   # ragged tensor-core tiles
     (1032, 576, 1100, 128, 256),  # CTA-pair tiles, partial pair, rank 128
-    (264, 640, 17, 8, 0),       # 17 tokens: decode slices of 16 and 1, DQ off
-    (264, 640, 40, 8, 0),       # few-token forward just past the slice limit, DQ off
+    (264, 640, 17, 8, 0),       # 17 tokens: the decode path's 32-token pass, DQ off
+    (264, 640, 40, 8, 0),       # few-token forward past the decode limit, DQ off
     (1032, 576, 100, 128, 256), # few-token forward: ragged tile, shared tiles, rank 128
     (520, 4160, 16, 32, 256),   # decode path, long K
     (776, 1088, 5, 8, 256),     # decode path, ragged N

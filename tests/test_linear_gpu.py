@@ -70,8 +70,8 @@ SHAPES = [
     (328, 320, 600, 16),    # CTA-pair tiles, ragged
     (1032, 576, 1100, 32),  # CTA-pair tiles, partial pair in N and M
     (520, 448, 300, 8),     # rank 8 on the tensor-core forward path
-    (264, 640, 17, 64),     # 17 tokens: decode slices of 16 and 1 (forward)
-    (264, 640, 33, 64),     # one token past the slice limit: the few-token kernel
+    (264, 640, 17, 64),     # 17 tokens: the decode path's 32-token pass (forward)
+    (264, 640, 33, 64),     # one token past the decode limit: the few-token kernel
 ]
 
 
@@ -268,7 +268,7 @@ def test_back_to_back_independent_calls_equal_synchronised_calls(ql):
 @pytest.mark.parametrize("N,K,M,r", [(1032, 576, 1100, 32), (264, 640, 17, 64), (520, 1088, 9, 16)])
 def test_fp4_weights_forward_backward(ql, N, K, M, r):
     """The same layer with FP4-coded weights (tensor-core path and, for
-    M <= 16, the decode path): within tolerance of the oracle on the FP4
+    M <= 32, the decode path): within tolerance of the oracle on the FP4
     dequantized weight."""
     W, X, A, B, dY, s = make_case(N, K, M, r, seed=N + M + 3)
     dev = torch.device("cuda")

@@ -1,6 +1,6 @@
 """GPU parity of the few-token forward (32 < M <= 128 tokens: the transposed
 tensor-core product split over all SMs, csrc/skinny.cu; and 17-32 tokens, run
-as 16-token slices through the decode path) against the fp64 oracle.
+by the decode path in one 32-token pass) against the fp64 oracle.
 
 Same tolerance as the other GEMM results (relative Frobenius <= 5e-3,
 |err| <= 1e-2 (|ref| + rms(ref)) per element, fp32 accumulation on the same
@@ -52,8 +52,8 @@ SHAPES = [
     (776, 1088, 64, 32, 0, 0),      # double quantization off
     (520, 1088, 48, 16, 256, 1),    # FP4 code table, Mp = 64
     (136, 4160, 34, 64, 256, 0),    # two tiles, long reduction: many CTAs share each tile
-    (1032, 576, 17, 128, 256, 0),   # 17 tokens: a 16-token and a 1-token slice (decode path)
-    (776, 1088, 32, 32, 0, 0),      # 32 tokens: two 16-token slices, double quantization off
+    (1032, 576, 17, 128, 256, 0),   # 17 tokens: the decode path's 32-token pass, 15 empty columns
+    (776, 1088, 32, 32, 0, 0),      # 32 tokens (decode path), double quantization off
 ]
 
 
@@ -97,7 +97,7 @@ def test_in_kernel_dequant_is_bit_exact(ql, N, K, M):
 @pytest.mark.parametrize("idx,M", [(0, 128), (1, 128), (2, 128), (1, 48), (1, 32)])
 def test_llama13b_full_size(ql, idx, M):
     """LLaMA-13B shapes (5120^2, 13824x5120, 5120x13824), r = 64, checked in
-    full against the oracle (M = 32: two decode slices)."""
+    full against the oracle (M = 32: the decode path)."""
     from bit_nf4_quantized_38_b300.workloads import case_inputs, case_weight, llama13b_decode
     case = llama13b_decode(M=M).cases[idx]
     W = case_weight(case)
