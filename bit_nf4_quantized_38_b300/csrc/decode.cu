@@ -13,13 +13,13 @@
 //                    (rows past M zero filled).  The first units are loaded
 //                    at the start, each later one by the last warp to finish
 //                    with a stage.  Warp w owns rows 16 w .. 16 w + 15 of the
-//                    unit: every packed byte (two codes) is looked up in a
-//                    256-entry table of fp32 level pairs kept once per lane
-//                    in shared memory (one byte permute forms the lookup
-//                    address, and lookups never conflict on a bank); each
-//                    level times the block constant, rounded to bf16, is the
-//                    dequantized weight, and warp MMAs m16n8k16 with weight
-//                    rows as M and tokens as N accumulate in fp32.  When a
+//                    unit, and lane t of a row the unit's 64-block t (the
+//                    order of K within a unit is permuted alike for the
+//                    weight and X): per unit a lane forms its two rows' 16
+//                    dequantized values bf16(fl32(q[c] * m_hat)) once, in
+//                    registers, and expands every 8 packed codes through them
+//                    with byte permutes; warp MMAs m16n8k16 with weight rows
+//                    as M and tokens as N accumulate in fp32.  When a
 //                    CTA leaves a row group it stores its partial tile to the
 //                    group's slot for that CTA.  Before streaming, the first
 //                    NX CTAs stage their share of the K rows of A and X (bulk
@@ -51,6 +51,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "convert.cuh"
 #include "decode.cuh"
 #include "ptx.cuh"
 
@@ -63,7 +64,7 @@ constexpr int ST_STAGES = 3;                  // ring stages (two with 32 tokens
 constexpr int UNIT_ROWS = 256;                // rows per unit
 constexpr int UNIT_K = 256;                   // K values per unit (128 packed bytes per row)
 constexpr int W_BYTES = UNIT_ROWS * 128;      // packed box of a unit
-constexpr int TAB_BYTES = 256 * 256;          // 256 entries x 256 B (32 lanes x an fp32 pair)
+constexpr int TAB_BYTES = 256 * 256;          // level table (one token tile): 256 entries x 32 lanes x 8 B
 constexpr int PD = 2;                         // units of block constants loaded ahead
 constexpr int G_MAX = 160;                    // persistent CTAs at most (one per SM)
 constexpr int MAX_TOKS = 32;                  // tokens of the largest variant (MT = 4)
@@ -71,6 +72,10 @@ constexpr int XA_A_BYTES = 16384;             // staged rows of A per chunk, at 
 constexpr int XA_KC_MAX = 256;
 constexpr int FIN_WARPS = 4;                  // finishing kernel: 4 warps x 32 rows
 constexpr int FIN_ROWS = FIN_WARPS * 32;
+// registers of a stream CTA (THREADS threads at the 96-register cap): two never
+// fit on one SM (65536 registers), a stream CTA and a finishing CTA do
+constexpr int kStreamRegs = THREADS * 96;
+static_assert(2 * kStreamRegs > 65536 && kStreamRegs + FIN_WARPS * 32 * 96 <= 65536, "decode CTA residency");
 
 template <int MT>
 constexpr int stage_bytes() { return W_BYTES + 4 * (MT * 8) * 128; }
@@ -91,7 +96,7 @@ constexpr int xa_smem() {  // A chunk, X chunk (toks<MT> rows)
 }
 template <int MT, int NT>
 constexpr size_t dec_smem() {
-  return (size_t)TAB_BYTES + 1024 + (size_t)st_stages<MT>() * stage_bytes<MT>() + (size_t)xa_smem<MT, NT>();
+  return (MT == 1 ? TAB_BYTES : 0) + 1024 + (size_t)st_stages<MT>() * stage_bytes<MT>() + (size_t)xa_smem<MT, NT>();
 }
 // room for a finishing CTA (8 KB of XA, 1 KB reserved) beside a stream CTA in 228 KB
 static_assert(dec_smem<2, 16>() + 1024 + 8192 + 1024 <= 228 * 1024, "decode shared memory");
@@ -136,6 +141,19 @@ __device__ __forceinline__ uint32_t w_hat_pair(uint32_t addr, float m) {
   const uint2 v = lds64(addr);
   return pack_bf16x2(__fmul_rn(__uint_as_float(v.x), m), __fmul_rn(__uint_as_float(v.y), m));
 }
+// The 16 dequantized values bf16(fl32(q[c] * m)) of a row-block with block
+// constant m, as low-byte (TL) and high-byte (TH) planes: entry c in byte
+// c % 4 of word c / 4 (the table lookup8 reads).
+__device__ __forceinline__ void w_hat_planes(const float (&q)[16], float m, uint32_t (&TL)[4], uint32_t (&TH)[4]) {
+  uint32_t P[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) P[k] = pack_bf16x2(__fmul_rn(q[2 * k], m), __fmul_rn(q[2 * k + 1], m));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    TL[i] = prmt(P[2 * i], P[2 * i + 1], 0x6420u);
+    TH[i] = prmt(P[2 * i], P[2 * i + 1], 0x7531u);
+  }
+}
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
@@ -149,15 +167,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                : "memory");
 }
 
-// Wait for phase `parity` of a barrier for at most `limit_ns`, ignoring any
-// abort flag: lets copies already in flight land before a CTA that gave up
-// exits.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 100000000ull) {
-  const uint64_t t0 = ptx::globaltimer();
-#pragma unroll 1
-  while (!ptx::mbar_try_wait(bar, parity) && ptx::globaltimer() - t0 < limit_ns) {
-  }
-}
 
 struct StreamArgs {  // N K / 64 < 2^31 and units < 2^31 (checked on the host)
   int M, K, N;
@@ -279,8 +288,9 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
   __shared__ unsigned released[ST_STAGES];  // warps done with the stage's current unit
   __shared__ int abort_flag, xa_chunks;
   volatile int *abort_v = &abort_flag;
-  const uint32_t tab = ptx::smem_u32(smem);  // the lookup table sits at the start
-  const uint32_t stages = (tab + TAB_BYTES + 1023u) & ~1023u;
+  // with one token tile the fp32 level table sits at the start
+  const uint32_t tab = ptx::smem_u32(smem);
+  const uint32_t stages = (tab + (MT == 1 ? TAB_BYTES : 0) + 1023u) & ~1023u;
   const uint32_t xa_base = stages + (uint32_t)(ST_STAGES * SB);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, c = blockIdx.x;
@@ -338,7 +348,7 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     if (!a.x_early) ptx::griddep_wait();
     xa_issue<NT>(a, xa_base, ptx::smem_u32(&xa_bar), 0);
   }
-  {
+  if constexpr (MT == 1) {
     // entry e (a packed byte), lane l: the fp32 levels (q[e >> 4], q[e & 15])
     // at byte 256 e + 8 l; the high nibble is element 2j, the lower k of the
     // MMA pair
@@ -450,6 +460,14 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     for (int k = 0; k < 2; ++k)
       mh[k] = a.dq ? __fadd_rn(__fmul_rn(dq_code_value((int8_t)pre.c[k], a.dqt), pre.b[k]), mu) : pre.a[k];
     pre = load_pre(i + PD);
+    // two or four token tiles: the lane's two rows' dequantized values in
+    // block t (TL0/TH0: row pg, TL1/TH1: row pg + 8), formed while the stage
+    // may still be loading
+    uint32_t TL0[4], TH0[4], TL1[4], TH1[4];
+    if constexpr (MT > 1) {
+      w_hat_planes(a.q, mh[0], TL0, TH0);
+      w_hat_planes(a.q, mh[1], TL1, TH1);
+    }
 
     bool landed = false;
     if (!*abort_v)
@@ -457,37 +475,40 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     const bool ok = __all_sync(0xffffffffu, landed);
     if (ok) {
       const uint32_t wsb = stages + (uint32_t)(s * SB), xsb = wsb + W_BYTES;
+      // Two or four token tiles, step blk: lane t takes K values 16 sg ..
+      // 16 sg + 15 of block t, sg = blk ^ t, and its X fragments the same K
+      // values (the reduction order is a permutation of the unit's K, the
+      // same for both operands).  The packed bytes are 8-byte piece sg of
+      // block t's 32 (16-byte chunk 2 t + sg / 2 of the row, at chunk ^ (row
+      // mod 8)); X is chunks 2 sg, 2 sg + 1 of block t's 128-byte token row,
+      // at chunk ^ (row mod 8).  sg is a Latin square in (t, blk), so no load
+      // of a step conflicts on a bank.  Past the row's last block (a ragged
+      // unit) the weight and X boxes are zero filled, so those lanes add zero
+      // products.
       if constexpr (MT == 4) {
-        // 32 tokens: the weights of a block (its 16 A fragments) are formed
+        // 32 tokens: the weights of a step (its 16 A fragments) are formed
         // once and used for two pairs of token tiles in turn, so their cost is
         // shared by all four tiles
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {
-          if (b * 4 + blk >= nb_row) break;
-          const float m0 = __shfl_sync(0xffffffffu, mh[0], (g << 2) | blk);
-          const float m1 = __shfl_sync(0xffffffffu, mh[1], (g << 2) | blk);
-          const uint32_t coff = ((uint32_t)((2 * blk + (t >> 1)) ^ pg) << 4) + (uint32_t)(t & 1) * 8u;
+          const int sg = blk ^ t;
+          const uint32_t coff = ((uint32_t)((2 * t + (sg >> 1)) ^ pg) << 4) + (uint32_t)(sg & 1) * 8u;
           const uint32_t r0 = wsb + (uint32_t)(warp * 16 + pg) * 128u + coff;
           const uint2 wg = lds64(r0), wg8 = lds64(r0 + 8 * 128);
           uint32_t af[4][4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t wa = (j >> 1) ? wg.y : wg.x, wb = (j >> 1) ? wg8.y : wg8.x;
-            const uint32_t s0 = 0x5504u | ((uint32_t)((j & 1) * 2) << 4), s1 = s0 + 0x10u;
-            af[j][0] = w_hat_pair(tab + prmt(wa, lanebase, s0), m0);
-            af[j][2] = w_hat_pair(tab + prmt(wa, lanebase, s1), m0);
-            af[j][1] = w_hat_pair(tab + prmt(wb, lanebase, s0), m1);
-            af[j][3] = w_hat_pair(tab + prmt(wb, lanebase, s1), m1);
-          }
+          lookup8(wg.x, TL0, TH0, af[0][0], af[0][2], af[1][0], af[1][2]);
+          lookup8(wg.y, TL0, TH0, af[2][0], af[2][2], af[3][0], af[3][2]);
+          lookup8(wg8.x, TL1, TH1, af[0][1], af[0][3], af[1][1], af[1][3]);
+          lookup8(wg8.y, TL1, TH1, af[2][1], af[2][3], af[3][1], af[3][3]);
 #pragma unroll
           for (int tp = 0; tp < 2; ++tp) {
             uint32_t xw[2][8];
 #pragma unroll
             for (int mm = 0; mm < 2; ++mm) {
               const int mt = 2 * tp + mm;
-              const uint32_t rowa = xsb + (uint32_t)(blk * XR * 128 + (mt * 8 + g) * 128);
-              const uint4 x0 = lds128(rowa + ((uint32_t)((2 * t) ^ g) << 4));
-              const uint4 x1 = lds128(rowa + ((uint32_t)((2 * t + 1) ^ g) << 4));
+              const uint32_t rowa = xsb + (uint32_t)(t * XR * 128 + (mt * 8 + g) * 128);
+              const uint4 x0 = lds128(rowa + ((uint32_t)((2 * sg) ^ g) << 4));
+              const uint4 x1 = lds128(rowa + ((uint32_t)((2 * sg + 1) ^ g) << 4));
               xw[mm][0] = x0.x; xw[mm][1] = x0.y; xw[mm][2] = x0.z; xw[mm][3] = x0.w;
               xw[mm][4] = x1.x; xw[mm][5] = x1.y; xw[mm][6] = x1.z; xw[mm][7] = x1.w;
             }
@@ -499,41 +520,64 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
                          xw[mm][2 * j + 1]);
           }
         }
-      } else {
+      } else if constexpr (MT == 1) {
+        // One token tile: few X loads, so the level table in shared memory
+        // (8 B per lookup) costs less than the register planes' byte permutes.
+        // Step blk is block blk of the unit and lane t takes its K values
+        // 16 t .. 16 t + 15 (chunks 2 blk + t / 2 of the packed row, 2t and
+        // 2t + 1 of the X row); the block constants come from lane 4 g + blk.
 #pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {
-        if (b * 4 + blk >= nb_row) break;
-        // X fragments of block blk: token rows 8 mt + xg, K values 16 t .. 16 t + 15
-        // (16-byte chunks 2t, 2t+1 of the 128-byte row, swizzled by row mod 8)
-        uint32_t xw[MT][8];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          const uint32_t rowa = xsb + (uint32_t)(blk * XR * 128 + (mt * 8 + xg) * 128);
+        for (int blk = 0; blk < 4; ++blk) {
+          if (b * 4 + blk >= nb_row) break;
+          const uint32_t rowa = xsb + (uint32_t)(blk * XR * 128 + xg * 128);
           const uint4 x0 = lds128(rowa + ((uint32_t)((2 * t) ^ xg) << 4));
           const uint4 x1 = lds128(rowa + ((uint32_t)((2 * t + 1) ^ xg) << 4));
-          xw[mt][0] = x0.x; xw[mt][1] = x0.y; xw[mt][2] = x0.z; xw[mt][3] = x0.w;
-          xw[mt][4] = x1.x; xw[mt][5] = x1.y; xw[mt][6] = x1.z; xw[mt][7] = x1.w;
-        }
-        const float m0 = __shfl_sync(0xffffffffu, mh[0], (g << 2) | blk);
-        const float m1 = __shfl_sync(0xffffffffu, mh[1], (g << 2) | blk);
-        // packed bytes of block blk, lane t: chunk 2 blk + t/2 of the row, at
-        // position chunk ^ (row mod 8) (128-byte swizzle), 8 bytes
-        const uint32_t coff = ((uint32_t)((2 * blk + (t >> 1)) ^ pg) << 4) + (uint32_t)(t & 1) * 8u;
-        const uint32_t r0 = wsb + (uint32_t)(warp * 16 + pg) * 128u + coff;
-        const uint2 wg = lds64(r0), wg8 = lds64(r0 + 8 * 128);
+          const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          const float m0 = __shfl_sync(0xffffffffu, mh[0], (g << 2) | blk);
+          const float m1 = __shfl_sync(0xffffffffu, mh[1], (g << 2) | blk);
+          const uint32_t coff = ((uint32_t)((2 * blk + (t >> 1)) ^ pg) << 4) + (uint32_t)(t & 1) * 8u;
+          const uint32_t r0 = wsb + (uint32_t)(warp * 16 + pg) * 128u + coff;
+          const uint2 wg = lds64(r0), wg8 = lds64(r0 + 8 * 128);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          // MMA j takes k = 16 t + 4 j + [0, 4) of this block: bytes 2j and 2j+1
-          const uint32_t wa = (j >> 1) ? wg.y : wg.x, wb = (j >> 1) ? wg8.y : wg8.x;
-          const uint32_t s0 = 0x5504u | ((uint32_t)((j & 1) * 2) << 4), s1 = s0 + 0x10u;
-          const uint32_t a0 = w_hat_pair(tab + prmt(wa, lanebase, s0), m0);
-          const uint32_t a2 = w_hat_pair(tab + prmt(wa, lanebase, s1), m0);
-          const uint32_t a1 = w_hat_pair(tab + prmt(wb, lanebase, s0), m1);
-          const uint32_t a3 = w_hat_pair(tab + prmt(wb, lanebase, s1), m1);
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) mma16816(acc[mt], a0, a1, a2, a3, xw[mt][2 * j], xw[mt][2 * j + 1]);
+          for (int j = 0; j < 4; ++j) {
+            // MMA j takes K values 16 t + 4 j + [0, 4): bytes 2j and 2j + 1
+            const uint32_t wa = (j >> 1) ? wg.y : wg.x, wb = (j >> 1) ? wg8.y : wg8.x;
+            const uint32_t s0 = 0x5504u | ((uint32_t)((j & 1) * 2) << 4), s1 = s0 + 0x10u;
+            const uint32_t a0 = w_hat_pair(tab + prmt(wa, lanebase, s0), m0);
+            const uint32_t a2 = w_hat_pair(tab + prmt(wa, lanebase, s1), m0);
+            const uint32_t a1 = w_hat_pair(tab + prmt(wb, lanebase, s0), m1);
+            const uint32_t a3 = w_hat_pair(tab + prmt(wb, lanebase, s1), m1);
+            mma16816(acc[0], a0, a1, a2, a3, xw[2 * j], xw[2 * j + 1]);
+          }
         }
-      }
+      } else {
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) {
+          const int sg = blk ^ t;
+          uint32_t xw[MT][8];
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const uint32_t rowa = xsb + (uint32_t)(t * XR * 128 + (mt * 8 + xg) * 128);
+            const uint4 x0 = lds128(rowa + ((uint32_t)((2 * sg) ^ xg) << 4));
+            const uint4 x1 = lds128(rowa + ((uint32_t)((2 * sg + 1) ^ xg) << 4));
+            xw[mt][0] = x0.x; xw[mt][1] = x0.y; xw[mt][2] = x0.z; xw[mt][3] = x0.w;
+            xw[mt][4] = x1.x; xw[mt][5] = x1.y; xw[mt][6] = x1.z; xw[mt][7] = x1.w;
+          }
+          const uint32_t coff = ((uint32_t)((2 * t + (sg >> 1)) ^ pg) << 4) + (uint32_t)(sg & 1) * 8u;
+          const uint32_t r0 = wsb + (uint32_t)(warp * 16 + pg) * 128u + coff;
+          const uint2 wg = lds64(r0), wg8 = lds64(r0 + 8 * 128);
+          // MMA j takes K values 16 sg + 4 j + [0, 4): bytes 2j and 2j + 1 of the piece
+          uint32_t af[4][4];
+          lookup8(wg.x, TL0, TH0, af[0][0], af[0][2], af[1][0], af[1][2]);
+          lookup8(wg.y, TL0, TH0, af[2][0], af[2][2], af[3][0], af[3][2]);
+          lookup8(wg8.x, TL1, TH1, af[0][1], af[0][3], af[1][1], af[1][3]);
+          lookup8(wg8.y, TL1, TH1, af[2][1], af[2][3], af[3][1], af[3][3]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+              mma16816(acc[mt], af[j][0], af[j][1], af[j][2], af[j][3], xw[mt][2 * j], xw[mt][2 * j + 1]);
+        }
       }
     }
     // stage s has been read by this warp; the last warp to finish with it
@@ -663,7 +707,8 @@ k_decode_finish(const __grid_constant__ FinArgs a) {
   // The next call may start once this kernel has waited for the stream kernel
   // (and so for every grid before it).  When the stream kernel has a CTA on
   // every SM it may start at once instead: its CTAs (too large to share an SM
-  // with a stream CTA) then take each SM only when this call's stream CTA on
+  // with a stream CTA: their registers alone exceed the SM's, see
+  // kStreamRegs) then take each SM only when this call's stream CTA on
   // it exits, which that CTA does only after the call before this one has
   // completed; so whatever the next call starts with still sees every call
   // before this one complete, as it would otherwise.
@@ -681,9 +726,14 @@ k_decode_finish(const __grid_constant__ FinArgs a) {
       const int zg = (FIN_WARPS * 32) / MR4, i = tid % MR4, zc = tid / MR4;
       float4 sacc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       if (zc < zg) {
+        // a counted loop (the trip count known on entry), so the unrolled
+        // loads are issued together rather than one per loop-exit test
+        const int cnt = (a.nx - zc + zg - 1) / zg;
+        const float4 *src = reinterpret_cast<const float4 *>(a.xap + (int64_t)zc * TSL * R) + i;
+        const int64_t step = (int64_t)zg * TSL * R / 4;
 #pragma unroll 8
-        for (int z = zc; z < a.nx; z += zg) {
-          const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.xap + (int64_t)z * TSL * R) + i);
+        for (int u = 0; u < cnt; ++u) {
+          const float4 v = __ldcg(src + u * step);
           sacc.x += v.x;
           sacc.y += v.y;
           sacc.z += v.z;

@@ -105,8 +105,8 @@ def test_decode_chained_calls_and_any_workspace_contents(ql):
     """Layer chains on one stream: the second call reads the first call's Y (it
     must wait for it) while its weight may stream early.  Results must equal
     the same calls made one at a time with a synchronisation in between, on a
-    workspace filled with arbitrary bytes (the arrival counters carry a call
-    stamp, so no initialisation is needed)."""
+    workspace filled with arbitrary bytes (every workspace word a call reads
+    was written by that call first, so no initialisation is needed)."""
     from bit_nf4_quantized_38_b300.workloads import normal_bf16
     dev = torch.device("cuda")
     K0, N1, N2, r = 1024, 2048, 1024, 16
@@ -133,8 +133,8 @@ def test_decode_chained_calls_and_any_workspace_contents(ql):
 
 
 def test_decode_graph_replays_reuse_the_workspace(ql):
-    """A captured sequence of decode calls on one workspace (the same call
-    stamps every replay) gives the eager results on every replay."""
+    """A captured sequence of decode calls on one workspace (the same
+    workspace halves every replay) gives the eager results on every replay."""
     from bit_nf4_quantized_38_b300.workloads import normal_bf16
     dev = torch.device("cuda")
     shapes = [(1024, 1024, 1), (3072, 1024, 16), (1024, 3072, 9)]
