@@ -460,14 +460,12 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     for (int k = 0; k < 2; ++k)
       mh[k] = a.dq ? __fadd_rn(__fmul_rn(dq_code_value((int8_t)pre.c[k], a.dqt), pre.b[k]), mu) : pre.a[k];
     pre = load_pre(i + PD);
-    // two or four token tiles: the lane's two rows' dequantized values in
-    // block t (TL0/TH0: row pg, TL1/TH1: row pg + 8), formed while the stage
-    // may still be loading
+    // the lane's rows' dequantized values in block t (TL0/TH0: row pg, two or
+    // four token tiles only; TL1/TH1: row pg + 8), formed while the stage may
+    // still be loading
     uint32_t TL0[4], TH0[4], TL1[4], TH1[4];
-    if constexpr (MT > 1) {
-      w_hat_planes(a.q, mh[0], TL0, TH0);
-      w_hat_planes(a.q, mh[1], TL1, TH1);
-    }
+    if constexpr (MT > 1) w_hat_planes(a.q, mh[0], TL0, TH0);
+    w_hat_planes(a.q, mh[1], TL1, TH1);
 
     bool landed = false;
     if (!*abort_v)
@@ -475,16 +473,15 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     const bool ok = __all_sync(0xffffffffu, landed);
     if (ok) {
       const uint32_t wsb = stages + (uint32_t)(s * SB), xsb = wsb + W_BYTES;
-      // Two or four token tiles, step blk: lane t takes K values 16 sg ..
-      // 16 sg + 15 of block t, sg = blk ^ t, and its X fragments the same K
-      // values (the reduction order is a permutation of the unit's K, the
-      // same for both operands).  The packed bytes are 8-byte piece sg of
-      // block t's 32 (16-byte chunk 2 t + sg / 2 of the row, at chunk ^ (row
-      // mod 8)); X is chunks 2 sg, 2 sg + 1 of block t's 128-byte token row,
-      // at chunk ^ (row mod 8).  sg is a Latin square in (t, blk), so no load
-      // of a step conflicts on a bank.  Past the row's last block (a ragged
-      // unit) the weight and X boxes are zero filled, so those lanes add zero
-      // products.
+      // Step blk: lane t takes K values 16 sg .. 16 sg + 15 of block t, sg =
+      // blk ^ t, and its X fragments the same K values (the reduction order
+      // is a permutation of the unit's K, the same for both operands).  The
+      // packed bytes are 8-byte piece sg of block t's 32 (16-byte chunk
+      // 2 t + sg / 2 of the row, at chunk ^ (row mod 8)); X is chunks 2 sg,
+      // 2 sg + 1 of block t's 128-byte token row, at chunk ^ (row mod 8).  sg
+      // is a Latin square in (t, blk), so no load of a step conflicts on a
+      // bank.  Past the row's last block (a ragged unit) the weight and X
+      // boxes are zero filled, so those lanes add zero products.
       if constexpr (MT == 4) {
         // 32 tokens: the weights of a step (its 16 A fragments) are formed
         // once and used for two pairs of token tiles in turn, so their cost is
@@ -521,34 +518,35 @@ k_decode_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
           }
         }
       } else if constexpr (MT == 1) {
-        // One token tile: few X loads, so the level table in shared memory
-        // (8 B per lookup) costs less than the register planes' byte permutes.
-        // Step blk is block blk of the unit and lane t takes its K values
-        // 16 t .. 16 t + 15 (chunks 2 blk + t / 2 of the packed row, 2t and
-        // 2t + 1 of the X row); the block constants come from lane 4 g + blk.
+        // One token tile: few X loads, so shared memory has room for half of
+        // the weights' lookups.  Row pg takes its levels from the shared-memory
+        // table (one 64-bit load per packed byte, times the lane's block
+        // constant), row pg + 8 from the register planes: the two resources
+        // share the work.
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {
-          if (b * 4 + blk >= nb_row) break;
-          const uint32_t rowa = xsb + (uint32_t)(blk * XR * 128 + xg * 128);
-          const uint4 x0 = lds128(rowa + ((uint32_t)((2 * t) ^ xg) << 4));
-          const uint4 x1 = lds128(rowa + ((uint32_t)((2 * t + 1) ^ xg) << 4));
+          const int sg = blk ^ t;
+          const uint32_t rowa = xsb + (uint32_t)(t * XR * 128 + xg * 128);
+          const uint4 x0 = lds128(rowa + ((uint32_t)((2 * sg) ^ xg) << 4));
+          const uint4 x1 = lds128(rowa + ((uint32_t)((2 * sg + 1) ^ xg) << 4));
           const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-          const float m0 = __shfl_sync(0xffffffffu, mh[0], (g << 2) | blk);
-          const float m1 = __shfl_sync(0xffffffffu, mh[1], (g << 2) | blk);
-          const uint32_t coff = ((uint32_t)((2 * blk + (t >> 1)) ^ pg) << 4) + (uint32_t)(t & 1) * 8u;
+          const uint32_t coff = ((uint32_t)((2 * t + (sg >> 1)) ^ pg) << 4) + (uint32_t)(sg & 1) * 8u;
           const uint32_t r0 = wsb + (uint32_t)(warp * 16 + pg) * 128u + coff;
           const uint2 wg = lds64(r0), wg8 = lds64(r0 + 8 * 128);
+          uint32_t af[4][4];
+          lookup8(wg8.x, TL1, TH1, af[0][1], af[0][3], af[1][1], af[1][3]);
+          lookup8(wg8.y, TL1, TH1, af[2][1], af[2][3], af[3][1], af[3][3]);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            // MMA j takes K values 16 t + 4 j + [0, 4): bytes 2j and 2j + 1
-            const uint32_t wa = (j >> 1) ? wg.y : wg.x, wb = (j >> 1) ? wg8.y : wg8.x;
+            // MMA j takes K values 16 sg + 4 j + [0, 4): bytes 2j and 2j + 1 of the piece
+            const uint32_t wa = (j >> 1) ? wg.y : wg.x;
             const uint32_t s0 = 0x5504u | ((uint32_t)((j & 1) * 2) << 4), s1 = s0 + 0x10u;
-            const uint32_t a0 = w_hat_pair(tab + prmt(wa, lanebase, s0), m0);
-            const uint32_t a2 = w_hat_pair(tab + prmt(wa, lanebase, s1), m0);
-            const uint32_t a1 = w_hat_pair(tab + prmt(wb, lanebase, s0), m1);
-            const uint32_t a3 = w_hat_pair(tab + prmt(wb, lanebase, s1), m1);
-            mma16816(acc[0], a0, a1, a2, a3, xw[2 * j], xw[2 * j + 1]);
+            af[j][0] = w_hat_pair(tab + prmt(wa, lanebase, s0), mh[0]);
+            af[j][2] = w_hat_pair(tab + prmt(wa, lanebase, s1), mh[0]);
           }
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            mma16816(acc[0], af[j][0], af[j][1], af[j][2], af[j][3], xw[2 * j], xw[2 * j + 1]);
         }
       } else {
 #pragma unroll
